@@ -1,0 +1,474 @@
+"""Pins for the fp64 CPU oracle: each test checks the oracle against something other
+than itself -- hand-worked fixtures, brute force, closed forms, or a library routine
+(numpy argmax, torch scaled_dot_product_attention) in a special case the method
+reduces to.  CPU only."""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_speculative_decoding_jf_gb300 import workloads as wl
+from conftest import GOLDEN
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def closure(parent):
+    """Ancestor-or-self relation by boolean reflexive-transitive closure of the parent
+    adjacency (repeated squaring) -- a different computation from walking parents."""
+    N = len(parent)
+    A = np.zeros((N, N), dtype=bool)
+    for i in range(1, N):
+        A[i, parent[i]] = True
+    R = A | np.eye(N, dtype=bool)
+    while True:
+        R2 = (R.astype(np.int64) @ R.astype(np.int64)) > 0
+        if (R2 == R).all():
+            return R
+        R = R2
+
+
+def pack_rows(R):
+    """Pack boolean rows LSB-first into little-endian uint64 words (numpy packbits)."""
+    N = R.shape[1]
+    W = (N + 63) // 64
+    padded = np.zeros((R.shape[0], W * 64), dtype=bool)
+    padded[:, :N] = R
+    return np.packbits(padded, axis=1, bitorder="little").view("<u8")
+
+
+def all_topological_trees(N):
+    for choice in itertools.product(*[range(i) for i in range(1, N)]):
+        yield np.array((-1,) + choice, dtype=np.int32)
+
+
+def random_tree(rng, N):
+    p = np.full(N, -1, dtype=np.int32)
+    for i in range(1, N):
+        p[i] = rng.integers(0, i)
+    return p
+
+
+def f32(bits):
+    return wl.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def logical_kv(w, b, g):
+    """Contiguous K, V [P_b + N][D] (float64) for sequence b, kv-head g, gathered from
+    the pool with numpy fancy indexing through the block table."""
+    L = int(w.prefix_len[b]) + w.N
+    t = np.arange(L)
+    pages = w.block_table[b][t // w.page]
+    slots = t % w.page
+    k = f32(w.k_cache[pages, slots, g, :])
+    v = f32(w.v_cache[pages, slots, g, :])
+    return k, v
+
+
+def sdpa(q, k, v, scale, mask=None):
+    """torch fp64 scaled_dot_product_attention for one head: q [n][D], k/v [L][D]."""
+    tq = torch.from_numpy(q)[None, None]
+    tk = torch.from_numpy(k)[None, None]
+    tv = torch.from_numpy(v)[None, None]
+    m = None if mask is None else torch.from_numpy(mask)[None, None]
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=m, scale=scale)
+    return out[0, 0].numpy()
+
+
+def tiny(B=1, N=8, Hq=4, Hkv=2, D=16, P=20, tree="random", seed=0, permute=False,
+         parent=None, V=64):
+    rng = np.random.default_rng(seed + 1000)
+    if parent is None:
+        if tree == "random":
+            parent = np.stack([random_tree(rng, N) for _ in range(B)])
+            tree_kind = "chain"
+        else:
+            parent, tree_kind = None, tree
+    if parent is not None:
+        return wl.make_workload("tiny", B, N, Hq, Hkv, D, V, P, parent=np.asarray(parent),
+                                permute_pages=permute, seed=seed, logits_dtype="f32")
+    return wl.make_workload("tiny", B, N, Hq, Hkv, D, V, P, tree=tree_kind,
+                            permute_pages=permute, seed=seed, logits_dtype="f32")
+
+
+def read_golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.rstrip("\n") for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# ----------------------------------------------------------------------------- mask
+
+def test_mask_golden_hand_worked():
+    lines = read_golden("mask_7node.txt")
+    parent = np.array([int(x) for x in lines[0].split(":")[1].split()], dtype=np.int32)
+    P = int(lines[1].split(":")[1])
+    mask, depth, pos = oracle.tree_mask(parent[None], np.array([P], dtype=np.int32))
+    for ln in lines[2:]:
+        node, vis, dep, ps = [s.strip() for s in ln.split(":")]
+        i = int(node)
+        want = 0
+        for j in vis.split():
+            want |= 1 << int(j)
+        assert int(mask[0, i, 0]) == want
+        assert depth[0, i] == int(dep) and pos[0, i] == int(ps)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 6])
+def test_mask_exhaustive_small_trees_vs_closure(N):
+    for parent in all_topological_trees(N):
+        mask, depth, pos = oracle.tree_mask(parent[None], np.array([7], dtype=np.int32))
+        R = closure(parent)
+        assert (mask[0] == pack_rows(R)).all()
+        assert (depth[0] == R.sum(1) - 1).all()
+        assert (pos[0] == 7 + R.sum(1) - 1).all()
+
+
+@pytest.mark.parametrize("N", [12, 64, 65, 130, 256])
+def test_mask_random_trees_vs_closure_multiword(N):
+    rng = np.random.default_rng(N)
+    parents = np.stack([random_tree(rng, N) for _ in range(3)] + [wl.tree_chain(N)])
+    P = np.array([0, 5, 16, 1000], dtype=np.int32)
+    mask, depth, pos = oracle.tree_mask(parents, P)
+    for b in range(len(parents)):
+        R = closure(parents[b])
+        assert (mask[b] == pack_rows(R)).all()   # includes zero padding past N
+        assert (pos[b] == P[b] + depth[b]).all()
+
+
+def test_mask_invariants_chain_star():
+    N = 70
+    m, d, _ = oracle.tree_mask(wl.tree_chain(N)[None], np.zeros(1, np.int32))
+    bits = np.unpackbits(m[0].view(np.uint8), axis=1, bitorder="little")[:, :N].astype(bool)
+    assert (bits == np.tril(np.ones((N, N), dtype=bool))).all()
+    assert (d[0] == np.arange(N)).all()
+    m, d, _ = oracle.tree_mask(wl.tree_star(N)[None], np.zeros(1, np.int32))
+    bits = np.unpackbits(m[0].view(np.uint8), axis=1, bitorder="little")[:, :N].astype(bool)
+    want = np.eye(N, dtype=bool)
+    want[:, 0] = True
+    assert (bits == want).all()
+
+
+def test_mask_parent_recurrence_and_popcount():
+    rng = np.random.default_rng(5)
+    parent = random_tree(rng, 200)
+    m, d, _ = oracle.tree_mask(parent[None], np.zeros(1, np.int32))
+    for i in range(1, 200):
+        bit = np.zeros(4, dtype=np.uint64)
+        bit[i // 64] = np.uint64(1) << np.uint64(i % 64)
+        assert (m[0, i] == (m[0, parent[i]] | bit)).all()
+        pc = sum(bin(int(x)).count("1") for x in m[0, i])
+        assert pc == d[0, i] + 1
+
+
+def test_mask_rejects_non_topological_tree():
+    with pytest.raises(oracle.OracleError):
+        oracle.tree_mask(np.array([[-1, 2, 0]], np.int32), np.zeros(1, np.int32))
+    with pytest.raises(oracle.OracleError):
+        oracle.tree_mask(np.array([[0, 0]], np.int32), np.zeros(1, np.int32))
+
+
+# ----------------------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("P,N", [(0, 8), (20, 8), (37, 13), (5, 40)])
+def test_attention_chain_equals_causal_sdpa(P, N):
+    w = tiny(N=N, P=P, tree="chain", Hq=4, Hkv=2, D=16, seed=P + N)
+    out, lse = oracle.tree_attention(w)
+    G = w.G
+    for h in range(w.Hq):
+        k, v = logical_kv(w, 0, h // G)
+        q = f32(w.q[0, :, h, :])
+        causal = np.tril(np.ones((N, P + N), dtype=bool), k=P)   # bottom-right causal
+        ref = sdpa(q, k, v, w.scale, causal)
+        np.testing.assert_allclose(out[0, :, h, :], ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("P", [1, 17, 64])
+def test_attention_single_node_equals_decode_sdpa(P):
+    w = tiny(N=1, P=P, tree="chain", Hq=8, Hkv=2, D=32, seed=P)
+    out, lse = oracle.tree_attention(w)
+    for h in range(w.Hq):
+        k, v = logical_kv(w, 0, h // w.G)
+        q = f32(w.q[0, :, h, :])
+        np.testing.assert_allclose(out[0, :, h, :], sdpa(q, k, v, w.scale), rtol=1e-12, atol=1e-13)
+        s = (q @ k.T)[0] * w.scale
+        np.testing.assert_allclose(lse[0, h, 0], np.logaddexp.reduce(s), rtol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_attention_root_path_brute_force(seed):
+    """Each node's output equals plain attention over prefix + its root path alone
+    (the branch factorisation of the draft distribution, explainer §2)."""
+    rng = np.random.default_rng(seed)
+    N, P = int(rng.integers(2, 14)), int(rng.integers(0, 40))
+    w = tiny(B=2, N=N, P=P, Hq=4, Hkv=1, D=8, seed=seed, permute=bool(seed % 2))
+    out, lse = oracle.tree_attention(w)
+    for b in range(w.B):
+        for i in range(N):
+            path, a = [], i
+            while a >= 0:
+                path.append(a)
+                a = int(w.parent[b, a])
+            keys = list(range(P)) + [P + j for j in sorted(path)]
+            for h in range(w.Hq):
+                k, v = logical_kv(w, b, h // w.G)
+                q = f32(w.q[b, i, h, :])[None]
+                ref = sdpa(q, k[keys], v[keys], w.scale)[0]
+                np.testing.assert_allclose(out[b, i, h], ref, rtol=1e-12, atol=1e-13)
+
+
+def _relabel(parent, rng):
+    """Random topological relabelling: returns perm with new_id = perm[old_id]."""
+    N = len(parent)
+    children = [[] for _ in range(N)]
+    for i in range(1, N):
+        children[parent[i]].append(i)
+    perm = np.empty(N, dtype=np.int64)
+    ready, nxt = [0], 0
+    while ready:
+        x = ready.pop(int(rng.integers(0, len(ready))))
+        perm[x] = nxt
+        nxt += 1
+        ready.extend(children[x])
+    return perm
+
+
+def test_attention_sibling_renumbering_equivariant():
+    rng = np.random.default_rng(11)
+    N, P = 12, 9
+    w = tiny(N=N, P=P, Hq=2, Hkv=1, D=8, seed=3)
+    perm = _relabel(w.parent[0], rng)
+    w2 = tiny(N=N, P=P, Hq=2, Hkv=1, D=8, seed=3)
+    newp = np.full(N, -1, np.int32)
+    for i in range(1, N):
+        newp[perm[i]] = perm[w.parent[0, i]]
+    w2.parent = newp[None].copy()
+    w2.q = w.q.copy()
+    w2.q[0, perm] = w.q[0]
+    for c_src, c_dst in ((w.k_cache, w2.k_cache), (w.v_cache, w2.v_cache)):
+        for j in range(N):
+            t_old, t_new = P + j, P + perm[j]
+            po, pn = w.block_table[0, t_old // 16], w2.block_table[0, t_new // 16]
+            c_dst[pn, t_new % 16] = c_src[po, t_old % 16]
+    o1, l1 = oracle.tree_attention(w)
+    o2, l2 = oracle.tree_attention(w2)
+    np.testing.assert_allclose(o2[0, perm], o1[0], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l2[0][:, perm], l1[0], rtol=1e-12)
+
+
+def test_attention_masked_weights_exactly_zero():
+    w = tiny(N=16, P=10, Hq=2, Hkv=1, D=8, seed=7)
+    R = closure(w.parent[0])
+    for h in range(w.Hq):
+        probs = oracle.attention_probs(w, 0, h)
+        assert (probs[:, :10] > 0).all()
+        tree = probs[:, 10:]
+        assert (tree[~R] == 0.0).all()
+        assert (tree[R] > 0).all()
+        np.testing.assert_allclose(probs.sum(1), 1.0, rtol=1e-13)
+
+
+def test_attention_closed_form_single_root_no_prefix():
+    w = tiny(N=1, P=0, Hq=4, Hkv=2, D=16, tree="chain", seed=2)
+    out, lse = oracle.tree_attention(w)
+    for h in range(4):
+        g = h // 2
+        v = f32(w.v_cache[w.block_table[0, 0], 0, g])
+        k = f32(w.k_cache[w.block_table[0, 0], 0, g])
+        assert (out[0, 0, h] == v).all()                       # exactly v_root
+        assert lse[0, h, 0] == pytest.approx(w.scale * float(f32(w.q[0, 0, h]) @ k), rel=1e-14)
+
+
+def test_attention_closed_form_equal_keys_gives_mean_of_visible_values():
+    w = tiny(N=10, P=7, Hq=2, Hkv=1, D=8, seed=4)
+    w.k_cache[:] = w.k_cache[0, 0]            # every key identical -> uniform weights
+    out, _ = oracle.tree_attention(w)
+    R = closure(w.parent[0])
+    k, v = logical_kv(w, 0, 0)
+    for i in range(10):
+        vis = list(range(7)) + [7 + j for j in np.nonzero(R[i])[0]]
+        np.testing.assert_allclose(out[0, i, 0], v[vis].mean(0), rtol=1e-12, atol=1e-14)
+
+
+def test_attention_gqa_equals_mha_with_duplicated_kv_heads():
+    w1 = tiny(N=6, P=11, Hq=2, Hkv=1, D=8, seed=9)
+    w2 = tiny(N=6, P=11, Hq=2, Hkv=2, D=8, seed=9)
+    w2.parent = w1.parent.copy()
+    w2.q = w1.q.copy()
+    w2.k_cache = np.repeat(w1.k_cache, 2, axis=2)
+    w2.v_cache = np.repeat(w1.v_cache, 2, axis=2)
+    w2.block_table = w1.block_table.copy()
+    o1, l1 = oracle.tree_attention(w1)
+    o2, l2 = oracle.tree_attention(w2)
+    assert (o1 == o2).all() and (l1 == l2).all()
+
+
+def test_attention_page_permutation_invariant():
+    a = tiny(B=2, N=9, P=45, Hq=4, Hkv=2, D=8, seed=21, permute=False)
+    b = tiny(B=2, N=9, P=45, Hq=4, Hkv=2, D=8, seed=21, permute=True)
+    assert not (a.block_table == b.block_table).all()
+    # put a's logical rows into b's pool layout
+    for bb in range(2):
+        L = int(a.prefix_len[bb]) + a.N
+        for t in range(L):
+            pa, pb = a.block_table[bb, t // 16], b.block_table[bb, t // 16]
+            b.k_cache[pb, t % 16] = a.k_cache[pa, t % 16]
+            b.v_cache[pb, t % 16] = a.v_cache[pa, t % 16]
+    b.q, b.parent = a.q, a.parent
+    oa, la = oracle.tree_attention(a)
+    ob, lb = oracle.tree_attention(b)
+    assert (oa == ob).all() and (la == lb).all()
+
+
+def test_attention_rows_sample_matches_full():
+    w = tiny(B=2, N=7, P=30, Hq=4, Hkv=2, D=8, seed=5)
+    out, lse = oracle.tree_attention(w)
+    rb, rh, ri = np.array([1, 0, 1]), np.array([3, 0, 2]), np.array([6, 0, 4])
+    o, l = oracle.tree_attention_rows(w, rb, rh, ri)
+    for n in range(3):
+        assert (o[n] == out[rb[n], ri[n], rh[n]]).all()
+        assert l[n] == lse[rb[n], rh[n], ri[n]]
+
+
+# ----------------------------------------------------------------------------- verify
+
+def _golden_argmax_rows():
+    rows = []
+    for ln in read_golden("argmax_rows.txt"):
+        idx, vals = ln.split(":")
+        rows.append((int(idx), [float(x) for x in vals.split()]))
+    return rows
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_argmax_golden_ties_and_signed_zero(dtype):
+    for idx, vals in _golden_argmax_rows():
+        x = np.array(vals, dtype=np.float32)
+        if dtype == "bf16":
+            x = wl.to_bf16_bits(x)
+            assert (wl.bf16_bits_to_f32(x) == np.array(vals, dtype=np.float32)).all()
+        assert oracle.argmax(x[None], dtype)[0] == idx
+
+
+def test_argmax_matches_numpy_first_occurrence():
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal((64, 5000)) * 2).astype(np.float32)
+    x[3, 100] = x[3, 4000] = 50.0      # tie: first occurrence
+    assert (oracle.argmax(x, "f32") == np.argmax(x, axis=1)).all()
+    xb = wl.to_bf16_bits(x)            # bf16 rounding creates many ties
+    assert (oracle.argmax(xb, "bf16") == np.argmax(wl.bf16_bits_to_f32(xb), axis=1)).all()
+
+
+def _golden_walk_cases():
+    lines = read_golden("verify_walk.txt")
+    cases, cur = [], None
+    for ln in lines:
+        key, val = ln.split(":", 1)
+        key = key.strip()
+        if key == "case":
+            cur = {"name": val.strip()}
+            cases.append(cur)
+        elif key == "expect":
+            a, p, bo = val.split("|")
+            cur["expect"] = (int(a), [int(x) for x in p.split()], int(bo))
+        else:
+            cur[key] = np.array([int(x) for x in val.split()], dtype=np.int32)
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_walk_cases(), ids=lambda c: c["name"])
+def test_tree_walk_golden(case):
+    acc, path, bonus = oracle.tree_walk(case["argmax"][None], case["draft"][None],
+                                        case["parent"][None])
+    a, p, bo = case["expect"]
+    assert acc[0] == a and list(path[0]) == p and bonus[0] == bo
+
+
+def _brute_force_walk(argmax, draft, parent):
+    """Enumerate every root path, keep the all-accepted ones, take the longest and
+    among those the lexicographically smallest sequence of node ids."""
+    N = len(parent)
+    best = [0]
+    for n in range(N):
+        path, a = [], n
+        while a >= 0:
+            path.append(a)
+            a = int(parent[a])
+        path = path[::-1]
+        ok = all(draft[c] == argmax[parent[c]] for c in path[1:])
+        if ok and (len(path) > len(best) or (len(path) == len(best) and path < best)):
+            best = path
+    return len(best) - 1, best + [-1] * (N - len(best)), int(argmax[best[-1]])
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_tree_walk_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    N = int(rng.integers(1, 13))
+    parent = random_tree(rng, N)
+    argmax = rng.integers(0, 3, N).astype(np.int32)
+    draft = rng.integers(0, 3, N).astype(np.int32)
+    acc, path, bonus = oracle.tree_walk(argmax[None], draft[None], parent[None])
+    a, p, bo = _brute_force_walk(argmax, draft, parent)
+    assert acc[0] == a and list(path[0]) == p and bonus[0] == bo
+
+
+def test_tree_walk_accept_len_invariant_under_renumbering():
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        N = 12
+        parent = random_tree(rng, N)
+        argmax = rng.integers(0, 2, N).astype(np.int32)
+        draft = rng.integers(0, 2, N).astype(np.int32)
+        perm = _relabel(parent, rng)
+        p2 = np.full(N, -1, np.int32)
+        a2, d2 = np.empty(N, np.int32), np.empty(N, np.int32)
+        for i in range(N):
+            a2[perm[i]], d2[perm[i]] = argmax[i], draft[i]
+            if i:
+                p2[perm[i]] = perm[parent[i]]
+        x = oracle.tree_walk(argmax[None], draft[None], parent[None])
+        y = oracle.tree_walk(a2[None], d2[None], p2[None])
+        assert x[0][0] == y[0][0]
+
+
+def test_chain5_forcing_gives_accept_len_five():
+    w = wl.make_workload("chain5", 1, 16, 4, 1, 16, 4096, 32, tree="chain",
+                         forcing="chain5", seed=3)
+    am, acc, path, bonus = oracle.tree_verify(w)
+    assert acc[0] == 5 and list(path[0][:7]) == [0, 1, 2, 3, 4, 5, -1]
+    assert bonus[0] == am[0, 5]
+
+
+# ----------------------------------------------------------------------------- inputs
+
+def test_generators_are_deterministic():
+    a = wl.config("c1_tiny_random16")
+    b = wl.config("c1_tiny_random16")
+    for f in ("parent", "q", "k_cache", "v_cache", "block_table", "logits", "draft"):
+        assert (getattr(a, f) == getattr(b, f)).all()
+
+
+def test_best_first_tree_shape():
+    rng = np.random.default_rng(0)
+    parent, tokens = wl.tree_best_first(rng, 256, 151936)
+    assert parent[0] == -1 and all(0 <= parent[i] < i for i in range(1, 256))
+    depth = np.zeros(256, int)
+    for i in range(1, 256):
+        depth[i] = depth[parent[i]] + 1
+    assert depth.max() <= 15
+    for p in set(parent[1:].tolist()):
+        kids = tokens[parent == p]
+        assert len(set(kids.tolist())) == len(kids)      # distinct candidate tokens
+
+
+def test_c1_config_shape_and_forcing():
+    w = wl.config("c1_tiny_random16")
+    assert w.q.shape == (1, 16, 4, 64) and w.k_cache.shape == (9, 16, 1, 64)
+    _, depth, _ = oracle.tree_mask(w.parent, w.prefix_len)
+    assert depth.max() <= 6
+    am = oracle.argmax(w.logits, "f32")
+    forced = [c for c in range(1, 16) if w.draft[0, c] == am[0, w.parent[0, c]]]
+    assert len(forced) >= 3
