@@ -1,0 +1,174 @@
+/*
+ * jf.h -- C ABI of the GB300 (sm_103a) tree-speculative-decoding hot path:
+ *   tree-causal attention mask  ->  tree-causal paged attention  ->  greedy tree verify.
+ *
+ * Source of the operations: "JetFlow: Breaking the Scaling Ceiling of Speculative
+ * Decoding with Parallel Tree Drafting" (gist.science explainer, technical summary §2
+ * "Method" -- tree-causal attention mask, branch factorisation, best-first tree
+ * construction; §3 -- paged attention kernel with tree-mask staging used for tree
+ * verification; §4 -- accepted tokens tau), and the qxai.app commentary on the same
+ * paper (section "まず、何が問題なのか": the large model checks the drafted candidates
+ * together and keeps the part it agrees with).
+ *
+ * Conventions shared by every call:
+ *  - Every pointer argument except `stream` is a DEVICE pointer owned by the caller;
+ *    the library never frees, keeps or allocates caller memory.  Scalars are host values.
+ *  - Calls only enqueue kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and return; they never synchronise.  Several calls may be captured in a
+ *    CUDA graph.
+ *  - Host-visible problems (null pointer, unsupported size, misalignment, small
+ *    workspace) are returned synchronously and nothing is launched.
+ *  - Data-dependent problems (a malformed tree, a page id outside the pool, a token
+ *    outside the vocabulary, a prefix longer than the block table allows) are OR-ed as
+ *    JF_DEVERR_* bits into *dev_err (a device int32 the caller zeroes and reads after
+ *    its next synchronisation; may be NULL to skip reporting).  The affected outputs are
+ *    then unspecified, but every access stays in bounds.  No kernel traps or asserts.
+ *  - A kernel wait that exceeds its time limit (about one second) sets
+ *    JF_DEVERR_TIMEOUT and the kernel returns instead of hanging.
+ *  - Node numbering: parent[b][0] == -1 (the root) and 0 <= parent[b][i] < i.
+ */
+#ifndef JF_H_
+#define JF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* jf_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  JF_OK = 0,
+  JF_ERR_INVALID_ARGUMENT = 1,    /* null pointer, non-positive size, bad dtype      */
+  JF_ERR_INVALID_TREE = 2,        /* reserved: tree errors are reported on device      */
+  JF_ERR_UNSUPPORTED = 3,         /* valid but unsupported shape (see each call)       */
+  JF_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the *_workspace_size value  */
+  JF_ERR_CUDA = 5,                /* a CUDA runtime call or kernel launch failed       */
+  JF_ERR_TIMEOUT = 6,             /* reserved: timeouts are reported on device         */
+  JF_ERR_MISALIGNED = 7           /* a pointer is not 16-byte aligned where required   */
+} jf_status;
+
+typedef enum { JF_DTYPE_BF16 = 0, JF_DTYPE_F32 = 1 } jf_dtype;
+
+/* Bits OR-ed into *dev_err. */
+#define JF_DEVERR_BAD_PARENT 0x1 /* parent[0] != -1 or parent[i] outside [0, i)         */
+#define JF_DEVERR_BAD_PAGE 0x2   /* block_table entry outside [0, num_pages)            */
+#define JF_DEVERR_BAD_PREFIX 0x4 /* prefix_len < 0 or prefix_len + N > max_pages * page */
+#define JF_DEVERR_BAD_TOKEN 0x8  /* draft token (non-root node) outside [0, V)          */
+#define JF_DEVERR_TIMEOUT 0x10   /* an in-kernel wait gave up after its time limit      */
+
+/* Largest tree (nodes per sequence) any call accepts. */
+#define JF_MAX_NODES 4096
+
+/* Human-readable name of a jf_status value (static storage, never NULL). */
+const char* jf_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int jf_version(void);
+
+/*
+ * jf_build_tree_mask -- tree-causal attention mask (explainer §2, "Tree-Causal Attention
+ * Mask": a draft node attends to the prefix and to its own ancestors, never to its
+ * descendants or to unrelated sibling branches).
+ *
+ *   parent     int32 [B][N]   parent[b][0] = -1, 0 <= parent[b][i] < i.
+ *   prefix_len int32 [B]      P_b, number of prefix tokens before the tree.
+ *   mask       uint64 [B][N][W], W = ceil(N / 64): bit (j & 63) of word (j >> 6) of row
+ *                             (b, i) is 1 iff node j is node i or an ancestor of i.
+ *                             Bits at j >= N are 0.
+ *   depth      int32 [B][N]   number of ancestors of i (root: 0).  May be NULL.
+ *   pos        int32 [B][N]   position id P_b + depth[b][i].          May be NULL.
+ *   dev_err    int32 [1]      JF_DEVERR_BAD_PARENT on a malformed tree. May be NULL.
+ * Limits: 1 <= N <= JF_MAX_NODES, B >= 1.  mask must be 8-byte aligned.
+ */
+jf_status jf_build_tree_mask(const int32_t* parent, const int32_t* prefix_len, int32_t B,
+                             int32_t N, uint64_t* mask, int32_t* depth, int32_t* pos,
+                             int32_t* dev_err, jf_stream_t stream);
+
+/*
+ * Bytes of device workspace jf_tree_attention needs for these sizes on the CURRENT
+ * device (split-KV partial results).  0 means no workspace is needed.  Returns
+ * (size_t)-1 if the sizes are unsupported or the device cannot be queried.
+ */
+size_t jf_tree_attention_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
+                                        int32_t D, int32_t max_pages, int32_t page_size);
+
+/*
+ * jf_tree_attention -- tree-causal paged attention (explainer §2 mask and branch
+ * factorisation q(pi(v)|x) = prod_{u in pi(v)} q(y_u | x, h_x, pi_{<u}); §3 paged
+ * attention kernel for tree verification).  For every sequence b, query head h and
+ * node i, with kv-head g = h / (Hq / Hkv):
+ *     visible keys S = {0 .. P_b-1} u {P_b + j : bit j of mask[b][i] is set}
+ *     out[b][i][h] = sum_{t in S} softmax_t(scale * q . k_t) v_t
+ *     lse[b][h][i] = log sum_{t in S} exp(scale * q . k_t)      (natural log)
+ * Key/value t of sequence b is row (page = block_table[b][t / page_size],
+ * slot = t % page_size, head g) of the paged pool; the N tree nodes' keys/values sit at
+ * logical positions P_b .. P_b + N - 1, right after the prefix.
+ *
+ *   q            bf16 [B][N][Hq][D]                    (RoPE already applied)
+ *   k_cache      bf16 [num_pages][page_size][Hkv][D]
+ *   v_cache      bf16 [num_pages][page_size][Hkv][D]
+ *   block_table  int32 [B][max_pages]; entries past ceil((P_b + N) / page_size) are
+ *                never read.
+ *   prefix_len   int32 [B]
+ *   mask         uint64 [B][N][W] as written by jf_build_tree_mask.
+ *   scale        softmax scale (usually 1 / sqrt(D)).
+ *   out          bf16 [B][N][Hq][D] (written, round-to-nearest-even).
+ *   lse          float [B][Hq][N] or NULL.
+ *   workspace    device buffer of at least jf_tree_attention_workspace_size(...) bytes
+ *                (may be NULL when that size is 0); contents need no initialisation.
+ *   dev_err      JF_DEVERR_BAD_PAGE / _BAD_PREFIX / _TIMEOUT.  May be NULL.
+ * Limits: D in {64, 128}; page_size == 16; Hq % Hkv == 0 and G = Hq / Hkv a power of
+ * two <= 128; N * G rows per kv-head split into 128-row tiles; 1 <= N <= 2048 * G / 128
+ * ... capped at JF_MAX_NODES; q, caches and out 16-byte aligned.  Others return
+ * JF_ERR_UNSUPPORTED.
+ */
+jf_status jf_tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_table, const int32_t* prefix_len,
+                            const uint64_t* mask, int32_t B, int32_t N, int32_t Hq,
+                            int32_t Hkv, int32_t D, int32_t page_size, int32_t max_pages,
+                            int32_t num_pages, float scale, void* out, float* lse,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                            jf_stream_t stream);
+
+/*
+ * Bytes of device workspace jf_tree_verify needs on the CURRENT device (per-chunk argmax
+ * partials).  Returns (size_t)-1 for unsupported sizes.
+ */
+size_t jf_tree_verify_workspace_size(int32_t B, int32_t N, int32_t V);
+
+/*
+ * jf_tree_verify -- greedy tree verification (the target checks every drafted node in
+ * one pass and keeps the longest drafted prefix it agrees with; explainer §4 counts the
+ * accepted tokens tau).
+ *   argmax[b][i] = smallest v with logits[b][i][v] == max_v logits[b][i][v]
+ *                  (values compared as real numbers, -0 == +0; inputs must be finite)
+ *   node c (c >= 1) is accepted iff draft[b][c] == argmax[b][parent[b][c]]
+ *   len(i) = 0 if i has no accepted child, else 1 + max len over accepted children
+ *   accept_len[b] = len(root)       (accepted draft nodes; the root is not counted)
+ *   path[b]       = root, then repeatedly the accepted child with the greatest len
+ *                   (ties: smallest node id); remaining entries -1
+ *   bonus[b]      = argmax[b][last node of path[b]]
+ *
+ *   logits     [B][N][V], dtype JF_DTYPE_BF16 or JF_DTYPE_F32.
+ *   draft      int32 [B][N]; draft[b][0] (the root's token) is ignored.
+ *   parent     int32 [B][N].
+ *   argmax     int32 [B][N] or NULL.
+ *   accept_len int32 [B];  path int32 [B][N];  bonus int32 [B].
+ *   workspace  at least jf_tree_verify_workspace_size(B, N, V) bytes, no initialisation.
+ *   dev_err    JF_DEVERR_BAD_PARENT / _BAD_TOKEN.  May be NULL.
+ * Limits: 1 <= N <= JF_MAX_NODES, 1 <= V < 2^31.
+ */
+jf_status jf_tree_verify(const void* logits, int32_t dtype, const int32_t* draft,
+                         const int32_t* parent, int32_t B, int32_t N, int32_t V,
+                         int32_t* argmax, int32_t* accept_len, int32_t* path, int32_t* bonus,
+                         void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                         jf_stream_t stream);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* JF_H_ */

@@ -1,0 +1,78 @@
+"""The C-ABI library loads, exports every function include/jf.h declares, and rejects bad
+host arguments before touching the GPU.  CPU only (no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tree_speculative_decoding_jf_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    names = []
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(jf_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for n in ("jf_build_tree_mask", "jf_tree_attention", "jf_tree_verify",
+              "jf_tree_attention_workspace_size", "jf_tree_verify_workspace_size",
+              "jf_status_string", "jf_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"libjf.so does not export {n}"
+
+
+def test_status_strings(lib):
+    lib.jf_status_string.restype = ctypes.c_char_p
+    assert lib.jf_status_string(0) == b"JF_OK"
+    assert lib.jf_status_string(4) == b"JF_ERR_WORKSPACE_TOO_SMALL"
+    assert lib.jf_status_string(99) == b"JF_ERR_UNKNOWN"
+
+
+def test_host_argument_validation_needs_no_gpu(lib):
+    P = ctypes.c_void_p
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails early
+    lib.jf_build_tree_mask.argtypes = [P, P, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P]
+    assert lib.jf_build_tree_mask(None, fake, 1, 4, fake, None, None, None, None) == 1
+    assert lib.jf_build_tree_mask(fake, fake, 0, 4, fake, None, None, None, None) == 1
+    assert lib.jf_build_tree_mask(fake, fake, 1, 5000, fake, None, None, None, None) == 3
+    assert lib.jf_build_tree_mask(fake, fake, 1, 4, ctypes.c_void_p(0x10004), None, None,
+                                  None, None) == 7
+    i32 = ctypes.c_int32
+    lib.jf_tree_attention.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                      ctypes.c_float, P, P, P, ctypes.c_size_t, P, P]
+    args = [fake] * 6 + [1, 16, 32, 8, 128, 16, 10, 10, 0.088, fake, None, None, 0, None, None]
+    bad_d = list(args); bad_d[10] = 96
+    assert lib.jf_tree_attention(*bad_d) == 3          # D not in {64, 128}
+    bad_g = list(args); bad_g[9] = 5
+    assert lib.jf_tree_attention(*bad_g) == 3          # Hq % Hkv != 0
+    bad_page = list(args); bad_page[11] = 32
+    assert lib.jf_tree_attention(*bad_page) == 3       # page size must be 16
+    nul = list(args); nul[0] = None
+    assert lib.jf_tree_attention(*nul) == 1
+    mis = list(args); mis[0] = ctypes.c_void_p(0x10008)
+    assert lib.jf_tree_attention(*mis) == 7
+    lib.jf_tree_verify.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P, P, P, ctypes.c_size_t,
+                                   P, P]
+    assert lib.jf_tree_verify(fake, 7, fake, fake, 1, 4, 10, None, fake, fake, fake, fake,
+                              1 << 20, None, None) == 1      # bad dtype
+    assert lib.jf_tree_verify(fake, 0, fake, fake, 1, 4, 10, None, fake, fake, fake, None,
+                              1 << 20, None, None) == 1      # missing workspace

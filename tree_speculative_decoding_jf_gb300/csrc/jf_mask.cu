@@ -1,0 +1,80 @@
+// jf_mask.cu -- tree-causal attention mask builder.
+//
+// JetFlow explainer, technical summary §2 ("Tree-Causal Attention Mask"): each draft node
+// sees the prefix and its own ancestors, never descendants or unrelated sibling branches.
+// The mask row of node i is the ancestor-or-self set packed LSB-first into W = ceil(N/64)
+// uint64 words.
+//
+// One CTA per sequence.  The sequence's parent array is staged in shared memory and
+// validated once; then each thread owns (node i, word w) pairs and walks i's ancestor
+// chain, setting the bits that fall into word w and stopping as soon as the chain drops
+// below the word's first node (ancestor ids decrease strictly).  The w == 0 walk reaches
+// the root, so it also yields depth and position id.
+#include "jf_common.cuh"
+
+namespace jf {
+namespace {
+
+constexpr int kMaskThreads = 256;
+
+__global__ void __launch_bounds__(kMaskThreads)
+    tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefix_len,
+                     int N, int W, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
+                     int32_t* __restrict__ pos, int32_t* dev_err) {
+  extern __shared__ int32_t s_par[];   // [N]; malformed entries replaced by -1
+  const int b = blockIdx.x;
+  const int32_t* par = parent + static_cast<size_t>(b) * N;
+  int bad = 0;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    int p = par[i];
+    const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+    if (!ok) {
+      bad = 1;
+      p = -1;
+    }
+    s_par[i] = p;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) report(dev_err, JF_DEVERR_BAD_PARENT);
+
+  const int P = prefix_len[b];
+  uint64_t* mrow = mask + static_cast<size_t>(b) * N * W;
+  const int pairs = N * W;
+  for (int e = threadIdx.x; e < pairs; e += blockDim.x) {
+    const int i = e / W;
+    const int w = e - i * W;
+    const int lo = w * 64;
+    uint64_t word = 0;
+    int count = 0;
+    int a = i;
+    // Bits above the word are skipped; the walk ends below the word's first node unless
+    // w == 0, whose walk runs to the root to count the depth.
+    while (a >= lo) {
+      if (a < lo + 64) word |= 1ull << (a - lo);
+      ++count;
+      a = s_par[a];
+    }
+    mrow[e] = word;
+    if (w == 0) {
+      const int d = count - 1;
+      if (depth != nullptr) depth[static_cast<size_t>(b) * N + i] = d;
+      if (pos != nullptr) pos[static_cast<size_t>(b) * N + i] = P + d;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace jf
+
+extern "C" jf_status jf_build_tree_mask(const int32_t* parent, const int32_t* prefix_len,
+                                        int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
+                                        int32_t* pos, int32_t* dev_err, jf_stream_t stream) {
+  if (parent == nullptr || prefix_len == nullptr || mask == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  if (B < 1 || N < 1) return JF_ERR_INVALID_ARGUMENT;
+  if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  if (!jf::aligned_to(mask, 8)) return JF_ERR_MISALIGNED;
+  const int W = (N + 63) / 64;
+  const size_t smem = sizeof(int32_t) * static_cast<size_t>(N);
+  jf::tree_mask_kernel<<<B, jf::kMaskThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+      parent, prefix_len, N, W, mask, depth, pos, dev_err);
+  return jf::launch_status();
+}

@@ -1,0 +1,320 @@
+// jf_verify.cu -- greedy tree verification: per-node vocabulary argmax, then the longest
+// accepted root path.
+//
+// The target model checks all drafted nodes in one pass and keeps the drafted prefix it
+// agrees with (qxai.app commentary on JetFlow, "まず、何が問題なのか"; the explainer's §4
+// counts the accepted tokens tau).  Greedy reading: child c of p is accepted iff
+// draft[c] == argmax(logits[p]).
+//
+// Kernel 1 (HBM-bound): each CTA scans one chunk of one logits row with 16-byte loads and
+// writes a packed 64-bit key (order-preserving value bits << 32 | ~index) into the
+// workspace; max over keys gives the largest value and, among equal values, the smallest
+// index.  Chunks per row are chosen so that rows x chunks fills the GPU.
+// Kernel 2 (one CTA per sequence): merges the chunk keys into argmax, finds depths by
+// pointer jumping, computes accepted-subtree lengths level by level from the deepest
+// level up with shared-memory atomicMax on (len + 1) << 16 | (0xFFFF - child), and walks
+// the best children from the root.
+#include <algorithm>
+
+#include "jf_common.cuh"
+
+namespace jf {
+namespace {
+
+constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxUnroll = 4;
+constexpr int kWalkThreads = 512;
+constexpr int kMinChunkElems = 8192;
+
+// Order-preserving map of a float to uint32 (larger float -> larger integer); -0 -> +0.
+__device__ __forceinline__ uint32_t ordered_bits(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t pack_key(float v, int idx) {
+  return (static_cast<uint64_t>(ordered_bits(v)) << 32) |
+         static_cast<uint64_t>(~static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<uint16_t>(uint16_t x) {
+  return __uint_as_float(static_cast<uint32_t>(x) << 16);
+}
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+
+struct Best {
+  float v;
+  int i;
+  __device__ __forceinline__ void take(float x, int idx) {
+    if (x > v) { v = x; i = idx; }   // indices arrive in increasing order per thread
+  }
+};
+
+__device__ __forceinline__ void take_vec(Best& b, uint4 q, int idx, uint16_t) {
+  b.take(bf16_lo(q.x), idx + 0); b.take(bf16_hi(q.x), idx + 1);
+  b.take(bf16_lo(q.y), idx + 2); b.take(bf16_hi(q.y), idx + 3);
+  b.take(bf16_lo(q.z), idx + 4); b.take(bf16_hi(q.z), idx + 5);
+  b.take(bf16_lo(q.w), idx + 6); b.take(bf16_hi(q.w), idx + 7);
+}
+__device__ __forceinline__ void take_vec(Best& b, uint4 q, int idx, float) {
+  b.take(__uint_as_float(q.x), idx + 0); b.take(__uint_as_float(q.y), idx + 1);
+  b.take(__uint_as_float(q.z), idx + 2); b.take(__uint_as_float(q.w), idx + 3);
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t k) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t other = __shfl_xor_sync(0xffffffffu, k, o);
+    k = other > k ? other : k;
+  }
+  return k;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kArgmaxThreads)
+    argmax_chunk_kernel(const T* __restrict__ logits, long long V, int chunks, int chunk_len,
+                        uint64_t* __restrict__ part) {
+  constexpr int kVec = 16 / sizeof(T);
+  const long long row = blockIdx.x / chunks;
+  const int c = blockIdx.x - static_cast<int>(row * chunks);
+  const long long s = static_cast<long long>(c) * chunk_len;
+  const long long e = min(V, s + chunk_len);
+  const T* base = logits + row * V;
+
+  // Split [s, e) into a scalar head up to the first 16-byte boundary, a vector body and
+  // a scalar tail; every thread sees its indices in increasing order.
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base + s);
+  long long head = ((16 - (addr & 15)) & 15) / sizeof(T);
+  if (head > e - s) head = e - s;
+  const long long body0 = s + head;
+  const long long nvec = (e - body0) / kVec;
+  const long long body1 = body0 + nvec * kVec;
+
+  Best best{-INFINITY, -1};
+  int first = -1;   // first index this thread looked at (for all -inf rows)
+  if (threadIdx.x < head) {
+    const long long idx = s + threadIdx.x;
+    best.take(to_f<T>(base[idx]), static_cast<int>(idx));
+    first = static_cast<int>(idx);
+  }
+  const uint4* vb = reinterpret_cast<const uint4*>(base + body0);
+  for (long long v0 = threadIdx.x; v0 < nvec; v0 += kArgmaxThreads * kArgmaxUnroll) {
+    uint4 q[kArgmaxUnroll];
+#pragma unroll
+    for (int u = 0; u < kArgmaxUnroll; ++u) {
+      const long long vi = v0 + static_cast<long long>(u) * kArgmaxThreads;
+      if (vi < nvec) q[u] = __ldcs(vb + vi);
+    }
+#pragma unroll
+    for (int u = 0; u < kArgmaxUnroll; ++u) {
+      const long long vi = v0 + static_cast<long long>(u) * kArgmaxThreads;
+      if (vi < nvec) {
+        const int idx = static_cast<int>(body0 + vi * kVec);
+        if (first < 0) first = idx;
+        take_vec(best, q[u], idx, T());
+      }
+    }
+  }
+  if (threadIdx.x < e - body1) {
+    const long long idx = body1 + threadIdx.x;
+    best.take(to_f<T>(base[idx]), static_cast<int>(idx));
+    if (first < 0) first = static_cast<int>(idx);
+  }
+  if (best.i < 0 && first >= 0) best.i = first;   // every value it saw was -inf
+  uint64_t key = best.i < 0 ? 0ull : pack_key(best.v, best.i);
+
+  __shared__ uint64_t s_keys[kArgmaxThreads / 32];
+  key = warp_max_u64(key);
+  if ((threadIdx.x & 31) == 0) s_keys[threadIdx.x >> 5] = key;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    key = threadIdx.x < kArgmaxThreads / 32 ? s_keys[threadIdx.x] : 0ull;
+    key = warp_max_u64(key);
+    if (threadIdx.x == 0) part[blockIdx.x] = key;
+  }
+}
+
+__global__ void __launch_bounds__(kWalkThreads)
+    tree_walk_kernel(const uint64_t* __restrict__ part, int chunks,
+                     const int32_t* __restrict__ draft, const int32_t* __restrict__ parent,
+                     int N, int V, int32_t* __restrict__ argmax_out,
+                     int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
+                     int32_t* __restrict__ bonus, int32_t* dev_err) {
+  extern __shared__ int32_t sm[];
+  int32_t* s_par = sm;            // [N] parent, malformed -> -1
+  int32_t* s_am = s_par + N;      // [N] argmax
+  int32_t* s_dep = s_am + N;      // [N] depth (pointer jumping)
+  int32_t* s_anc = s_dep + N;     // [N] ancestor pointer (pointer jumping)
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(s_anc + N);   // [N] best accepted child
+  int32_t* s_path = reinterpret_cast<int32_t*>(s_key + N);    // [N]
+  __shared__ int s_flag;
+  __shared__ int s_len;
+
+  const int b = blockIdx.x;
+  const size_t rb = static_cast<size_t>(b) * N;
+  int bad_parent = 0, bad_token = 0;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    uint64_t k = 0;
+    const uint64_t* pk = part + (rb + i) * chunks;
+    for (int c = 0; c < chunks; ++c) k = max(k, pk[c]);
+    const int am = static_cast<int>(~static_cast<uint32_t>(k & 0xFFFFFFFFull));
+    s_am[i] = am;
+    if (argmax_out != nullptr) argmax_out[rb + i] = am;
+    int p = parent[rb + i];
+    const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+    if (!ok) { bad_parent = 1; p = -1; }
+    s_par[i] = p;
+    s_anc[i] = p;
+    s_dep[i] = p >= 0 ? 1 : 0;
+    s_key[i] = 0u;
+    if (i > 0) {
+      const int d = draft[rb + i];
+      if (d < 0 || d >= V) bad_token = 1;
+    }
+  }
+  bad_parent = __syncthreads_or(bad_parent);
+  bad_token = __syncthreads_or(bad_token);
+  if (threadIdx.x == 0) {
+    if (bad_parent) report(dev_err, JF_DEVERR_BAD_PARENT);
+    if (bad_token) report(dev_err, JF_DEVERR_BAD_TOKEN);
+  }
+
+  // Depth by pointer jumping: dep[i] += dep[anc[i]], anc[i] = anc[anc[i]].
+  constexpr int kPer = (JF_MAX_NODES + kWalkThreads - 1) / kWalkThreads;
+  for (int round = 0; round < 32; ++round) {
+    int nd[kPer], na[kPer];
+    int any = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kWalkThreads;
+      if (i < N) {
+        const int a = s_anc[i];
+        nd[k] = s_dep[i];
+        na[k] = a;
+        if (a >= 0) {
+          nd[k] += s_dep[a];
+          na[k] = s_anc[a];
+          any = 1;
+        }
+      }
+    }
+    if (!__syncthreads_or(any)) break;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = threadIdx.x + k * kWalkThreads;
+      if (i < N) { s_dep[i] = nd[k]; s_anc[i] = na[k]; }
+    }
+    __syncthreads();
+  }
+  int maxd = 0;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) maxd = max(maxd, s_dep[i]);
+  if (threadIdx.x == 0) s_flag = 0;
+  __syncthreads();
+  atomicMax(&s_flag, maxd);
+  __syncthreads();
+  maxd = s_flag;
+
+  // Accepted-subtree lengths, deepest level first: a node's key is final once every
+  // node one level below has been processed.
+  for (int d = maxd; d >= 1; --d) {
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+      const int p = s_par[i];
+      if (s_dep[i] == d && p >= 0 && draft[rb + i] == s_am[p]) {
+        const uint32_t len = (s_key[i] >> 16) + 1u;
+        atomicMax(&s_key[p], (len << 16) | static_cast<uint32_t>(0xFFFF - i));
+      }
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    int cur = 0, n = 0;
+    s_path[0] = 0;
+    while (s_key[cur] != 0u && n < N - 1) {
+      cur = 0xFFFF - static_cast<int>(s_key[cur] & 0xFFFFu);
+      s_path[++n] = cur;
+    }
+    s_len = n;
+    accept_len[b] = n;
+    bonus[b] = s_am[cur];
+  }
+  __syncthreads();
+  const int n = s_len;
+  for (int k = threadIdx.x; k < N; k += blockDim.x) path[rb + k] = k <= n ? s_path[k] : -1;
+}
+
+struct VerifyPlan {
+  int chunks;
+  int chunk_len;
+};
+
+bool plan_verify(int B, int N, int V, VerifyPlan* p) {
+  if (B < 1 || N < 1 || N > JF_MAX_NODES || V < 1) return false;
+  const int sms = current_sm_count() > 0 ? current_sm_count() : 148;
+  const long long rows = static_cast<long long>(B) * N;
+  const long long target = static_cast<long long>(sms) * 4;   // CTAs to keep HBM busy
+  long long c = (target + rows - 1) / rows;
+  const long long cmax = std::max<long long>(1, (V + kMinChunkElems - 1) / kMinChunkElems);
+  c = std::min(std::max<long long>(c, 1), cmax);
+  long long len = (V + c - 1) / c;
+  len = (len + 7) / 8 * 8;
+  c = (V + len - 1) / len;
+  p->chunks = static_cast<int>(c);
+  p->chunk_len = static_cast<int>(len);
+  return true;
+}
+
+}  // namespace
+}  // namespace jf
+
+extern "C" size_t jf_tree_verify_workspace_size(int32_t B, int32_t N, int32_t V) {
+  jf::VerifyPlan p;
+  if (!jf::plan_verify(B, N, V, &p)) return static_cast<size_t>(-1);
+  return static_cast<size_t>(B) * N * p.chunks * sizeof(uint64_t);
+}
+
+extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int32_t* draft,
+                                    const int32_t* parent, int32_t B, int32_t N, int32_t V,
+                                    int32_t* argmax, int32_t* accept_len, int32_t* path,
+                                    int32_t* bonus, void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_err, jf_stream_t stream) {
+  if (logits == nullptr || draft == nullptr || parent == nullptr || accept_len == nullptr ||
+      path == nullptr || bonus == nullptr || workspace == nullptr)
+    return JF_ERR_INVALID_ARGUMENT;
+  if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
+  if (B < 1 || N < 1 || V < 1) return JF_ERR_INVALID_ARGUMENT;
+  if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  jf::VerifyPlan p;
+  if (!jf::plan_verify(B, N, V, &p)) return JF_ERR_UNSUPPORTED;
+  const size_t need = static_cast<size_t>(B) * N * p.chunks * sizeof(uint64_t);
+  if (workspace_bytes < need) return JF_ERR_WORKSPACE_TOO_SMALL;
+  if (!jf::aligned_to(workspace, 8)) return JF_ERR_MISALIGNED;
+  if (!jf::aligned_to(logits, dtype == JF_DTYPE_BF16 ? 2 : 4)) return JF_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint64_t* part = static_cast<uint64_t*>(workspace);
+  const long long grid = static_cast<long long>(B) * N * p.chunks;
+  if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  if (dtype == JF_DTYPE_BF16)
+    jf::argmax_chunk_kernel<uint16_t><<<static_cast<unsigned>(grid), jf::kArgmaxThreads, 0, s>>>(
+        static_cast<const uint16_t*>(logits), V, p.chunks, p.chunk_len, part);
+  else
+    jf::argmax_chunk_kernel<float><<<static_cast<unsigned>(grid), jf::kArgmaxThreads, 0, s>>>(
+        static_cast<const float*>(logits), V, p.chunks, p.chunk_len, part);
+  if (cudaGetLastError() != cudaSuccess) return JF_ERR_CUDA;
+  const size_t smem = static_cast<size_t>(N) * 6 * sizeof(int32_t);
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return JF_ERR_CUDA;
+  }
+  jf::tree_walk_kernel<<<B, jf::kWalkThreads, smem, s>>>(part, p.chunks, draft, parent, N, V,
+                                                         argmax, accept_len, path, bonus, dev_err);
+  return jf::launch_status();
+}

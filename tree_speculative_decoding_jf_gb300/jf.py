@@ -1,0 +1,231 @@
+"""Thin ctypes binding over libjf.so (declared in include/jf.h).
+
+The functions named ``jf_*`` mirror the C entry points one to one: they take torch tensors
+that already live on the GPU, check dtype/shape/contiguity, and pass raw pointers and the
+current CUDA stream.  All computation happens in the library's kernels; there is no
+fallback of any kind -- if libjf.so is missing or fails to load, importing this module
+raises.  ``build_tree_mask``, ``tree_attention`` and ``tree_verify`` are conveniences that
+also allocate the outputs (with torch) before calling the same entry points.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libjf.so")
+
+JF_OK = 0
+STATUS_NAMES = {0: "JF_OK", 1: "JF_ERR_INVALID_ARGUMENT", 2: "JF_ERR_INVALID_TREE",
+                3: "JF_ERR_UNSUPPORTED", 4: "JF_ERR_WORKSPACE_TOO_SMALL", 5: "JF_ERR_CUDA",
+                6: "JF_ERR_TIMEOUT", 7: "JF_ERR_MISALIGNED"}
+JF_DTYPE_BF16, JF_DTYPE_F32 = 0, 1
+DEVERR_BAD_PARENT, DEVERR_BAD_PAGE, DEVERR_BAD_PREFIX = 0x1, 0x2, 0x4
+DEVERR_BAD_TOKEN, DEVERR_TIMEOUT = 0x8, 0x10
+MAX_NODES = 4096
+PAGE_SIZE = 16
+
+
+class JFError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m tree_speculative_decoding_jf_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    lib.jf_status_string.argtypes = [ctypes.c_int]
+    lib.jf_status_string.restype = ctypes.c_char_p
+    lib.jf_version.restype = ctypes.c_int
+    lib.jf_build_tree_mask.argtypes = [P, P, i32, i32, P, P, P, P, P]
+    lib.jf_build_tree_mask.restype = ctypes.c_int
+    lib.jf_tree_attention_workspace_size.argtypes = [i32] * 7
+    lib.jf_tree_attention_workspace_size.restype = sz
+    lib.jf_tree_attention.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                      f32, P, P, P, sz, P, P]
+    lib.jf_tree_attention.restype = ctypes.c_int
+    lib.jf_tree_verify_workspace_size.argtypes = [i32, i32, i32]
+    lib.jf_tree_verify_workspace_size.restype = sz
+    lib.jf_tree_verify.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P, P, P, sz, P, P]
+    lib.jf_tree_verify.restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check(fn: str, status: int):
+    if status != JF_OK:
+        raise JFError(fn, status)
+
+
+def jf_status_string(status: int) -> str:
+    return _lib.jf_status_string(status).decode()
+
+
+def jf_version() -> int:
+    return _lib.jf_version()
+
+
+def jf_build_tree_mask(parent, prefix_len, mask, depth=None, pos=None, dev_err=None,
+                       stream=None) -> None:
+    B, N = parent.shape
+    W = (N + 63) // 64
+    _need(parent, "parent", torch.int32)
+    _need(prefix_len, "prefix_len", torch.int32, (B,))
+    _need(mask, "mask", torch.int64, (B, N, W))
+    for name, t in (("depth", depth), ("pos", pos)):
+        if t is not None:
+            _need(t, name, torch.int32, (B, N))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_build_tree_mask", _lib.jf_build_tree_mask(
+        _ptr(parent), _ptr(prefix_len), B, N, _ptr(mask), _ptr(depth), _ptr(pos), _ptr(dev_err),
+        _stream(stream)))
+
+
+def jf_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_pages, page_size=PAGE_SIZE) -> int:
+    n = _lib.jf_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_pages, page_size)
+    if n == SIZE_MAX:
+        raise JFError("jf_tree_attention_workspace_size", 3)
+    return int(n)
+
+
+def jf_tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale, out, lse=None,
+                      workspace=None, dev_err=None, stream=None) -> None:
+    B, N, Hq, D = q.shape
+    num_pages, page, Hkv, D2 = k_cache.shape
+    max_pages = block_table.shape[1]
+    W = (N + 63) // 64
+    _need(q, "q", torch.bfloat16)
+    _need(k_cache, "k_cache", torch.bfloat16)
+    _need(v_cache, "v_cache", torch.bfloat16, k_cache.shape)
+    _need(block_table, "block_table", torch.int32, (B, max_pages))
+    _need(prefix_len, "prefix_len", torch.int32, (B,))
+    _need(mask, "mask", torch.int64, (B, N, W))
+    _need(out, "out", torch.bfloat16, (B, N, Hq, D))
+    if D2 != D:
+        raise ValueError("q and k_cache head dims differ")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (B, Hq, N))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    ws_bytes = 0
+    if workspace is not None:
+        if workspace.device.type != "cuda" or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("jf_tree_attention", _lib.jf_tree_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(prefix_len), _ptr(mask),
+        B, N, Hq, Hkv, D, page, max_pages, num_pages, float(scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)))
+
+
+def jf_tree_verify_workspace_size(B, N, V) -> int:
+    n = _lib.jf_tree_verify_workspace_size(B, N, V)
+    if n == SIZE_MAX:
+        raise JFError("jf_tree_verify_workspace_size", 3)
+    return int(n)
+
+
+def jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax=None, workspace=None,
+                   dev_err=None, stream=None) -> None:
+    B, N, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = JF_DTYPE_BF16
+    elif logits.dtype == torch.float32:
+        dt = JF_DTYPE_F32
+    else:
+        raise TypeError("logits must be bfloat16 or float32")
+    _need(logits, "logits", logits.dtype)
+    _need(draft, "draft", torch.int32, (B, N))
+    _need(parent, "parent", torch.int32, (B, N))
+    _need(accept_len, "accept_len", torch.int32, (B,))
+    _need(path, "path", torch.int32, (B, N))
+    _need(bonus, "bonus", torch.int32, (B,))
+    if argmax is not None:
+        _need(argmax, "argmax", torch.int32, (B, N))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    ws_bytes = 0
+    if workspace is not None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("jf_tree_verify", _lib.jf_tree_verify(
+        _ptr(logits), dt, _ptr(draft), _ptr(parent), B, N, V, _ptr(argmax), _ptr(accept_len),
+        _ptr(path), _ptr(bonus), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- conveniences
+
+def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    return torch.empty((nbytes + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def build_tree_mask(parent: torch.Tensor, prefix_len: torch.Tensor, dev_err=None, stream=None):
+    B, N = parent.shape
+    W = (N + 63) // 64
+    mask = torch.empty((B, N, W), dtype=torch.int64, device=parent.device)
+    depth = torch.empty((B, N), dtype=torch.int32, device=parent.device)
+    pos = torch.empty((B, N), dtype=torch.int32, device=parent.device)
+    jf_build_tree_mask(parent, prefix_len, mask, depth, pos, dev_err, stream)
+    return mask, depth, pos
+
+
+def tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale=None,
+                   with_lse=False, dev_err=None, stream=None):
+    B, N, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    if scale is None:
+        scale = D ** -0.5
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if with_lse else None
+    ws = _workspace(jf_tree_attention_workspace_size(B, N, Hq, Hkv, D, block_table.shape[1],
+                                                     k_cache.shape[1]), q.device)
+    jf_tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale, out, lse, ws,
+                      dev_err, stream)
+    return (out, lse) if with_lse else out
+
+
+def tree_verify(logits, draft, parent, dev_err=None, stream=None):
+    B, N, V = logits.shape
+    dev = logits.device
+    argmax = torch.empty((B, N), dtype=torch.int32, device=dev)
+    accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    bonus = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = _workspace(jf_tree_verify_workspace_size(B, N, V), dev)
+    jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax, ws, dev_err, stream)
+    return argmax, accept_len, path, bonus

@@ -170,32 +170,6 @@ class Workload:
     def kv_len(self) -> np.ndarray:
         return self.prefix_len.astype(np.int64) + self.N
 
-    def algorithmic_bytes(self) -> int:
-        """Bytes a single tree-attention call must move (one read of every visible
-        K/V row per kv-head, Q read, O written, masks and block table read)."""
-        kv = int(self.kv_len().sum()) * self.Hkv * self.D * 2 * 2
-        qo = 2 * self.B * self.N * self.Hq * self.D * 2
-        w = (self.N + 63) // 64
-        mask = self.B * self.N * w * 8
-        bt = int(((self.kv_len() + self.page - 1) // self.page).sum()) * 4
-        return kv + qo + mask + bt
-
-
-def _depths(parent: np.ndarray) -> np.ndarray:
-    d = np.zeros(len(parent), dtype=np.int64)
-    for i in range(1, len(parent)):
-        d[i] = d[parent[i]] + 1
-    return d
-
-
-def algorithmic_flops(w: Workload) -> int:
-    """4*D*Hq*sum_b(N*P_b + sum_i(depth_i + 1)): visible (query, key) pairs only."""
-    tot = 0
-    for b in range(w.B):
-        dep = _depths(w.parent[b])
-        tot += w.N * int(w.prefix_len[b]) + int((dep + 1).sum())
-    return 4 * w.D * w.Hq * tot
-
 
 def make_workload(name: str, B: int, N: int, Hq: int, Hkv: int, D: int, V: int,
                   prefix_len, tree: str = "chain", logits_dtype: str = "bf16",
@@ -321,3 +295,25 @@ def config(name: str, forcing: Optional[str] = None, with_logits: bool = True) -
     if forcing is not None:
         kw["forcing"] = forcing
     return make_workload(name, with_logits=with_logits, **kw)
+
+
+def device_tensors(w: Workload, device="cuda", with_logits: bool = True) -> dict:
+    """Copy a workload's arrays into torch tensors on ``device`` (bf16 bit patterns are
+    reinterpreted, not converted)."""
+    import torch
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+    d = dict(q=bf16(w.q), k_cache=bf16(w.k_cache), v_cache=bf16(w.v_cache),
+             block_table=i32(w.block_table), prefix_len=i32(w.prefix_len), parent=i32(w.parent),
+             draft=i32(w.draft))
+    if with_logits and w.logits.size:
+        if w.logits_dtype == "f32":
+            d["logits"] = torch.from_numpy(np.ascontiguousarray(w.logits)).to(device)
+        else:
+            d["logits"] = bf16(w.logits)
+    return d
