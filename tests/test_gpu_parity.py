@@ -127,7 +127,7 @@ def test_verify_golden_walk_cases(jf):
     rng = np.random.default_rng(0)
     for case in _golden_walk_cases():
         N = len(case["parent"])
-        V = 16
+        V = 64
         logits = rng.uniform(-1, 1, size=(1, N, V)).astype(np.float32)
         logits[0, np.arange(N), case["argmax"]] = 5.0
         lg = torch.from_numpy(logits).cuda()
