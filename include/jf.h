@@ -47,7 +47,8 @@ typedef enum {
   JF_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the *_workspace_size value  */
   JF_ERR_CUDA = 5,                /* a CUDA runtime call or kernel launch failed       */
   JF_ERR_TIMEOUT = 6,             /* reserved: timeouts are reported on device         */
-  JF_ERR_MISALIGNED = 7           /* a pointer is not 16-byte aligned where required   */
+  JF_ERR_MISALIGNED = 7,          /* a pointer is not 16-byte aligned where required   */
+  JF_ERR_SCRATCH_CAPACITY = 8     /* sizes exceed the static scratch of a *_static call */
 } jf_status;
 
 typedef enum { JF_DTYPE_BF16 = 0, JF_DTYPE_F32 = 1 } jf_dtype;
@@ -166,6 +167,33 @@ jf_status jf_tree_verify(const void* logits, int32_t dtype, const int32_t* draft
                          int32_t* argmax, int32_t* accept_len, int32_t* path, int32_t* bonus,
                          void* workspace, size_t workspace_bytes, int32_t* dev_err,
                          jf_stream_t stream);
+
+/*
+ * jf_tree_verify_static -- the same computation and outputs as jf_tree_verify, for
+ * callers that cannot allocate device memory on their call path: for example a serving
+ * engine that reserves all free device memory for its KV-cache pool at start-up, or a
+ * plug-in running inside a host application that does not expose an allocator.  The
+ * paper has no counterpart; this is a packaging variant of the verify call.
+ *
+ * Instead of a caller-provided workspace it uses a fixed scratch array compiled into the
+ * library (JF_VERIFY_STATIC_SCRATCH_KEYS uint64 entries, 4 MiB), which every GPU that
+ * loads the library keeps until the process exits.  The call itself allocates nothing.
+ *   - The first call on each device looks up the array's device address with
+ *     cudaGetSymbolAddress (a runtime query, no allocation) while that device is current,
+ *     and caches it; make that first call before any stream capture.
+ *   - Capacity: B * N * chunks entries, where chunks = jf_tree_verify_workspace_size(B, N,
+ *     V) / (8 * B * N).  Larger problems return JF_ERR_SCRATCH_CAPACITY and launch nothing.
+ *   - The array is shared by every call and keeps the last call's contents; nothing in it
+ *     needs to start at zero (each entry read is written earlier in the same call).
+ *     Calls whose kernels overlap on the GPU (different streams, or different host
+ *     threads) race on it: serialise them.
+ * Arguments, limits and device error bits are those of jf_tree_verify.
+ */
+#define JF_VERIFY_STATIC_SCRATCH_KEYS (1u << 19)
+jf_status jf_tree_verify_static(const void* logits, int32_t dtype, const int32_t* draft,
+                                const int32_t* parent, int32_t B, int32_t N, int32_t V,
+                                int32_t* argmax, int32_t* accept_len, int32_t* path,
+                                int32_t* bonus, int32_t* dev_err, jf_stream_t stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -33,6 +33,7 @@ extern "C" const char* jf_status_string(int status) {
     case JF_ERR_CUDA: return "JF_ERR_CUDA";
     case JF_ERR_TIMEOUT: return "JF_ERR_TIMEOUT";
     case JF_ERR_MISALIGNED: return "JF_ERR_MISALIGNED";
+    case JF_ERR_SCRATCH_CAPACITY: return "JF_ERR_SCRATCH_CAPACITY";
     default: return "JF_ERR_UNKNOWN";
   }
 }

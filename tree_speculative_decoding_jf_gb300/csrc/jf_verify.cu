@@ -15,6 +15,7 @@
 // level up with shared-memory atomicMax on (len + 1) << 16 | (0xFFFF - child), and walks
 // the best children from the root.
 #include <algorithm>
+#include <mutex>
 
 #include "jf_common.cuh"
 
@@ -314,6 +315,74 @@ extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int
                              static_cast<int>(smem)) != cudaSuccess)
       return JF_ERR_CUDA;
   }
+  jf::tree_walk_kernel<<<B, jf::kWalkThreads, smem, s>>>(part, p.chunks, draft, parent, N, V,
+                                                         argmax, accept_len, path, bonus, dev_err);
+  return jf::launch_status();
+}
+
+// ------------------------------------------------------------------------ allocation-free
+// jf_tree_verify_static: the argmax partial keys live in a fixed array compiled into the
+// library instead of a caller workspace.  Host code only ever passes the array's device
+// address (looked up per device); the symbol itself is a host-side stand-in.
+static __device__ __align__(256) uint64_t g_verify_static_scratch[JF_VERIFY_STATIC_SCRATCH_KEYS];
+
+namespace jf {
+namespace {
+
+// Device address of g_verify_static_scratch on the current device, looked up once per
+// device with that device current; null if the lookup fails.
+uint64_t* verify_static_scratch() {
+  static std::mutex mu;
+  static uint64_t* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_verify_static_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = static_cast<uint64_t*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace jf
+
+extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
+                                           const int32_t* draft, const int32_t* parent,
+                                           int32_t B, int32_t N, int32_t V, int32_t* argmax,
+                                           int32_t* accept_len, int32_t* path, int32_t* bonus,
+                                           int32_t* dev_err, jf_stream_t stream) {
+  if (logits == nullptr || draft == nullptr || parent == nullptr || accept_len == nullptr ||
+      path == nullptr || bonus == nullptr)
+    return JF_ERR_INVALID_ARGUMENT;
+  if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
+  if (B < 1 || N < 1 || V < 1) return JF_ERR_INVALID_ARGUMENT;
+  if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  jf::VerifyPlan p;
+  if (!jf::plan_verify(B, N, V, &p)) return JF_ERR_UNSUPPORTED;
+  const unsigned long long keys = static_cast<unsigned long long>(B) * N * p.chunks;
+  if (keys > JF_VERIFY_STATIC_SCRATCH_KEYS) return JF_ERR_SCRATCH_CAPACITY;
+  if (!jf::aligned_to(logits, dtype == JF_DTYPE_BF16 ? 2 : 4)) return JF_ERR_MISALIGNED;
+  uint64_t* part = jf::verify_static_scratch();
+  if (part == nullptr) return JF_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const unsigned grid = static_cast<unsigned>(keys);
+  if (dtype == JF_DTYPE_BF16)
+    jf::argmax_chunk_kernel<uint16_t><<<grid, jf::kArgmaxThreads, 0, s>>>(
+        static_cast<const uint16_t*>(logits), V, p.chunks, p.chunk_len, part);
+  else
+    jf::argmax_chunk_kernel<float><<<grid, jf::kArgmaxThreads, 0, s>>>(
+        static_cast<const float*>(logits), V, p.chunks, p.chunk_len, part);
+  if (cudaGetLastError() != cudaSuccess) return JF_ERR_CUDA;
+  const size_t smem = static_cast<size_t>(N) * 6 * sizeof(int32_t);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return JF_ERR_CUDA;
   jf::tree_walk_kernel<<<B, jf::kWalkThreads, smem, s>>>(part, p.chunks, draft, parent, N, V,
                                                          argmax, accept_len, path, bonus, dev_err);
   return jf::launch_status();

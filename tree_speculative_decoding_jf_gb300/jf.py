@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libjf.so")
 JF_OK = 0
 STATUS_NAMES = {0: "JF_OK", 1: "JF_ERR_INVALID_ARGUMENT", 2: "JF_ERR_INVALID_TREE",
                 3: "JF_ERR_UNSUPPORTED", 4: "JF_ERR_WORKSPACE_TOO_SMALL", 5: "JF_ERR_CUDA",
-                6: "JF_ERR_TIMEOUT", 7: "JF_ERR_MISALIGNED"}
+                6: "JF_ERR_TIMEOUT", 7: "JF_ERR_MISALIGNED", 8: "JF_ERR_SCRATCH_CAPACITY"}
 JF_DTYPE_BF16, JF_DTYPE_F32 = 0, 1
 DEVERR_BAD_PARENT, DEVERR_BAD_PAGE, DEVERR_BAD_PREFIX = 0x1, 0x2, 0x4
 DEVERR_BAD_TOKEN, DEVERR_TIMEOUT = 0x8, 0x10
@@ -55,6 +55,8 @@ def _load():
     lib.jf_tree_verify_workspace_size.restype = sz
     lib.jf_tree_verify.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P, P, P, sz, P, P]
     lib.jf_tree_verify.restype = ctypes.c_int
+    lib.jf_tree_verify_static.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P, P, P, P]
+    lib.jf_tree_verify_static.restype = ctypes.c_int
     return lib
 
 
@@ -184,6 +186,31 @@ def jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax=None, 
     _check("jf_tree_verify", _lib.jf_tree_verify(
         _ptr(logits), dt, _ptr(draft), _ptr(parent), B, N, V, _ptr(argmax), _ptr(accept_len),
         _ptr(path), _ptr(bonus), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)))
+
+
+def jf_tree_verify_static(logits, draft, parent, accept_len, path, bonus, argmax=None,
+                          dev_err=None, stream=None) -> None:
+    """jf_tree_verify without a workspace: the library's fixed scratch array is used
+    (see include/jf.h for its capacity and the rules for concurrent calls)."""
+    B, N, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = JF_DTYPE_BF16
+    elif logits.dtype == torch.float32:
+        dt = JF_DTYPE_F32
+    else:
+        raise TypeError("logits must be bfloat16 or float32")
+    _need(logits, "logits", logits.dtype)
+    for name, t, shape in (("draft", draft, (B, N)), ("parent", parent, (B, N)),
+                           ("accept_len", accept_len, (B,)), ("path", path, (B, N)),
+                           ("bonus", bonus, (B,))):
+        _need(t, name, torch.int32, shape)
+    if argmax is not None:
+        _need(argmax, "argmax", torch.int32, (B, N))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_tree_verify_static", _lib.jf_tree_verify_static(
+        _ptr(logits), dt, _ptr(draft), _ptr(parent), B, N, V, _ptr(argmax), _ptr(accept_len),
+        _ptr(path), _ptr(bonus), _ptr(dev_err), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- conveniences
