@@ -294,6 +294,8 @@ def config(name: str, forcing: Optional[str] = None, with_logits: bool = True) -
         kw["prefix_len"] = _streams(kw["seed"])["prefix"].integers(512, 8193, size=kw["B"])
     if forcing is not None:
         kw["forcing"] = forcing
+    if not with_logits:               # forced drafts only concern the verify logits
+        kw["forcing"] = "none"
     return make_workload(name, with_logits=with_logits, **kw)
 
 
