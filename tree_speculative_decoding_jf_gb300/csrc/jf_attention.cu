@@ -15,20 +15,28 @@
 //
 // Roles inside a CTA (128 * (1 + NT) threads):
 //   warp 0      TMA producer: stages the split's page ids from the block table in shared
-//               memory (bounds-checked), loads the Q tiles once, then per key tile eight
-//               16-key pages of K and of V (one TMA box each per 64-column half) into a
-//               STAGES-deep ring.  Pages past the sequence end load as zeros.
+//               memory (bounds-checked, eight loads in flight per lane; the first stages'
+//               ids first), loads the Q tiles once, then per key tile one TMA box per
+//               (16-key page, 64-column half) of K and of V -- issued by 16 lanes at once --
+//               into a STAGES-deep ring.  Pages past the sequence end load as zeros.
 //   warp 1      allocates TMEM and issues tcgen05.mma from one lane:
 //                 S_t = Q_t K^T  (128 x 128, fp32 in TMEM),  O_t += P_t V  (P from TMEM).
-//               It zeroes V rows past the sequence end in the last tile (garbage in unused
-//               page slots must not meet a zero probability as NaN).
+//               A V stage is released as soon as the tile's last PV MMA is issued, a K
+//               stage as soon as the next tile's S MMAs are.  It zeroes V rows past the
+//               sequence end in the last tile (garbage in unused page slots must not meet
+//               a zero probability as NaN).
 //   warps 4..   one warpgroup per row tile t: TMEM lane = row, so each thread owns one
 //               full score row.  Ancestor bitmasks of the tile's nodes are staged in
-//               shared memory and applied to keys at positions >= P_b.  Online softmax in
-//               the log2 domain; the running max is only raised when a tile's max
-//               exceeds it by more than 8 (factor 256), which keeps P <= 256 in bf16 and
-//               makes the O rescale (TMEM load/scale/store) rare.  P (bf16) is written
-//               back into the S columns and consumed by the PV MMA from TMEM.
+//               shared memory; on tiles reaching positions >= P_b they become one 32-bit
+//               visibility word per 32 keys.  Online softmax in the log2 domain (row max
+//               and row sum over independent partial accumulators); the running max is
+//               only raised when a tile's max exceeds it by more than 8 (factor 256),
+//               which keeps P <= 256 in bf16 and makes the O rescale (TMEM
+//               load/scale/store) rare.  P (bf16) is written back into the S columns and
+//               consumed by the PV MMA from TMEM.
+// The control warpgroup hands registers to the softmax warpgroups (setmaxnreg).  Split
+// partials go to a workspace laid out [b][kv-head][split][row][D] (row-contiguous per CTA)
+// and a combine kernel, launched as a programmatic dependent, merges them.
 // All waits are bounded (see jf_sm100.cuh); on a timeout the CTA records
 // JF_DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -36,6 +44,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "jf_common.cuh"
@@ -48,7 +57,6 @@ constexpr int kKeyTile = 128;     // keys per pipeline stage
 constexpr int kRowTile = 128;     // rows per tensor-core tile (TMEM lanes)
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kKeyTile / kPage;
-constexpr int kPageWindowTiles = 256;                   // page ids staged at a time
 constexpr int kMaskBytesPerTile = 8192;                 // staged mask words per row tile
 constexpr float kRescaleThreshold = 8.0f;               // log2 units
 
@@ -61,8 +69,7 @@ struct Cfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + NT * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kPageOff = kVOff + kStages * kTileBytes;
-  static constexpr int kMaskOff = kPageOff + kPageWindowTiles * kPagesPerTile * 4;
+  static constexpr int kMaskOff = kVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kMaskOff + NT * kMaskBytesPerTile + 1024;
   static constexpr int kThreads = 128 * (1 + NT);
   static constexpr uint32_t kTmemCols = (NT == 2) ? 512 : 256;
@@ -76,11 +83,12 @@ struct AttnParams {
   const uint64_t* mask;
   uint16_t* out;        // bf16 [B][N][Hq][D]      (splits == 1)
   float* lse;           // [B][Hq][N] or null      (splits == 1)
-  float* ws_o;          // [B][Hq][N][splits][D]   (splits > 1)
-  float* ws_lse;        // [B][Hq][N][splits]      (log2 domain)
+  float* ws_o;          // [B][Hkv][splits][M][D]  (splits > 1), row r = node * G + head
+  float* ws_lse;        // [B][Hkv][splits][M]     (log2 domain)
   int32_t* dev_err;
   int B, N, Hq, Hkv, G, W, max_pages, num_pages;
   int n_groups, splits, chunk_tiles, M;
+  int cluster_merge;    // 1: the splits of a unit form one cluster and merge through DSMEM
   float scale_log2;     // softmax scale * log2(e)
 };
 
@@ -102,6 +110,76 @@ __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// 2^x on the FMA pipe, to take part of the exponentials off the MUFU unit (the
+// softmax issues one exponential per score; at D = 128 the MUFU rate is as low as the
+// tensor rate).  Cody-Waite style reduction x = n + f with n = round(x), f in
+// [-0.5, 0.5] (the 1.5 * 2^23 shifter leaves n in the low mantissa bits), then a
+// degree-3 polynomial for 2^f fitted by iteratively reweighted least squares to a
+// near-minimax relative error of 7.5e-5 on [-0.5, 0.5] (below bf16's 3.9e-3), and n
+// added to the exponent field.  Inputs are finite scores; x is clamped at -126.
+__device__ __forceinline__ float exp2_poly(float x) {
+  x = fmaxf(x, -126.0f);
+  const float t = x + 12582912.0f;
+  const float f = x - (t - 12582912.0f);
+  float q = fmaf(f, 0.0551716685f, 0.2426111251f);
+  q = fmaf(q, f, 0.6932609677f);
+  q = fmaf(q, f, 0.9999280572f);
+  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+}
+
+// One in kPolyEvery exponential pairs of an unmasked tile goes to exp2_poly (0: none).
+constexpr int kPolyEvery = 0;
+constexpr int kPolyMod = kPolyEvery > 0 ? kPolyEvery : 1;
+
+// Paired fp32 arithmetic (one instruction for two lanes of data) and a 3-input max.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Bits [j0, j0 + 32) of the little-endian bit string words[0 .. W) (zero outside it).
+__device__ __forceinline__ uint32_t mask_bits32(const uint64_t* words, int W, int j0) {
+  if (j0 <= -32 || j0 >= 64 * W) return 0u;
+  if (j0 < 0) return static_cast<uint32_t>(words[0] << (-j0));
+  const int wi = j0 >> 6, off = j0 & 63;
+  uint64_t v = words[wi] >> off;
+  if (off > 32 && wi + 1 < W) v |= words[wi + 1] << (64 - off);
+  return static_cast<uint32_t>(v);
+}
+
 // Four 32-column TMEM loads followed by one wait that ties all 128 registers.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
   tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -114,11 +192,85 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
   tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&r[96]));
 }
 
+// Split partials of one unit live in the shared memory of the cluster's CTAs: normalised
+// fp32 rows in the (idle) K/V ring, row r's 16-byte chunk k at chunk k ^ (r % 8), and the
+// log2-domain LSE of each row in the (idle) mask area.  CTA `rank` merges rows
+// [rank * R / S, (rank + 1) * R / S) of the unit's R = NT * 128 rows, one warp per row,
+// reading every split's row through distributed shared memory.
+template <int NT, int D>
+__device__ __forceinline__ float* part_row(uint8_t* sm, int t, int row) {
+  return reinterpret_cast<float*>(sm + Cfg<NT, D>::kKOff + (t * kRowTile + row) * (D * 4));
+}
+template <int NT, int D>
+__device__ __forceinline__ float* part_lse(uint8_t* sm, int t) {
+  return reinterpret_cast<float*>(sm + Cfg<NT, D>::kMaskOff + t * kMaskBytesPerTile);
+}
+
+template <int NT, int D>
+__device__ void merge_cluster(uint8_t* sm, const AttnParams& p, int b, int g, int mp, int rank) {
+  constexpr int E = D / 32;
+  cluster_sync();                                        // every split's partial is written
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int S = p.splits;
+  const int R = NT * kRowTile;
+  const int per = (R + S - 1) / S;
+  const int r_lo = rank * per, r_hi = min(R, r_lo + per);
+  for (int rr = r_lo + warp; rr < r_hi; rr += nwarps) {
+    const int t = rr / kRowTile, row = rr % kRowTile;
+    const int rg = (mp * NT + t) * kRowTile + row;       // row within the kv-head group
+    if (rg >= p.M) continue;
+    float ls = -INFINITY;
+    if (lane < S) ls = dsmem_ld_f32(dsmem_addr(part_lse<NT, D>(sm, t) + row, lane));
+    float mx = ls;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float w = (ls == -INFINITY) ? 0.f : exp2f(ls - mx);
+    float wsum = w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    const uint32_t sw = static_cast<uint32_t>(row & 7);
+    uint32_t off;
+    if constexpr (E == 4) off = ((static_cast<uint32_t>(lane) ^ sw) << 4);
+    else off = (((static_cast<uint32_t>(lane) >> 1) ^ sw) << 4) + (lane & 1) * 8;
+    const float* mine = part_row<NT, D>(sm, t, row);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int s2 = 0; s2 < S; ++s2) {
+      const float ws = __shfl_sync(0xffffffffu, w, s2);
+      if (ws == 0.f) continue;
+      const uint32_t a = dsmem_addr(reinterpret_cast<const uint8_t*>(mine) + off, s2);
+      if constexpr (E == 4) {
+        const float4 v = dsmem_ld_f32x4(a);
+        acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
+      } else {
+        const float2 v = dsmem_ld_f32x2(a);
+        acc[0] += ws * v.x; acc[1] += ws * v.y;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int i = rg / p.G, h = g * p.G + (rg % p.G);
+    uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * D + lane * E;
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (p.lse != nullptr && lane == 0)
+      p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.N + i] =
+          (wsum > 0.f ? mx + __log2f(wsum) : -INFINITY) * 0.69314718055994531f;
+  }
+  cluster_sync();                                        // nobody leaves while others read it
+}
+
 template <int NT, int D>
 __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     tree_attention_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
-                          const __grid_constant__ CUtensorMap vmap, const AttnParams p) {
+                          const __grid_constant__ CUtensorMap vmap,
+                          const __grid_constant__ CUtensorMap omap,
+                          const __grid_constant__ CUtensorMap wmap, const AttnParams p) {
   using C = Cfg<NT, D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -131,13 +283,13 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
 
-  // ---- which (b, kv-head, row-tile group, split) this CTA owns; group index fastest so
-  // CTAs that read the same K/V tiles run side by side.
+  // ---- which (b, kv-head, row-tile group, split) this CTA owns; split fastest, then the
+  // row-tile group, so CTAs that read the same K/V tiles run side by side.
   int bid = blockIdx.x;
+  const int split = bid % p.splits;      // == rank in the cluster when merging through DSMEM
+  bid /= p.splits;
   const int mp = bid % p.n_groups;
   bid /= p.n_groups;
-  const int split = bid % p.splits;
-  bid /= p.splits;
   const int g = bid % p.Hkv;
   const int b = bid / p.Hkv;
 
@@ -155,15 +307,20 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (T == 0) {   // this split lies past the sequence: an empty partial (weight 0)
+  if (T == 0 && p.cluster_merge) {    // empty split: weight 0, but it joins the merge
+    for (int t = 0; t < NT; ++t)
+      for (int e = threadIdx.x; e < kRowTile; e += blockDim.x) part_lse<NT, D>(sm, t)[e] = -INFINITY;
+    merge_cluster<NT, D>(sm, p, b, g, mp, split);
+    return;
+  }
+  if (T == 0) {                         // split past the sequence: an empty partial (weight 0)
     if (warp >= 4) {
       const int t = (warp >> 2) - 1;
       const int r = (mp * NT + t) * kRowTile + ((warp & 3) * 32 + lane);
       if (r < p.M) {
-        const int i = r / p.G, h = g * p.G + (r % p.G);
-        const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.N + i;
-        p.ws_lse[row * p.splits + split] = -INFINITY;
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.splits + split) * D);
+        const size_t prow = ((static_cast<size_t>(b) * p.Hkv + g) * p.splits + split) * p.M + r;
+        p.ws_lse[prow] = -INFINITY;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * D);
         for (int d = 0; d < D / 4; ++d) dst[d] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
@@ -200,9 +357,13 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   uint8_t* k_s = sm + C::kKOff;
   uint8_t* v_s = sm + C::kVOff;
 
+  // 384 threads x 168 registers at launch (NT == 2): the control warpgroup hands
+  // registers to the two softmax warpgroups (56 * 128 + 224 * 256 = 168 * 384).  The
+  // adjustment sits inside each role's branch so the compiler budgets each region.
+  if (warp < 4) {
+  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
   if (warp == 0) {
     // ================================================================ TMA producer
-    int32_t* s_pages = reinterpret_cast<int32_t*>(sm + C::kPageOff);
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
     if (lane == 0) {
       tma_prefetch_desc(&qmap);
@@ -216,65 +377,69 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                       g * p.G, node0, b);
       }
     }
-    int issued = 0;
-    bool ok = true;
-    for (int j = 0; j < T && ok; ++j) {
-      if (j % kPageWindowTiles == 0) {
-        // Page ids of tiles [k0 + j, k0 + j + window): OOB id (zero fill) past the end.
-        int bad = 0;
-        for (int e = lane; e < kPageWindowTiles * kPagesPerTile; e += 32) {
-          const int tile = k0 + j + e / kPagesPerTile;
-          const int pl = tile * kPagesPerTile + (e % kPagesPerTile);
-          int pid = p.num_pages;
-          if (tile < k1 && pl * kPage < L) {
-            const int v = bt[pl];
-            if (v < 0 || v >= p.num_pages) bad = 1;
-            else pid = v;
-          }
-          s_pages[e] = pid;
-        }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.dev_err, JF_DEVERR_BAD_PAGE);
-        __syncwarp();
+    // Page ids travel through registers: lane q < 8 holds page q of the next kLookahead
+    // tiles, loaded kLookahead tiles before use so the block-table latency overlaps the
+    // wait for free stages.  Pages past the sequence end (and malformed ids, reported)
+    // become the out-of-bounds id num_pages, which TMA fills with zeros.
+    constexpr int kLookahead = 4;
+    auto load_pid = [&](int j) -> int {
+      const int pl = (k0 + j) * kPagesPerTile + lane;
+      if (lane >= kPagesPerTile || j >= T || pl * kPage >= L) return p.num_pages;
+      return __ldg(bt + pl);
+    };
+    int pid[kLookahead];
+#pragma unroll
+    for (int u = 0; u < kLookahead; ++u) pid[u] = load_pid(u);
+    int bad = 0;
+    // One TMA box per (page, 64-column half): lanes [0, 8 * halves) issue them in parallel.
+    auto issue = [&](uint8_t* ring, const CUtensorMap* map, uint64_t* full, int st, int page) {
+      if (lane < kPagesPerTile * C::kHalves) {
+        const int q = lane % kPagesPerTile, hh = lane / kPagesPerTile;
+        tma_load_3d(ring + st * C::kTileBytes + hh * C::kHalfBytes + q * (kPage * 128), map, full,
+                    hh * 64, g, page * kPage);
       }
+    };
+    int k_issued = 0, v_issued = 0;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      int mine = pid[0];
+      if (mine < 0 || mine > p.num_pages) { bad = 1; mine = p.num_pages; }
+      else if (mine == p.num_pages && lane < kPagesPerTile &&
+               ((k0 + j) * kPagesPerTile + lane) * kPage < L) bad = 1;
+      const int page = __shfl_sync(0xffffffffu, mine, lane % kPagesPerTile);
+#pragma unroll
+      for (int u = 0; u < kLookahead - 1; ++u) pid[u] = pid[u + 1];
+      pid[kLookahead - 1] = load_pid(j + kLookahead);
+      const int st = j % S;
+      const uint32_t reuse_parity = static_cast<uint32_t>((j / S) - 1) & 1u;
       int okl = 1;
       if (lane == 0) {
-        const int st = j % S;
-        const uint32_t reuse_parity = static_cast<uint32_t>((j / S) - 1) & 1u;
-        const int* pg = s_pages + (j % kPageWindowTiles) * kPagesPerTile;
         if (j >= S && !mbar_wait(&k_empty[st], reuse_parity, abort)) okl = 0;
-        if (okl) {
-          mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
-          uint8_t* dst = k_s + st * C::kTileBytes;
-          for (int q = 0; q < kPagesPerTile; ++q)
-            for (int hh = 0; hh < C::kHalves; ++hh)
-              tma_load_3d(dst + hh * C::kHalfBytes + q * (kPage * 128), &kmap, &k_full[st],
-                          hh * 64, g, pg[q] * kPage);
-        }
-        if (okl && j >= S && !mbar_wait(&v_empty[st], reuse_parity, abort)) okl = 0;
-        if (okl) {
-          mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
-          uint8_t* dst = v_s + st * C::kTileBytes;
-          for (int q = 0; q < kPagesPerTile; ++q)
-            for (int hh = 0; hh < C::kHalves; ++hh)
-              tma_load_3d(dst + hh * C::kHalfBytes + q * (kPage * 128), &vmap, &v_full[st],
-                          hh * 64, g, pg[q] * kPage);
-          issued = j + 1;
-        } else {
-          set_abort(abort, p.dev_err);
-        }
+        else mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
       }
-      ok = __shfl_sync(0xffffffffu, okl, 0) != 0;
+      if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+      issue(k_s, &kmap, &k_full[st], st, page);
+      k_issued = j + 1;
+      if (lane == 0) {
+        if (j >= S && !mbar_wait(&v_empty[st], reuse_parity, abort)) okl = 0;
+        else mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+      }
+      if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+      issue(v_s, &vmap, &v_full[st], st, page);
+      v_issued = j + 1;
     }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.dev_err, JF_DEVERR_BAD_PAGE);
+    if (!ok && lane == 0) set_abort(abort, p.dev_err);
+    __syncwarp();
     // Drain: make sure no copy is still landing in shared memory when the CTA exits.
     if (lane == 0) {
       int zero_q = 0;
       mbar_wait(&q_full, 0, &zero_q);
-      for (int j = max(0, issued - S); j < issued; ++j) {
-        const uint32_t par = static_cast<uint32_t>(j / S) & 1u;
-        int zero = 0;
-        mbar_wait(&k_full[j % S], par, &zero);
-        mbar_wait(&v_full[j % S], par, &zero);
-      }
+      int zero = 0;
+      for (int j = max(0, k_issued - S); j < k_issued; ++j)
+        mbar_wait(&k_full[j % S], static_cast<uint32_t>(j / S) & 1u, &zero);
+      for (int j = max(0, v_issued - S); j < v_issued; ++j)
+        mbar_wait(&v_full[j % S], static_cast<uint32_t>(j / S) & 1u, &zero);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -332,6 +497,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         if (lane == 0) {
           tc_fence_after();
           issue_pv(t, st, j > 0);
+          if (t == NT - 1) mma_commit(&v_empty[st]);    // V tile j no longer needed
         }
         if (j + 1 < T) {
           const int st1 = (j + 1) % S;
@@ -346,10 +512,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) {
-        mma_commit(&v_empty[st]);
-        if (j + 1 < T) mma_commit(&k_empty[(j + 1) % S]);
-      }
+      if (lane == 0 && j + 1 < T) mma_commit(&k_empty[(j + 1) % S]);
       __syncwarp();
     }
     if (!ok) set_abort(abort, p.dev_err);
@@ -360,7 +523,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       mbar_wait(&fin, 0, &zero);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  }
+  } else {
+    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
     // ================================================================ softmax / epilogue
     const int t = (warp >> 2) - 1;
     const int wq = warp & 3;
@@ -394,19 +559,31 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       tmem_ld128(tS, sr);
       float* sv = reinterpret_cast<float*>(sr);
       const int key0 = (k0 + j) * kKeyTile;
-      if (key0 + kKeyTile > P) {
+      const bool masked_tile = key0 + kKeyTile > P;
+      if (masked_tile) {
+        // Visibility of the tile's 128 keys as four 32-bit words: prefix keys always,
+        // tree key j iff bit j of the node's ancestor mask, nothing past the sequence end.
+        const int pre = min(max(P - key0, 0), kKeyTile);
+        const int end = min(max(L - key0, 0), kKeyTile);
+        uint32_t vis[4];
 #pragma unroll
-        for (int c = 0; c < kKeyTile; ++c) {
-          const int tk = key0 + c;
-          const int jt = tk - P;
-          bool vis = tk < P;
-          if (!vis && tk < L) vis = (my_mask[jt >> 6] >> (jt & 63)) & 1ull;
-          if (!vis) sv[c] = -INFINITY;
+        for (int w = 0; w < 4; ++w) {
+          const int c0 = 32 * w;
+          uint32_t m = mask_bits32(my_mask, W, key0 + c0 - P);
+          const int np = min(max(pre - c0, 0), 32);
+          const int ne = min(max(end - c0, 0), 32);
+          m |= np >= 32 ? 0xFFFFFFFFu : ((1u << np) - 1u);
+          m &= ne >= 32 ? 0xFFFFFFFFu : ((1u << ne) - 1u);
+          vis[w] = m;
         }
-      }
-      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kKeyTile; ++c) mx = fmaxf(mx, sv[c]);
+        for (int c = 0; c < kKeyTile; ++c)
+          if (!((vis[c >> 5] >> (c & 31)) & 1u)) sv[c] = -INFINITY;
+      }
+      float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+      for (int c = 4; c < kKeyTile; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
+      const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
       const float mt = mx * sl2;
       const bool raise = mt > m_run + kRescaleThreshold;
       const float m_old = m_run;
@@ -414,14 +591,27 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const float corr = raise ? fast_exp2(m_old - m_run) : 1.f;   // 0 when m_old = -inf
       const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
       uint32_t pk[64];
-      float ls = 0.f;
+      const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
+      uint64_t ls2[2] = {0ull, 0ull};       // paired partial row sums (0ull == {+0, +0})
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(fmaf(sv[2 * c], sl2, neg));
-        const float p1 = fast_exp2(fmaf(sv[2 * c + 1], sl2, neg));
-        ls += p0 + p1;
+        float x0, x1;
+        f2_split(ffma2(f2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2), x0, x1);
+        float p0, p1;
+        if (!masked_tile && kPolyEvery > 0 && c % kPolyMod == kPolyMod - 1) {
+          p0 = exp2_poly(x0);             // finite scores only (prefix tiles)
+          p1 = exp2_poly(x1);
+        } else {
+          p0 = fast_exp2(x0);
+          p1 = fast_exp2(x1);
+        }
+        ls2[c & 1] = fadd2(ls2[c & 1], f2(p0, p1));
         pk[c] = pack_bf16x2(p0, p1);
       }
+      float la, lb, lc, ld;
+      f2_split(ls2[0], la, lb);
+      f2_split(ls2[1], lc, ld);
+      const float ls = (la + lb) + (lc + ld);
       l = l * corr + ls;
       tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
@@ -443,82 +633,156 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
-    if (ok && wait_warp(&o_full, 0, abort)) {
+    // Every thread of the warpgroup reaches this vote (all waits are bounded), so the
+    // epilogue's own barriers are entered by all of them or by none.
+    const bool done = named_bar_and(1 + t, 128, ok && wait_warp(&o_full, 0, abort));
+    if (p.cluster_merge) {
+      // Normalised fp32 row and its LSE stay in this CTA's shared memory for the merge.
+      float lse2 = -INFINITY;
+      if (done) {
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        lse2 = l > 0.f ? m_run + __log2f(l) : -INFINITY;
+        uint8_t* dstrow = reinterpret_cast<uint8_t*>(part_row<NT, D>(sm, t, rl));
+        const uint32_t sw = static_cast<uint32_t>(rl & 7);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint32_t k = static_cast<uint32_t>(c * 8 + v);
+            *reinterpret_cast<float4*>(dstrow + ((k ^ sw) << 4)) =
+                make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                            __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          }
+        }
+      } else {
+        set_abort(abort, p.dev_err);
+      }
+      part_lse<NT, D>(sm, t)[rl] = lse2;
+    } else if (done) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse2 = l > 0.f ? m_run + __log2f(l) : -INFINITY;
-      const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.N + i;
+      // Every MMA has completed, so the K/V ring is free: stage this tile's output rows
+      // there in the 128-byte-swizzled layout of the TMA box (16-byte chunk k of row r at
+      // chunk k ^ (r % 8)), then one thread stores the tile with TMA.
+      const int tile_row0 = (mp * NT + t) * kRowTile;
+      const uint32_t sw = static_cast<uint32_t>(rl & 7);
+      if (p.splits == 1) {
+        uint8_t* stg = sm + C::kKOff + t * C::kTileBytes;          // [half][128 rows][128 B]
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        tmem_ld_wait(o);
-        if (valid) {
-          if (p.splits == 1) {
-            uint4* dst = reinterpret_cast<uint4*>(
-                p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * D + c * 32);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+          uint8_t* half = stg + (c >> 1) * C::kHalfBytes + rl * 128;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-              dst[v] = w;
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(p.ws_o + (row * p.splits + split) * D + c * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                   __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            const uint32_t k = static_cast<uint32_t>((c & 1) * 4 + v);
+            *reinterpret_cast<uint4*>(half + ((k ^ sw) << 4)) = w;
           }
+        }
+        fence_proxy_async_smem();
+        named_bar(1 + t, 128);
+        if (rl == 0) {
+          for (int hh = 0; hh < C::kHalves; ++hh)
+            tma_store_4d(&omap, stg + hh * C::kHalfBytes, hh * 64, g * p.G, node_base, b);
+          bulk_commit();
+          bulk_wait_all();
+        }
+      } else {
+        uint8_t* stg = sm + C::kKOff + t * 2 * C::kTileBytes;      // [32-col block][128 rows][128 B]
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+          uint8_t* blk = stg + c * C::kHalfBytes + rl * 128;
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(blk + ((static_cast<uint32_t>(v) ^ sw) << 4)) =
+                make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                            __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+        }
+        fence_proxy_async_smem();
+        named_bar(1 + t, 128);
+        if (rl == 0) {
+          const int plane = (b * p.Hkv + g) * p.splits + split;
+          for (int c = 0; c < D / 32; ++c)
+            tma_store_3d(&wmap, stg + c * C::kHalfBytes, c * 32, tile_row0, plane);
+          bulk_commit();
+          bulk_wait_all();
         }
       }
       if (valid) {
         if (p.splits == 1) {
-          if (p.lse != nullptr) p.lse[row] = lse2 * 0.69314718055994531f;
+          if (p.lse != nullptr)
+            p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.N + i] = lse2 * 0.69314718055994531f;
         } else {
-          p.ws_lse[row * p.splits + split] = lse2;
+          p.ws_lse[((static_cast<size_t>(b) * p.Hkv + g) * p.splits + split) * p.M + r] = lse2;
         }
       }
-    } else if (!ok) {
+    } else {
       set_abort(abort, p.dev_err);
     }
   }
+
+  if (p.cluster_merge) merge_cluster<NT, D>(sm, p, b, g, mp, split);
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Merges split partials: O = sum_s 2^(lse_s - lse) O_s,  lse = log2 sum_s 2^lse_s.
-// One warp per output row (b, h, i); each lane owns D/32 consecutive columns.
+// One warp per output row, rows enumerated in the output's [B][N][Hq] order so that
+// consecutive warps write consecutive rows; each lane owns D/32 consecutive columns.
 template <int D>
 __global__ void __launch_bounds__(256)
     tree_attention_combine_kernel(const float* __restrict__ ws_o,
                                   const float* __restrict__ ws_lse, int splits, int N, int Hq,
-                                  long long rows, uint16_t* __restrict__ out,
+                                  int Hkv, long long rows, uint16_t* __restrict__ out,
                                   float* __restrict__ lse) {
   constexpr int E = D / 32;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  // Launched as a programmatic dependent of the split kernel: wait for its results.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long rr = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float* ls = ws_lse + row * splits;
+  if (rr >= rows) return;
+  const int h = static_cast<int>(rr % Hq);
+  const long long bi = rr / Hq;
+  const int i = static_cast<int>(bi % N);
+  const long long b = bi / N;
+  const int G = Hq / Hkv;
+  const int g = h / G;
+  const long long M = static_cast<long long>(N) * G;
+  const long long r = static_cast<long long>(i) * G + (h % G);
+  const long long base = (b * Hkv + g) * splits;       // partial row of split s: (base + s) * M + r
   float mx = -INFINITY;
-  for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, ls[s]);
+  for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, ws_lse[(base + s) * M + r]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float wsum = 0.f;
+#pragma unroll 4
   for (int s = 0; s < splits; ++s) {
-    const float l = ls[s];
+    const long long prow = (base + s) * M + r;
+    const float l = ws_lse[prow];
     const float w = (l == -INFINITY) ? 0.f : exp2f(l - mx);
     wsum += w;
-    const float* o = ws_o + (row * splits + s) * D + lane * E;
+    const float* o = ws_o + prow * D + lane * E;
 #pragma unroll
     for (int e = 0; e < E; e += 4) {
       const float4 v = *reinterpret_cast<const float4*>(o + e);
@@ -529,11 +793,7 @@ __global__ void __launch_bounds__(256)
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const int i = static_cast<int>(row % N);
-  const long long bh = row / N;
-  const int h = static_cast<int>(bh % Hq);
-  const long long b = bh / Hq;
-  uint16_t* dst = out + ((b * N + i) * Hq + h) * D + lane * E;
+  uint16_t* dst = out + rr * D + lane * E;
   uint32_t packed[E / 2];
 #pragma unroll
   for (int e = 0; e < E; e += 2) packed[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
@@ -543,15 +803,74 @@ __global__ void __launch_bounds__(256)
     *reinterpret_cast<uint32_t*>(dst) = packed[0];
   }
   if (lse != nullptr && lane == 0)
-    lse[row] = (wsum > 0.f ? mx + __log2f(wsum) : -INFINITY) * 0.69314718055994531f;
+    lse[(b * Hq + h) * N + i] = (wsum > 0.f ? mx + __log2f(wsum) : -INFINITY) * 0.69314718055994531f;
 }
 
 // ------------------------------------------------------------------------ host side
 
 struct AttnPlan {
   int NT, n_groups, splits, chunk_tiles;
+  bool cluster;          // splits merged through distributed shared memory (no workspace)
   size_t ws_bytes;
 };
+
+template <int NT, int D>
+bool ensure_smem_attr() {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && done[dev]) return true;
+  if (cudaFuncSetAttribute(tree_attention_kernel<NT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<NT, D>::kSmemBytes) != cudaSuccess)
+    return false;
+  if (dev < 64) done[dev] = true;
+  return true;
+}
+
+// How many clusters of `s` CTAs of this kernel fit on the current device at once
+// (0 if that cluster shape cannot be launched).  Cached per device.
+template <int NT, int D>
+int cluster_capacity(int s) {
+  static std::mutex mu;
+  static int cache[64][9];
+  static bool init = false;
+  int dev = 0;
+  if (s < 2 || s > 8 || cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& row : cache)
+      for (int& v : row) v = -1;
+    init = true;
+  }
+  if (cache[dev][s] >= 0) return cache[dev][s];
+  int n = 0;
+  if (ensure_smem_attr<NT, D>()) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(s) * 64);
+    cfg.blockDim = dim3(Cfg<NT, D>::kThreads);
+    cfg.dynamicSmemBytes = Cfg<NT, D>::kSmemBytes;
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = static_cast<unsigned>(s);
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, tree_attention_kernel<NT, D>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+  }
+  cache[dev][s] = n;
+  return n;
+}
+
+int cluster_capacity_for(int NT, int D, int s) {
+  if (D == 128) return NT == 2 ? cluster_capacity<2, 128>(s) : cluster_capacity<1, 128>(s);
+  return NT == 2 ? cluster_capacity<2, 64>(s) : cluster_capacity<1, 64>(s);
+}
 
 bool shape_supported(int B, int N, int Hq, int Hkv, int D, int max_pages, int page_size) {
   if (B < 1 || N < 1 || N > JF_MAX_NODES || Hq < 1 || Hkv < 1 || max_pages < 1) return false;
@@ -576,30 +895,44 @@ bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms
   const int max_tiles = (max_pages * kPage + kKeyTile - 1) / kKeyTile;
   const long long units = static_cast<long long>(B) * Hkv * pl->n_groups;
   if (sms <= 0) sms = 148;
-  // Time model (arbitrary units of one key tile of one row tile at full tensor speed):
-  // waves * (tiles per split + prologue) * max(compute, HBM share), plus the merge.
+  // Time model: waves * (tiles per split + prologue/epilogue) * max(tensor time of a key
+  // tile, its share of HBM bandwidth), plus, for workspace splits, writing and re-reading
+  // the partials and one more launch.  Cluster splits (2..8 CTAs merging through DSMEM)
+  // pay no merge traffic but pack fewer CTAs per wave.
   const double hbm_per_tile = 2.0 * kKeyTile * D * 2;          // K + V bytes per key tile
   const double flops_per_tile = 4.0 * kRowTile * kKeyTile * D;  // QK^T + PV per row tile
   const double per_sm_flops = 1.9e15 / sms, hbm = 6.5e12;
+  auto t_tile = [&](double active) {
+    return std::max(pl->NT * flops_per_tile / per_sm_flops, hbm_per_tile * active / hbm);
+  };
   double best = 1e300;
   int best_s = 1;
+  bool best_cluster = false;
   for (int s = 1; s <= max_tiles; ++s) {
     const int chunk = (max_tiles + s - 1) / s;
     if (s > 1 && (s - 1) * chunk >= max_tiles) continue;         // last split would be empty
     const long long ctas = units * s;
     const long long waves = (ctas + sms - 1) / sms;
-    const double active = static_cast<double>(std::min<long long>(ctas, sms));
-    const double t_tile = std::max(pl->NT * flops_per_tile / per_sm_flops, hbm_per_tile * active / hbm);
-    double est = waves * (chunk + 1.5) * t_tile;
+    double est = waves * (chunk + 1.5) * t_tile(static_cast<double>(std::min<long long>(ctas, sms)));
     if (s > 1) {
       const double part = static_cast<double>(B) * Hq * N * s * (D + 1) * 4.0;
-      est += 3e-6 + 2.0 * part / hbm;
+      est += 1.5e-6 + 2.0 * part / hbm;
     }
-    if (est < best * 0.98) { best = est; best_s = s; }
+    if (est < best * 0.98) { best = est; best_s = s; best_cluster = false; }
+    // Clusters only when every cluster of the grid is resident at once: with several
+    // waves, a finished cluster must wait for s SMs of one GPC to free up together.
+    const int cap = (s >= 2 && s <= 8) ? cluster_capacity_for(pl->NT, D, s) : 0;
+    if (cap > 0 && units <= cap) {
+      const double est_c = (chunk + 1.5) * t_tile(static_cast<double>(units * s)) + 4e-6;
+      if (est_c < best * 0.98) { best = est_c; best_s = s; best_cluster = true; }
+    }
   }
   pl->splits = best_s;
+  pl->cluster = best_cluster;
   pl->chunk_tiles = (max_tiles + best_s - 1) / best_s;
-  pl->ws_bytes = best_s > 1 ? static_cast<size_t>(B) * Hq * N * best_s * (D + 1) * sizeof(float) + 256 : 0;
+  pl->ws_bytes = (best_s > 1 && !best_cluster)
+                     ? static_cast<size_t>(B) * Hq * N * best_s * (D + 1) * sizeof(float) + 256
+                     : 0;
   return true;
 }
 
@@ -618,36 +951,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
+            const cuuint64_t* strides, const cuuint32_t* box,
+            CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+  return fn(m, dt, rank, const_cast<void*>(base), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int NT, int D>
 jf_status launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                 const AttnParams& prm, long long grid, cudaStream_t s) {
+                 const CUtensorMap& om, const CUtensorMap& wm, const AttnParams& prm,
+                 long long grid, cudaStream_t s) {
   using C = Cfg<NT, D>;
-  static std::mutex mu;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 64 || !attr_set[dev]) {
-      if (cudaFuncSetAttribute(tree_attention_kernel<NT, D>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-          cudaSuccess)
-        return JF_ERR_CUDA;
-      if (dev < 64) attr_set[dev] = true;
-    }
+  if (!ensure_smem_attr<NT, D>()) return JF_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(grid));
+  lc.blockDim = dim3(C::kThreads);
+  lc.dynamicSmemBytes = C::kSmemBytes;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (prm.cluster_merge) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(prm.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
   }
-  tree_attention_kernel<NT, D><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, s>>>(
-      qm, km, vm, prm);
-  return launch_status();
+  const cudaError_t e = cudaLaunchKernelEx(&lc, tree_attention_kernel<NT, D>, qm, km, vm, om, wm, prm);
+  return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
 
 }  // namespace
@@ -693,8 +1028,11 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
     if (!aligned_to(workspace, 16)) return JF_ERR_MISALIGNED;
   }
   const int G = Hq / Hkv;
-  CUtensorMap qm, km, vm;
+  CUtensorMap qm, km, vm, om, wm;
+  std::memset(&om, 0, sizeof(om));
+  std::memset(&wm, 0, sizeof(wm));
   {
+    // q and out share one layout: [B][N][Hq][D], 128-row tiles of (node, head-in-group).
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
                                 static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
@@ -702,6 +1040,18 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
                                    static_cast<cuuint64_t>(N) * Hq * D * 2};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kRowTile / G), 1};
     if (!encode(&qm, q, 4, dims, strides, box)) return JF_ERR_CUDA;
+    if (pl.splits == 1 && !encode(&om, out, 4, dims, strides, box)) return JF_ERR_CUDA;
+  }
+  if (pl.splits > 1 && !pl.cluster) {
+    // split partials O_s: fp32 [B * Hkv * splits][M][D], stored in 32-column boxes
+    const long long M = static_cast<long long>(N) * G;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(M),
+                                static_cast<cuuint64_t>(B) * Hkv * pl.splits};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
+                                   static_cast<cuuint64_t>(M) * D * 4};
+    const cuuint32_t box[3] = {32, kRowTile, 1};
+    if (!encode(&wm, workspace, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return JF_ERR_CUDA;
   }
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
@@ -726,27 +1076,40 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
   prm.max_pages = max_pages; prm.num_pages = num_pages;
   prm.n_groups = pl.n_groups; prm.splits = pl.splits; prm.chunk_tiles = pl.chunk_tiles;
   prm.M = N * G;
+  prm.cluster_merge = pl.cluster ? 1 : 0;
   prm.scale_log2 = scale * 1.4426950408889634f;
   const long long grid = static_cast<long long>(B) * Hkv * pl.splits * pl.n_groups;
   if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   jf_status st;
   if (D == 128)
-    st = pl.NT == 2 ? launch<2, 128>(qm, km, vm, prm, grid, s) : launch<1, 128>(qm, km, vm, prm, grid, s);
+    st = pl.NT == 2 ? launch<2, 128>(qm, km, vm, om, wm, prm, grid, s)
+                    : launch<1, 128>(qm, km, vm, om, wm, prm, grid, s);
   else
-    st = pl.NT == 2 ? launch<2, 64>(qm, km, vm, prm, grid, s) : launch<1, 64>(qm, km, vm, prm, grid, s);
+    st = pl.NT == 2 ? launch<2, 64>(qm, km, vm, om, wm, prm, grid, s)
+                    : launch<1, 64>(qm, km, vm, om, wm, prm, grid, s);
   if (st != JF_OK) return st;
-  if (pl.splits > 1) {
+  if (pl.splits > 1 && !pl.cluster) {
     const long long nb = (static_cast<long long>(rows) + 7) / 8;
-    if (D == 128)
-      tree_attention_combine_kernel<128><<<static_cast<unsigned>(nb), 256, 0, s>>>(
-          prm.ws_o, prm.ws_lse, pl.splits, N, Hq, static_cast<long long>(rows),
-          static_cast<uint16_t*>(out), lse);
-    else
-      tree_attention_combine_kernel<64><<<static_cast<unsigned>(nb), 256, 0, s>>>(
-          prm.ws_o, prm.ws_lse, pl.splits, N, Hq, static_cast<long long>(rows),
-          static_cast<uint16_t*>(out), lse);
-    return launch_status();
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(static_cast<unsigned>(nb));
+    lc.blockDim = dim3(256);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const float* wso = prm.ws_o;
+    const float* wsl = prm.ws_lse;
+    const int nsp = pl.splits;
+    const long long nrows = static_cast<long long>(rows);
+    uint16_t* o16 = static_cast<uint16_t*>(out);
+    const cudaError_t e =
+        D == 128 ? cudaLaunchKernelEx(&lc, tree_attention_combine_kernel<128>, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse)
+                 : cudaLaunchKernelEx(&lc, tree_attention_combine_kernel<64>, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse);
+    return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
   }
   return JF_OK;
 }

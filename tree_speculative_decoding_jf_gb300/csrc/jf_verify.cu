@@ -10,10 +10,10 @@
 // writes a packed 64-bit key (order-preserving value bits << 32 | ~index) into the
 // workspace; max over keys gives the largest value and, among equal values, the smallest
 // index.  Chunks per row are chosen so that rows x chunks fills the GPU.
-// Kernel 2 (one CTA per sequence): merges the chunk keys into argmax, finds depths by
-// pointer jumping, computes accepted-subtree lengths level by level from the deepest
-// level up with shared-memory atomicMax on (len + 1) << 16 | (0xFFFF - child), and walks
-// the best children from the root.
+// Kernel 2 (one CTA per sequence): merges the chunk keys into argmax (a warp per row),
+// finds depths by pointer jumping, computes accepted-subtree lengths level by level from
+// the deepest level up with shared-memory atomicMax on (len + 1) << 16 | (0xFFFF - child),
+// and walks the best children from the root.
 #include <algorithm>
 #include <mutex>
 
@@ -156,19 +156,29 @@ __global__ void __launch_bounds__(kWalkThreads)
   int32_t* s_anc = s_dep + N;     // [N] ancestor pointer (pointer jumping)
   uint32_t* s_key = reinterpret_cast<uint32_t*>(s_anc + N);   // [N] best accepted child
   int32_t* s_path = reinterpret_cast<int32_t*>(s_key + N);    // [N]
+  int32_t* s_draft = s_path + N;                               // [N]
   __shared__ int s_flag;
   __shared__ int s_len;
 
   const int b = blockIdx.x;
   const size_t rb = static_cast<size_t>(b) * N;
+  // Chunk keys of each row: one warp per row, lanes over chunks, shuffle max.
+  {
+    const int lane = threadIdx.x & 31;
+    for (int i = threadIdx.x >> 5; i < N; i += blockDim.x >> 5) {
+      const uint64_t* pk = part + (rb + i) * chunks;
+      uint64_t k = 0;
+      for (int c = lane; c < chunks; c += 32) k = max(k, pk[c]);
+      k = warp_max_u64(k);
+      if (lane == 0) {
+        const int am = static_cast<int>(~static_cast<uint32_t>(k & 0xFFFFFFFFull));
+        s_am[i] = am;
+        if (argmax_out != nullptr) argmax_out[rb + i] = am;
+      }
+    }
+  }
   int bad_parent = 0, bad_token = 0;
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    uint64_t k = 0;
-    const uint64_t* pk = part + (rb + i) * chunks;
-    for (int c = 0; c < chunks; ++c) k = max(k, pk[c]);
-    const int am = static_cast<int>(~static_cast<uint32_t>(k & 0xFFFFFFFFull));
-    s_am[i] = am;
-    if (argmax_out != nullptr) argmax_out[rb + i] = am;
     int p = parent[rb + i];
     const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
     if (!ok) { bad_parent = 1; p = -1; }
@@ -176,10 +186,9 @@ __global__ void __launch_bounds__(kWalkThreads)
     s_anc[i] = p;
     s_dep[i] = p >= 0 ? 1 : 0;
     s_key[i] = 0u;
-    if (i > 0) {
-      const int d = draft[rb + i];
-      if (d < 0 || d >= V) bad_token = 1;
-    }
+    const int d = draft[rb + i];
+    s_draft[i] = d;
+    if (i > 0 && (d < 0 || d >= V)) bad_token = 1;
   }
   bad_parent = __syncthreads_or(bad_parent);
   bad_token = __syncthreads_or(bad_token);
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kWalkThreads)
   for (int d = maxd; d >= 1; --d) {
     for (int i = threadIdx.x; i < N; i += blockDim.x) {
       const int p = s_par[i];
-      if (s_dep[i] == d && p >= 0 && draft[rb + i] == s_am[p]) {
+      if (s_dep[i] == d && p >= 0 && s_draft[i] == s_am[p]) {
         const uint32_t len = (s_key[i] >> 16) + 1u;
         atomicMax(&s_key[p], (len << 16) | static_cast<uint32_t>(0xFFFF - i));
       }
@@ -309,7 +318,7 @@ extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int
     jf::argmax_chunk_kernel<float><<<static_cast<unsigned>(grid), jf::kArgmaxThreads, 0, s>>>(
         static_cast<const float*>(logits), V, p.chunks, p.chunk_len, part);
   if (cudaGetLastError() != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * 6 * sizeof(int32_t);
+  const size_t smem = static_cast<size_t>(N) * 7 * sizeof(int32_t);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
@@ -378,7 +387,7 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
     jf::argmax_chunk_kernel<float><<<grid, jf::kArgmaxThreads, 0, s>>>(
         static_cast<const float*>(logits), V, p.chunks, p.chunk_len, part);
   if (cudaGetLastError() != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * 6 * sizeof(int32_t);
+  const size_t smem = static_cast<size_t>(N) * 7 * sizeof(int32_t);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
