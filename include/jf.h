@@ -122,9 +122,10 @@ size_t jf_tree_attention_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_
  *                (may be NULL when that size is 0); contents need no initialisation.
  *   dev_err      JF_DEVERR_BAD_PAGE / _BAD_PREFIX / _TIMEOUT.  May be NULL.
  * Limits: D in {64, 128}; page_size == 16; Hq % Hkv == 0 and G = Hq / Hkv a power of
- * two <= 128; N * G rows per kv-head split into 128-row tiles; 1 <= N <= 2048 * G / 128
- * ... capped at JF_MAX_NODES; q, caches and out 16-byte aligned.  Others return
- * JF_ERR_UNSUPPORTED.
+ * two <= 128; 1 <= N <= JF_MAX_NODES; max_pages * page_size >= N; q, the caches, out and
+ * the workspace 16-byte aligned, mask 8-byte aligned.  Others return JF_ERR_UNSUPPORTED /
+ * JF_ERR_MISALIGNED.  Every slot of the tree region must hold finite K/V values; slots past
+ * P_b + N in the last page may hold anything (they are zeroed on chip before use).
  */
 jf_status jf_tree_attention(const void* q, const void* k_cache, const void* v_cache,
                             const int32_t* block_table, const int32_t* prefix_len,

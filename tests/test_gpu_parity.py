@@ -290,6 +290,7 @@ SHAPES = [  # B, N, Hq, Hkv, D, P, tree
     (1, 130, 1, 1, 64, 70, "random"),        # G = 1, ragged multiword mask
     (1, 1024, 4, 1, 128, 64, "random"),      # many nodes, W = 16
     (2, 7, 128, 1, 64, 33, "random"),        # G = 128: one node per row tile
+    (1, 2048, 2, 2, 64, 100, "random"),      # G = 1, W = 32: deep tree over many key tiles
 ]
 
 

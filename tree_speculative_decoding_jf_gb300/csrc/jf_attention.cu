@@ -14,11 +14,11 @@
 // split go to a workspace and a second kernel merges them by log-sum-exp.
 //
 // Roles inside a CTA (128 * (1 + NT) threads):
-//   warp 0      TMA producer: stages the split's page ids from the block table in shared
-//               memory (bounds-checked, eight loads in flight per lane; the first stages'
-//               ids first), loads the Q tiles once, then per key tile one TMA box per
-//               (16-key page, 64-column half) of K and of V -- issued by 16 lanes at once --
-//               into a STAGES-deep ring.  Pages past the sequence end load as zeros.
+//   warp 0      TMA producer: page ids travel through registers four tiles ahead (bounds-
+//               checked at use); Q is loaded once; per key tile K then V go into a
+//               STAGES-deep ring as one 128-row box per 64-column half when the tile's eight
+//               pages are consecutive in the pool, else one box per (page, half) issued by
+//               16 lanes at once.  Pages past the sequence end load as zeros.
 //   warp 1      allocates TMEM and issues tcgen05.mma from one lane:
 //                 S_t = Q_t K^T  (128 x 128, fp32 in TMEM),  O_t += P_t V  (P from TMEM).
 //               A V stage is released as soon as the tile's last PV MMA is issued, a K
@@ -57,20 +57,25 @@ constexpr int kKeyTile = 128;     // keys per pipeline stage
 constexpr int kRowTile = 128;     // rows per tensor-core tile (TMEM lanes)
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kKeyTile / kPage;
-constexpr int kMaskBytesPerTile = 8192;                 // staged mask words per row tile
 constexpr float kRescaleThreshold = 8.0f;               // log2 units
 
 template <int NT, int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;                  // 128-byte swizzle atoms per row
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  // V stages are released only when a tile's last PV MMA completes, K stages as soon as
+  // the next tile's S MMAs are issued, so V gets the deeper ring.
+  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kVStages = (D == 64) ? 6 : 3;
   static constexpr int kTileBytes = kRowTile * D * 2;     // one 128-row bf16 tile
   static constexpr int kHalfBytes = kRowTile * 128;       // one 64-column half of a tile
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + NT * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kMaskOff = kVOff + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kMaskOff + NT * kMaskBytesPerTile + 1024;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kRingBytes = (kKStages + kVStages) * kTileBytes;
+  // After the last MMA the ring holds the epilogue: fp32 rows [NT][128][D], then LSEs.
+  static constexpr int kPartLseOff = kKOff + NT * 2 * kTileBytes;
+  static_assert(NT * 2 * kTileBytes + NT * kRowTile * 4 <= kRingBytes, "epilogue fits the ring");
+  static constexpr int kSmemBytes = kKOff + kRingBytes + 1024;
   static constexpr int kThreads = 128 * (1 + NT);
   static constexpr uint32_t kTmemCols = (NT == 2) ? 512 : 256;
   static constexpr uint32_t kTmemO = 0;                   // O_t at column t*128
@@ -170,13 +175,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// Bits [j0, j0 + 32) of the little-endian bit string words[0 .. W) (zero outside it).
-__device__ __forceinline__ uint32_t mask_bits32(const uint64_t* words, int W, int j0) {
-  if (j0 <= -32 || j0 >= 64 * W) return 0u;
-  if (j0 < 0) return static_cast<uint32_t>(words[0] << (-j0));
-  const int wi = j0 >> 6, off = j0 & 63;
-  uint64_t v = words[wi] >> off;
-  if (off > 32 && wi + 1 < W) v |= words[wi + 1] << (64 - off);
+// Bits [rel, rel + 32) of the 192-bit little-endian window w[0..3) (zero outside it).
+__device__ __forceinline__ uint32_t window_bits32(const uint64_t (&w)[3], int rel) {
+  if (rel <= -32 || rel >= 192) return 0u;
+  if (rel < 0) return static_cast<uint32_t>(w[0] << (-rel));
+  const int wi = rel >> 6, off = rel & 63;
+  const uint64_t lo = wi == 0 ? w[0] : (wi == 1 ? w[1] : w[2]);
+  const uint64_t hi = wi == 0 ? w[1] : (wi == 1 ? w[2] : 0ull);
+  uint64_t v = lo >> off;
+  if (off > 32) v |= hi << (64 - off);
   return static_cast<uint32_t>(v);
 }
 
@@ -194,72 +201,83 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 
 // Split partials of one unit live in the shared memory of the cluster's CTAs: normalised
 // fp32 rows in the (idle) K/V ring, row r's 16-byte chunk k at chunk k ^ (r % 8), and the
-// log2-domain LSE of each row in the (idle) mask area.  CTA `rank` merges rows
-// [rank * R / S, (rank + 1) * R / S) of the unit's R = NT * 128 rows, one warp per row,
-// reading every split's row through distributed shared memory.
+// log2-domain LSE of each row right after them.  CTA `rank` merges rows
+// [rank * R / S, (rank + 1) * R / S) of the unit's R = NT * 128 rows through distributed
+// shared memory, batching the remote loads so each phase costs about one round trip.
 template <int NT, int D>
 __device__ __forceinline__ float* part_row(uint8_t* sm, int t, int row) {
   return reinterpret_cast<float*>(sm + Cfg<NT, D>::kKOff + (t * kRowTile + row) * (D * 4));
 }
 template <int NT, int D>
 __device__ __forceinline__ float* part_lse(uint8_t* sm, int t) {
-  return reinterpret_cast<float*>(sm + Cfg<NT, D>::kMaskOff + t * kMaskBytesPerTile);
+  return reinterpret_cast<float*>(sm + Cfg<NT, D>::kPartLseOff + t * kRowTile * 4);
 }
 
 template <int NT, int D>
 __device__ void merge_cluster(uint8_t* sm, const AttnParams& p, int b, int g, int mp, int rank) {
-  constexpr int E = D / 32;
+  constexpr int kChunks = D / 4;                         // 16-byte chunks per fp32 row
+  constexpr int kMaxSplits = 8;
   cluster_sync();                                        // every split's partial is written
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int S = p.splits;
   const int R = NT * kRowTile;
   const int per = (R + S - 1) / S;
-  const int r_lo = rank * per, r_hi = min(R, r_lo + per);
-  for (int rr = r_lo + warp; rr < r_hi; rr += nwarps) {
-    const int t = rr / kRowTile, row = rr % kRowTile;
-    const int rg = (mp * NT + t) * kRowTile + row;       // row within the kv-head group
-    if (rg >= p.M) continue;
-    float ls = -INFINITY;
-    if (lane < S) ls = dsmem_ld_f32(dsmem_addr(part_lse<NT, D>(sm, t) + row, lane));
-    float mx = ls;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float w = (ls == -INFINITY) ? 0.f : exp2f(ls - mx);
-    float wsum = w;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-    const uint32_t sw = static_cast<uint32_t>(row & 7);
-    uint32_t off;
-    if constexpr (E == 4) off = ((static_cast<uint32_t>(lane) ^ sw) << 4);
-    else off = (((static_cast<uint32_t>(lane) >> 1) ^ sw) << 4) + (lane & 1) * 8;
-    const float* mine = part_row<NT, D>(sm, t, row);
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  const int r_lo = rank * per;
+  const int nrows = max(0, min(R, r_lo + per) - r_lo);
+  // Scratch in this CTA's (idle) Q area: per merged row, the split weights.
+  float* s_w = reinterpret_cast<float*>(sm + Cfg<NT, D>::kQOff);          // [nrows][8]
+  // 1) every (row, split) LSE in one batch of remote loads
+  for (int e = threadIdx.x; e < nrows * S; e += blockDim.x) {
+    const int rr = r_lo + e / S, s2 = e % S;
+    s_w[(e / S) * kMaxSplits + s2] =
+        dsmem_ld_f32(dsmem_addr(part_lse<NT, D>(sm, rr / kRowTile) + rr % kRowTile, s2));
+  }
+  __syncthreads();
+  // 2) per row: weights 2^(lse_s - max) / sum and the merged LSE
+  for (int e = threadIdx.x; e < nrows; e += blockDim.x) {
+    float* w = s_w + e * kMaxSplits;
+    float mx = -INFINITY;
+    for (int s2 = 0; s2 < S; ++s2) mx = fmaxf(mx, w[s2]);
+    float sum = 0.f;
     for (int s2 = 0; s2 < S; ++s2) {
-      const float ws = __shfl_sync(0xffffffffu, w, s2);
-      if (ws == 0.f) continue;
-      const uint32_t a = dsmem_addr(reinterpret_cast<const uint8_t*>(mine) + off, s2);
-      if constexpr (E == 4) {
-        const float4 v = dsmem_ld_f32x4(a);
-        acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
-      } else {
-        const float2 v = dsmem_ld_f32x2(a);
-        acc[0] += ws * v.x; acc[1] += ws * v.y;
-      }
+      const float x = (w[s2] == -INFINITY) ? 0.f : exp2f(w[s2] - mx);
+      w[s2] = x;
+      sum += x;
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int i = rg / p.G, h = g * p.G + (rg % p.G);
-    uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * D + lane * E;
-    if constexpr (E == 4) {
-      *reinterpret_cast<uint2*>(dst) =
-          make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    }
-    if (p.lse != nullptr && lane == 0)
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
+    for (int s2 = 0; s2 < S; ++s2) w[s2] *= inv;
+    const int rr = r_lo + e;
+    const int rg = (mp * NT + rr / kRowTile) * kRowTile + rr % kRowTile;
+    if (p.lse != nullptr && rg < p.M) {
+      const int i = rg / p.G, h = g * p.G + (rg % p.G);
       p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.N + i] =
-          (wsum > 0.f ? mx + __log2f(wsum) : -INFINITY) * 0.69314718055994531f;
+          (sum > 0.f ? mx + __log2f(sum) : -INFINITY) * 0.69314718055994531f;
+    }
+  }
+  __syncthreads();
+  // 3) (row, 16-byte chunk) items: all splits' chunks are requested before any is used
+  for (int e = threadIdx.x; e < nrows * kChunks; e += blockDim.x) {
+    const int el = e / kChunks, k = e % kChunks;
+    const int rr = r_lo + el;
+    const int t = rr / kRowTile, row = rr % kRowTile;
+    const int rg = (mp * NT + t) * kRowTile + row;
+    if (rg >= p.M) continue;
+    const float* w = s_w + el * kMaxSplits;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(part_row<NT, D>(sm, t, row)) +
+                         ((static_cast<uint32_t>(k) ^ static_cast<uint32_t>(row & 7)) << 4);
+    float4 v[kMaxSplits];
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < S && w[s2] != 0.f) v[s2] = dsmem_ld_f32x4(dsmem_addr(src, s2));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < S && w[s2] != 0.f) {
+        acc.x += w[s2] * v[s2].x; acc.y += w[s2] * v[s2].y;
+        acc.z += w[s2] * v[s2].z; acc.w += w[s2] * v[s2].w;
+      }
+    const int i = rg / p.G, h = g * p.G + (rg % p.G);
+    uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * D + k * 4;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
   cluster_sync();                                        // nobody leaves while others read it
 }
@@ -269,19 +287,23 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     tree_attention_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
                           const __grid_constant__ CUtensorMap vmap,
+                          const __grid_constant__ CUtensorMap kmap_run,
+                          const __grid_constant__ CUtensorMap vmap_run,
                           const __grid_constant__ CUtensorMap omap,
                           const __grid_constant__ CUtensorMap wmap, const AttnParams p) {
   using C = Cfg<NT, D>;
-  constexpr int S = C::kStages;
+  constexpr int SK = C::kKStages;
+  constexpr int SV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t q_full, o_full, fin;
-  __shared__ uint64_t k_full[S], v_full[S], k_empty[S], v_empty[S];
+  __shared__ uint64_t k_full[SK], k_empty[SK], v_full[SV], v_empty[SV];
   __shared__ uint64_t s_full[NT], p_full[NT];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
+  grid_dependency_wait();
 
   // ---- which (b, kv-head, row-tile group, split) this CTA owns; split fastest, then the
   // row-tile group, so CTAs that read the same K/V tiles run side by side.
@@ -331,10 +353,12 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     mbar_init(&q_full, 1);
     mbar_init(&o_full, 1);
     mbar_init(&fin, 1);
-    for (int st = 0; st < S; ++st) {
+    for (int st = 0; st < SK; ++st) {
       mbar_init(&k_full[st], 1);
-      mbar_init(&v_full[st], 1);
       mbar_init(&k_empty[st], 1);
+    }
+    for (int st = 0; st < SV; ++st) {
+      mbar_init(&v_full[st], 1);
       mbar_init(&v_empty[st], 1);
     }
     for (int t = 0; t < NT; ++t) {
@@ -358,10 +382,10 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   uint8_t* v_s = sm + C::kVOff;
 
   // 384 threads x 168 registers at launch (NT == 2): the control warpgroup hands
-  // registers to the two softmax warpgroups (56 * 128 + 224 * 256 = 168 * 384).  The
+  // registers to the two softmax warpgroups (96 * 128 + 200 * 256 <= 168 * 384).  The
   // adjustment sits inside each role's branch so the compiler budgets each region.
   if (warp < 4) {
-  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
+  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
   if (warp == 0) {
     // ================================================================ TMA producer
     const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
@@ -369,6 +393,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       tma_prefetch_desc(&qmap);
       tma_prefetch_desc(&kmap);
       tma_prefetch_desc(&vmap);
+      tma_prefetch_desc(&kmap_run);
+      tma_prefetch_desc(&vmap_run);
       mbar_arrive_expect_tx(&q_full, NT * C::kTileBytes);
       for (int t = 0; t < NT; ++t) {
         const int node0 = ((mp * NT + t) * kRowTile) / p.G;
@@ -391,9 +417,16 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
 #pragma unroll
     for (int u = 0; u < kLookahead; ++u) pid[u] = load_pid(u);
     int bad = 0;
-    // One TMA box per (page, 64-column half): lanes [0, 8 * halves) issue them in parallel.
-    auto issue = [&](uint8_t* ring, const CUtensorMap* map, uint64_t* full, int st, int page) {
-      if (lane < kPagesPerTile * C::kHalves) {
+    // When the tile's eight pages are consecutive in the pool (page q == page 0 + q) one
+    // 128-row box per 64-column half moves the whole tile; otherwise one box per (page,
+    // half), issued by lanes [0, 8 * halves) in parallel.
+    auto issue = [&](uint8_t* ring, const CUtensorMap* map, const CUtensorMap* map_run,
+                     uint64_t* full, int st, int page, int page0, bool run) {
+      if (run) {
+        if (lane < C::kHalves)
+          tma_load_3d(ring + st * C::kTileBytes + lane * C::kHalfBytes, map_run, full, lane * 64, g,
+                      page0 * kPage);
+      } else if (lane < kPagesPerTile * C::kHalves) {
         const int q = lane % kPagesPerTile, hh = lane / kPagesPerTile;
         tma_load_3d(ring + st * C::kTileBytes + hh * C::kHalfBytes + q * (kPage * 128), map, full,
                     hh * 64, g, page * kPage);
@@ -407,25 +440,28 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       else if (mine == p.num_pages && lane < kPagesPerTile &&
                ((k0 + j) * kPagesPerTile + lane) * kPage < L) bad = 1;
       const int page = __shfl_sync(0xffffffffu, mine, lane % kPagesPerTile);
+      const int page0 = __shfl_sync(0xffffffffu, mine, 0);
+      const bool run = __all_sync(0xffffffffu, page == page0 + lane % kPagesPerTile);
 #pragma unroll
       for (int u = 0; u < kLookahead - 1; ++u) pid[u] = pid[u + 1];
       pid[kLookahead - 1] = load_pid(j + kLookahead);
-      const int st = j % S;
-      const uint32_t reuse_parity = static_cast<uint32_t>((j / S) - 1) & 1u;
+      const int sk = j % SK, sv = j % SV;
       int okl = 1;
       if (lane == 0) {
-        if (j >= S && !mbar_wait(&k_empty[st], reuse_parity, abort)) okl = 0;
-        else mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
+        if (j >= SK && !mbar_wait(&k_empty[sk], static_cast<uint32_t>((j / SK) - 1) & 1u, abort))
+          okl = 0;
+        else mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
       }
       if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
-      issue(k_s, &kmap, &k_full[st], st, page);
+      issue(k_s, &kmap, &kmap_run, &k_full[sk], sk, page, page0, run);
       k_issued = j + 1;
       if (lane == 0) {
-        if (j >= S && !mbar_wait(&v_empty[st], reuse_parity, abort)) okl = 0;
-        else mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+        if (j >= SV && !mbar_wait(&v_empty[sv], static_cast<uint32_t>((j / SV) - 1) & 1u, abort))
+          okl = 0;
+        else mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
       }
       if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
-      issue(v_s, &vmap, &v_full[st], st, page);
+      issue(v_s, &vmap, &vmap_run, &v_full[sv], sv, page, page0, run);
       v_issued = j + 1;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.dev_err, JF_DEVERR_BAD_PAGE);
@@ -436,31 +472,37 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       int zero_q = 0;
       mbar_wait(&q_full, 0, &zero_q);
       int zero = 0;
-      for (int j = max(0, k_issued - S); j < k_issued; ++j)
-        mbar_wait(&k_full[j % S], static_cast<uint32_t>(j / S) & 1u, &zero);
-      for (int j = max(0, v_issued - S); j < v_issued; ++j)
-        mbar_wait(&v_full[j % S], static_cast<uint32_t>(j / S) & 1u, &zero);
+      for (int j = max(0, k_issued - SK); j < k_issued; ++j)
+        mbar_wait(&k_full[j % SK], static_cast<uint32_t>(j / SK) & 1u, &zero);
+      for (int j = max(0, v_issued - SV); j < v_issued; ++j)
+        mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, &zero);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     constexpr uint32_t idS = idesc_bf16(kRowTile, kKeyTile, false, false);
     constexpr uint32_t idO = idesc_bf16(kRowTile, D, false, true);
+    // Matrix descriptors of the first Q tile / K stage / V stage; a tile, a stage or a
+    // K-step only moves the 14-bit start-address field (addresses < 256 KB, no carry).
+    const uint64_t dq = desc_sw128(smem_u32(q_s), 16, 1024);
+    const uint64_t dk = desc_sw128(smem_u32(k_s), 16, 1024);
+    const uint64_t dv = desc_sw128(smem_u32(v_s), C::kHalfBytes, 1024);
     auto issue_s = [&](int t, int st) {
-      const uint32_t qa = smem_u32(q_s + t * C::kTileBytes);
-      const uint32_t ka = smem_u32(k_s + st * C::kTileBytes);
+      const uint64_t da = dq + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
+      const uint64_t db = dk + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+      const uint32_t d_tmem = tmem + C::kTmemS + t * 128;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * C::kHalfBytes + (kk % 4) * 32;
-        mma_ss(tmem + C::kTmemS + t * 128, desc_sw128(qa + off, 16, 1024),
-               desc_sw128(ka + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+        const uint64_t off = static_cast<uint64_t>(((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4);
+        mma_ss(d_tmem, da + off, db + off, idS, kk > 0 ? 1u : 0u);
       }
     };
     auto issue_pv = [&](int t, int st, bool acc) {
-      const uint32_t va = smem_u32(v_s + st * C::kTileBytes);
+      const uint64_t db = dv + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+      const uint32_t d_tmem = tmem + C::kTmemO + t * 128;
+      const uint32_t a_tmem = tmem + C::kTmemS + t * 128;
 #pragma unroll
       for (int kk = 0; kk < kKeyTile / 16; ++kk)
-        mma_ts(tmem + C::kTmemO + t * 128, tmem + C::kTmemS + t * 128 + kk * 8,
-               desc_sw128(va + kk * 16 * 128, C::kHalfBytes, 1024), idO,
+        mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
                (acc || kk > 0) ? 1u : 0u);
     };
     bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
@@ -473,8 +515,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       mma_commit(&k_empty[0]);
     }
     for (int j = 0; j < T && ok; ++j) {
-      const int st = j % S;
-      const uint32_t par = static_cast<uint32_t>(j / S) & 1u;
+      const int st = j % SV;                        // V stage of tile j
+      const uint32_t par = static_cast<uint32_t>(j / SV) & 1u;
       if (!wait_warp(&v_full[st], par, abort)) { ok = false; break; }
       const int key0 = (k0 + j) * kKeyTile;
       if (key0 + kKeyTile > L) {
@@ -500,8 +542,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           if (t == NT - 1) mma_commit(&v_empty[st]);    // V tile j no longer needed
         }
         if (j + 1 < T) {
-          const int st1 = (j + 1) % S;
-          if (t == 0 && !wait_warp(&k_full[st1], static_cast<uint32_t>((j + 1) / S) & 1u, abort)) {
+          const int st1 = (j + 1) % SK;                // K stage of tile j + 1
+          if (t == 0 && !wait_warp(&k_full[st1], static_cast<uint32_t>((j + 1) / SK) & 1u, abort)) {
             ok = false;
             break;
           }
@@ -512,7 +554,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0 && j + 1 < T) mma_commit(&k_empty[(j + 1) % S]);
+      if (lane == 0 && j + 1 < T) mma_commit(&k_empty[(j + 1) % SK]);
       __syncwarp();
     }
     if (!ok) set_abort(abort, p.dev_err);
@@ -525,7 +567,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     __syncwarp();
   }
   } else {
-    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 224;");
+    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
     // ================================================================ softmax / epilogue
     const int t = (warp >> 2) - 1;
     const int wq = warp & 3;
@@ -536,15 +578,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     const int i = r / p.G;
     const int h = g * p.G + (r % p.G);
     const int W = p.W;
-    uint64_t* s_mask = reinterpret_cast<uint64_t*>(sm + C::kMaskOff + t * kMaskBytesPerTile);
-    if (k1 * kKeyTile > P) {                             // this split reaches tree keys
-      const int nodes = kRowTile / p.G;
-      const uint64_t* src = p.mask + (static_cast<size_t>(b) * p.N + node_base) * W;
-      for (int e = rl; e < nodes * W; e += 128)
-        s_mask[e] = (node_base + e / W) < p.N ? src[e] : 0ull;
-      named_bar(1 + t, 128);
-    }
-    const uint64_t* my_mask = s_mask + (rl / p.G) * W;
+    // The node's ancestor-mask words a tile needs (at most three 64-bit words for 128
+    // keys) are loaded into registers before the tile's S is waited for.
+    const uint64_t* mrow = p.mask + (static_cast<size_t>(b) * p.N + (valid ? i : 0)) * W;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + C::kTmemS + t * 128 + lane_off;
     const uint32_t tO = tmem + C::kTmemO + t * 128 + lane_off;
@@ -553,13 +589,20 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
+      const int key0 = (k0 + j) * kKeyTile;
+      const bool masked_tile = key0 + kKeyTile > P;
+      uint64_t mw[3] = {0ull, 0ull, 0ull};
+      const int w_lo = max(key0 - P, 0) >> 6;
+      if (masked_tile && valid) {
+#pragma unroll
+        for (int u = 0; u < 3; ++u)
+          if (w_lo + u < W) mw[u] = __ldg(reinterpret_cast<const unsigned long long*>(mrow) + w_lo + u);
+      }
       if (!wait_warp(&s_full[t], static_cast<uint32_t>(j) & 1u, abort)) { ok = false; break; }
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128(tS, sr);
       float* sv = reinterpret_cast<float*>(sr);
-      const int key0 = (k0 + j) * kKeyTile;
-      const bool masked_tile = key0 + kKeyTile > P;
       if (masked_tile) {
         // Visibility of the tile's 128 keys as four 32-bit words: prefix keys always,
         // tree key j iff bit j of the node's ancestor mask, nothing past the sequence end.
@@ -569,7 +612,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const int c0 = 32 * w;
-          uint32_t m = mask_bits32(my_mask, W, key0 + c0 - P);
+          uint32_t m = window_bits32(mw, key0 + c0 - P - 64 * w_lo);
           const int np = min(max(pre - c0, 0), 32);
           const int ne = min(max(end - c0, 0), 32);
           m |= np >= 32 ? 0xFFFFFFFFu : ((1u << np) - 1u);
@@ -741,7 +784,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  grid_dependents_launch();
 }
 
 // Merges split partials: O = sum_s 2^(lse_s - lse) O_s,  lse = log2 sum_s 2^lse_s.
@@ -755,7 +798,7 @@ __global__ void __launch_bounds__(256)
                                   float* __restrict__ lse) {
   constexpr int E = D / 32;
   // Launched as a programmatic dependent of the split kernel: wait for its results.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  grid_dependency_wait();
   const long long rr = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (rr >= rows) return;
@@ -879,8 +922,6 @@ bool shape_supported(int B, int N, int Hq, int Hkv, int D, int max_pages, int pa
   if (Hq % Hkv != 0) return false;
   const int G = Hq / Hkv;
   if (G > kRowTile || (G & (G - 1)) != 0) return false;
-  const int W = (N + 63) / 64;
-  if ((kRowTile / G) * W * 8 > kMaskBytesPerTile) return false;   // staged mask limit
   if (static_cast<long long>(max_pages) * kPage < N) return false;
   if (static_cast<long long>(max_pages) * kPage > (1ll << 30)) return false;
   return true;
@@ -963,8 +1004,8 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
 
 template <int NT, int D>
 jf_status launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                 const CUtensorMap& om, const CUtensorMap& wm, const AttnParams& prm,
-                 long long grid, cudaStream_t s) {
+                 const CUtensorMap& kr, const CUtensorMap& vr, const CUtensorMap& om,
+                 const CUtensorMap& wm, const AttnParams& prm, long long grid, cudaStream_t s) {
   using C = Cfg<NT, D>;
   if (!ensure_smem_attr<NT, D>()) return JF_ERR_CUDA;
   cudaLaunchConfig_t lc = {};
@@ -972,16 +1013,20 @@ jf_status launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap
   lc.blockDim = dim3(C::kThreads);
   lc.dynamicSmemBytes = C::kSmemBytes;
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
   if (prm.cluster_merge) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(prm.splits);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(prm.splits);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    lc.numAttrs = 2;
   }
-  const cudaError_t e = cudaLaunchKernelEx(&lc, tree_attention_kernel<NT, D>, qm, km, vm, om, wm, prm);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&lc, tree_attention_kernel<NT, D>, qm, km, vm, kr, vr, om, wm, prm);
   return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
 
@@ -1028,7 +1073,7 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
     if (!aligned_to(workspace, 16)) return JF_ERR_MISALIGNED;
   }
   const int G = Hq / Hkv;
-  CUtensorMap qm, km, vm, om, wm;
+  CUtensorMap qm, km, vm, kr, vr, om, wm;
   std::memset(&om, 0, sizeof(om));
   std::memset(&wm, 0, sizeof(wm));
   {
@@ -1061,6 +1106,9 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
     const cuuint32_t box[3] = {64, 1, kPage};
     if (!encode(&km, k_cache, 3, dims, strides, box)) return JF_ERR_CUDA;
     if (!encode(&vm, v_cache, 3, dims, strides, box)) return JF_ERR_CUDA;
+    const cuuint32_t box_run[3] = {64, 1, kKeyTile};   // eight consecutive pages at once
+    if (!encode(&kr, k_cache, 3, dims, strides, box_run)) return JF_ERR_CUDA;
+    if (!encode(&vr, v_cache, 3, dims, strides, box_run)) return JF_ERR_CUDA;
   }
   AttnParams prm;
   prm.block_table = block_table;
@@ -1083,11 +1131,11 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   jf_status st;
   if (D == 128)
-    st = pl.NT == 2 ? launch<2, 128>(qm, km, vm, om, wm, prm, grid, s)
-                    : launch<1, 128>(qm, km, vm, om, wm, prm, grid, s);
+    st = pl.NT == 2 ? launch<2, 128>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
+                    : launch<1, 128>(qm, km, vm, kr, vr, om, wm, prm, grid, s);
   else
-    st = pl.NT == 2 ? launch<2, 64>(qm, km, vm, om, wm, prm, grid, s)
-                    : launch<1, 64>(qm, km, vm, om, wm, prm, grid, s);
+    st = pl.NT == 2 ? launch<2, 64>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
+                    : launch<1, 64>(qm, km, vm, kr, vr, om, wm, prm, grid, s);
   if (st != JF_OK) return st;
   if (pl.splits > 1 && !pl.cluster) {
     const long long nb = (static_cast<long long>(rows) + 7) / 8;

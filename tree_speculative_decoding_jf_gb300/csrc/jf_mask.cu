@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kMaskThreads)
                      int N, int W, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
                      int32_t* __restrict__ pos, int32_t* dev_err) {
   extern __shared__ int32_t s_par[];   // [N]; malformed entries replaced by -1
+  grid_dependency_wait();
   const int b = blockIdx.x;
   const int32_t* par = parent + static_cast<size_t>(b) * N;
   int bad = 0;
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(kMaskThreads)
       if (pos != nullptr) pos[static_cast<size_t>(b) * N + i] = P + d;
     }
   }
+  grid_dependents_launch();
 }
 
 }  // namespace
@@ -74,7 +76,8 @@ extern "C" jf_status jf_build_tree_mask(const int32_t* parent, const int32_t* pr
   if (!jf::aligned_to(mask, 8)) return JF_ERR_MISALIGNED;
   const int W = (N + 63) / 64;
   const size_t smem = sizeof(int32_t) * static_cast<size_t>(N);
-  jf::tree_mask_kernel<<<B, jf::kMaskThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-      parent, prefix_len, N, W, mask, depth, pos, dev_err);
-  return jf::launch_status();
+  const cudaError_t e = jf::launch_pdl(jf::tree_mask_kernel, dim3(B), dim3(jf::kMaskThreads), smem,
+                                       reinterpret_cast<cudaStream_t>(stream), parent,
+                                       prefix_len, N, W, mask, depth, pos, dev_err);
+  return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }

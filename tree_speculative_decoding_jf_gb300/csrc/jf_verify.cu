@@ -10,7 +10,7 @@
 // writes a packed 64-bit key (order-preserving value bits << 32 | ~index) into the
 // workspace; max over keys gives the largest value and, among equal values, the smallest
 // index.  Chunks per row are chosen so that rows x chunks fills the GPU.
-// Kernel 2 (one CTA per sequence): merges the chunk keys into argmax (a warp per row),
+// Kernel 2 (one CTA per sequence): merges the chunk keys into argmax (shared atomicMax),
 // finds depths by pointer jumping, computes accepted-subtree lengths level by level from
 // the deepest level up with shared-memory atomicMax on (len + 1) << 16 | (0xFFFF - child),
 // and walks the best children from the root.
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kArgmaxThreads)
     argmax_chunk_kernel(const T* __restrict__ logits, long long V, int chunks, int chunk_len,
                         uint64_t* __restrict__ part) {
   constexpr int kVec = 16 / sizeof(T);
+  grid_dependency_wait();
   const long long row = blockIdx.x / chunks;
   const int c = blockIdx.x - static_cast<int>(row * chunks);
   const long long s = static_cast<long long>(c) * chunk_len;
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(kArgmaxThreads)
     key = warp_max_u64(key);
     if (threadIdx.x == 0) part[blockIdx.x] = key;
   }
+  grid_dependents_launch();
 }
 
 __global__ void __launch_bounds__(kWalkThreads)
@@ -149,7 +151,9 @@ __global__ void __launch_bounds__(kWalkThreads)
                      int N, int V, int32_t* __restrict__ argmax_out,
                      int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                      int32_t* __restrict__ bonus, int32_t* dev_err) {
-  extern __shared__ int32_t sm[];
+  extern __shared__ uint64_t sm64[];
+  unsigned long long* s_best = reinterpret_cast<unsigned long long*>(sm64);   // [N] best key
+  int32_t* sm = reinterpret_cast<int32_t*>(sm64 + N);
   int32_t* s_par = sm;            // [N] parent, malformed -> -1
   int32_t* s_am = s_par + N;      // [N] argmax
   int32_t* s_dep = s_am + N;      // [N] depth (pointer jumping)
@@ -160,22 +164,23 @@ __global__ void __launch_bounds__(kWalkThreads)
   __shared__ int s_flag;
   __shared__ int s_len;
 
+  grid_dependency_wait();
   const int b = blockIdx.x;
   const size_t rb = static_cast<size_t>(b) * N;
-  // Chunk keys of each row: one warp per row, lanes over chunks, shuffle max.
+  // Chunk keys of every row, all loads in flight together: (row, chunk) pairs spread over
+  // the block, combined per row with a shared-memory 64-bit atomicMax.
+  for (int i = threadIdx.x; i < N; i += blockDim.x) s_best[i] = 0ull;
+  __syncthreads();
   {
-    const int lane = threadIdx.x & 31;
-    for (int i = threadIdx.x >> 5; i < N; i += blockDim.x >> 5) {
-      const uint64_t* pk = part + (rb + i) * chunks;
-      uint64_t k = 0;
-      for (int c = lane; c < chunks; c += 32) k = max(k, pk[c]);
-      k = warp_max_u64(k);
-      if (lane == 0) {
-        const int am = static_cast<int>(~static_cast<uint32_t>(k & 0xFFFFFFFFull));
-        s_am[i] = am;
-        if (argmax_out != nullptr) argmax_out[rb + i] = am;
-      }
-    }
+    const int total = N * chunks;
+    const uint64_t* pk = part + rb * chunks;
+    for (int e = threadIdx.x; e < total; e += blockDim.x) atomicMax(&s_best[e / chunks], pk[e]);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const int am = static_cast<int>(~static_cast<uint32_t>(s_best[i] & 0xFFFFFFFFull));
+    s_am[i] = am;
+    if (argmax_out != nullptr) argmax_out[rb + i] = am;
   }
   int bad_parent = 0, bad_token = 0;
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
@@ -258,6 +263,7 @@ __global__ void __launch_bounds__(kWalkThreads)
   __syncthreads();
   const int n = s_len;
   for (int k = threadIdx.x; k < N; k += blockDim.x) path[rb + k] = k <= n ? s_path[k] : -1;
+  grid_dependents_launch();
 }
 
 struct VerifyPlan {
@@ -311,22 +317,26 @@ extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int
   uint64_t* part = static_cast<uint64_t*>(workspace);
   const long long grid = static_cast<long long>(B) * N * p.chunks;
   if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
-  if (dtype == JF_DTYPE_BF16)
-    jf::argmax_chunk_kernel<uint16_t><<<static_cast<unsigned>(grid), jf::kArgmaxThreads, 0, s>>>(
-        static_cast<const uint16_t*>(logits), V, p.chunks, p.chunk_len, part);
-  else
-    jf::argmax_chunk_kernel<float><<<static_cast<unsigned>(grid), jf::kArgmaxThreads, 0, s>>>(
-        static_cast<const float*>(logits), V, p.chunks, p.chunk_len, part);
-  if (cudaGetLastError() != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * 7 * sizeof(int32_t);
+  const long long Vl = V;
+  const cudaError_t ea =
+      dtype == JF_DTYPE_BF16
+          ? jf::launch_pdl(jf::argmax_chunk_kernel<uint16_t>, dim3(static_cast<unsigned>(grid)),
+                           dim3(jf::kArgmaxThreads), 0, s, static_cast<const uint16_t*>(logits),
+                           Vl, p.chunks, p.chunk_len, part)
+          : jf::launch_pdl(jf::argmax_chunk_kernel<float>, dim3(static_cast<unsigned>(grid)),
+                           dim3(jf::kArgmaxThreads), 0, s, static_cast<const float*>(logits), Vl,
+                           p.chunks, p.chunk_len, part);
+  if (ea != cudaSuccess) return JF_ERR_CUDA;
+  const size_t smem = static_cast<size_t>(N) * (7 * sizeof(int32_t) + sizeof(uint64_t));
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return JF_ERR_CUDA;
   }
-  jf::tree_walk_kernel<<<B, jf::kWalkThreads, smem, s>>>(part, p.chunks, draft, parent, N, V,
-                                                         argmax, accept_len, path, bonus, dev_err);
-  return jf::launch_status();
+  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::kWalkThreads), smem,
+                                        s, static_cast<const uint64_t*>(part), p.chunks, draft,
+                                        parent, N, V, argmax, accept_len, path, bonus, dev_err);
+  return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------------ allocation-free
@@ -380,19 +390,22 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
   if (part == nullptr) return JF_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const unsigned grid = static_cast<unsigned>(keys);
-  if (dtype == JF_DTYPE_BF16)
-    jf::argmax_chunk_kernel<uint16_t><<<grid, jf::kArgmaxThreads, 0, s>>>(
-        static_cast<const uint16_t*>(logits), V, p.chunks, p.chunk_len, part);
-  else
-    jf::argmax_chunk_kernel<float><<<grid, jf::kArgmaxThreads, 0, s>>>(
-        static_cast<const float*>(logits), V, p.chunks, p.chunk_len, part);
-  if (cudaGetLastError() != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * 7 * sizeof(int32_t);
+  const long long Vl = V;
+  const cudaError_t ea =
+      dtype == JF_DTYPE_BF16
+          ? jf::launch_pdl(jf::argmax_chunk_kernel<uint16_t>, dim3(grid), dim3(jf::kArgmaxThreads),
+                           0, s, static_cast<const uint16_t*>(logits), Vl, p.chunks, p.chunk_len,
+                           part)
+          : jf::launch_pdl(jf::argmax_chunk_kernel<float>, dim3(grid), dim3(jf::kArgmaxThreads), 0,
+                           s, static_cast<const float*>(logits), Vl, p.chunks, p.chunk_len, part);
+  if (ea != cudaSuccess) return JF_ERR_CUDA;
+  const size_t smem = static_cast<size_t>(N) * (7 * sizeof(int32_t) + sizeof(uint64_t));
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return JF_ERR_CUDA;
-  jf::tree_walk_kernel<<<B, jf::kWalkThreads, smem, s>>>(part, p.chunks, draft, parent, N, V,
-                                                         argmax, accept_len, path, bonus, dev_err);
-  return jf::launch_status();
+  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::kWalkThreads), smem,
+                                        s, static_cast<const uint64_t*>(part), p.chunks, draft,
+                                        parent, N, V, argmax, accept_len, path, bonus, dev_err);
+  return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
