@@ -59,6 +59,10 @@ constexpr int kPage = 16;
 constexpr int kPagesPerTile = kKeyTile / kPage;
 constexpr float kRescaleThreshold = 8.0f;               // log2 units
 
+// Step records: record i completes once step i - 1 (every row tile's PV of key tile i - 1
+// and S of key tile i) has finished on the tensor cores; record 0 marks the first S MMAs.
+constexpr int kStepRing = 8;
+
 template <int NT, int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;                  // 128-byte swizzle atoms per row
@@ -66,6 +70,9 @@ struct Cfg {
   // the next tile's S MMAs are issued, so V gets the deeper ring.
   static constexpr int kKStages = (D == 64) ? 4 : 2;
   static constexpr int kVStages = (D == 64) ? 6 : 3;
+  // K tile j may load after record j - kKStages, V tile j after record j - kVStages + 1;
+  // the producer loads both after record j - kStageLag.
+  static constexpr int kStageLag = kKStages < kVStages - 1 ? kKStages : kVStages - 1;
   static constexpr int kTileBytes = kRowTile * D * 2;     // one 128-row bf16 tile
   static constexpr int kHalfBytes = kRowTile * 128;       // one 64-column half of a tile
   static constexpr int kQOff = 0;
@@ -298,8 +305,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t q_full, o_full, fin;
-  __shared__ uint64_t k_full[SK], k_empty[SK], v_full[SV], v_empty[SV];
-  __shared__ uint64_t s_full[NT], p_full[NT];
+  __shared__ uint64_t k_full[SK], v_full[SV], step_done[kStepRing];
+  __shared__ uint64_t s_full[NT], p_full[NT], v_tail;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
@@ -353,18 +360,14 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     mbar_init(&q_full, 1);
     mbar_init(&o_full, 1);
     mbar_init(&fin, 1);
-    for (int st = 0; st < SK; ++st) {
-      mbar_init(&k_full[st], 1);
-      mbar_init(&k_empty[st], 1);
-    }
-    for (int st = 0; st < SV; ++st) {
-      mbar_init(&v_full[st], 1);
-      mbar_init(&v_empty[st], 1);
-    }
+    for (int st = 0; st < SK; ++st) mbar_init(&k_full[st], 1);
+    for (int st = 0; st < SV; ++st) mbar_init(&v_full[st], 1);
+    for (int st = 0; st < kStepRing; ++st) mbar_init(&step_done[st], 1);
     for (int t = 0; t < NT; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&p_full[t], 128 + 1);   // the softmax warpgroup + its data voucher
     }
+    mbar_init(&v_tail, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -446,25 +449,49 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       for (int u = 0; u < kLookahead - 1; ++u) pid[u] = pid[u + 1];
       pid[kLookahead - 1] = load_pid(j + kLookahead);
       const int sk = j % SK, sv = j % SV;
+      // K tile j reuses the stage of K tile j - SK, last read by the S MMAs of step
+      // j - SK - 1; V tile j reuses that of V tile j - SV, read in step j - SV.  One step
+      // record covers both (see Cfg::kStageLag).
+      const int rec = j - C::kStageLag;
       int okl = 1;
       if (lane == 0) {
-        if (j >= SK && !mbar_wait(&k_empty[sk], static_cast<uint32_t>((j / SK) - 1) & 1u, abort))
+        if (rec >= 0 && !mbar_wait(&step_done[rec % kStepRing],
+                                   static_cast<uint32_t>(rec / kStepRing) & 1u, abort)) {
           okl = 0;
-        else mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
+        } else {
+          mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
+          mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
+        }
       }
       if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
       issue(k_s, &kmap, &kmap_run, &k_full[sk], sk, page, page0, run);
       k_issued = j + 1;
-      if (lane == 0) {
-        if (j >= SV && !mbar_wait(&v_empty[sv], static_cast<uint32_t>((j / SV) - 1) & 1u, abort))
-          okl = 0;
-        else mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
-      }
-      if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
       issue(v_s, &vmap, &vmap_run, &v_full[sv], sv, page, page0, run);
       v_issued = j + 1;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.dev_err, JF_DEVERR_BAD_PAGE);
+    // V rows past the sequence end in the last key tile hold whatever the unused page
+    // slots contain; they meet a zero probability, so they must be finite: zero them once
+    // the tile has landed, then let the MMA issuer use it.
+    const int last_key0 = (k0 + T - 1) * kKeyTile;
+    if (ok && last_key0 + kKeyTile > L) {
+      const int jl = T - 1;
+      if (!wait_warp(&v_full[jl % SV], static_cast<uint32_t>(jl / SV) & 1u, abort)) {
+        ok = false;
+      } else {
+        const int r0 = L - last_key0;
+        uint8_t* vt = v_s + (jl % SV) * C::kTileBytes;
+        const int per_half = (kKeyTile - r0) * 8;                 // 16-byte chunks per half
+        for (int c = lane; c < per_half * C::kHalves; c += 32) {
+          const int hh = c / per_half, rem = c % per_half;
+          *reinterpret_cast<uint4*>(vt + hh * C::kHalfBytes + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&v_tail);
+      }
+    }
     if (!ok && lane == 0) set_abort(abort, p.dev_err);
     __syncwarp();
     // Drain: make sure no copy is still landing in shared memory when the CTA exits.
@@ -512,57 +539,84 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         issue_s(t, 0);
         mma_commit(&s_full[t]);
       }
-      mma_commit(&k_empty[0]);
-    }
-    for (int j = 0; j < T && ok; ++j) {
-      const int st = j % SV;                        // V stage of tile j
-      const uint32_t par = static_cast<uint32_t>(j / SV) & 1u;
-      if (!wait_warp(&v_full[st], par, abort)) { ok = false; break; }
-      const int key0 = (k0 + j) * kKeyTile;
-      if (key0 + kKeyTile > L) {
-        // Zero V rows past the sequence end (all 64-column halves).
-        const int r0 = L - key0;
-        uint8_t* vt = v_s + st * C::kTileBytes;
-        const int nchunks = (kKeyTile - r0) * 8 * C::kHalves;   // 16-byte chunks
-        for (int c = lane; c < nchunks; c += 32) {
-          const int hh = c / ((kKeyTile - r0) * 8);
-          const int rem = c % ((kKeyTile - r0) * 8);
-          const int row = r0 + rem / 8;
-          *reinterpret_cast<uint4*>(vt + hh * C::kHalfBytes + row * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      for (int t = 0; t < NT && ok; ++t) {
-        if (!wait_warp(&p_full[t], static_cast<uint32_t>(j) & 1u, abort)) { ok = false; break; }
-        if (lane == 0) {
+      mma_commit(&step_done[0]);
+      // One thread drives every row tile.  Row tile t's next step is PV of key tile
+      // jn[t] followed by S of key tile jn[t] + 1.  It may go once p_full[t] completes: the
+      // tile's softmax has arrived and so has its voucher warp, which arrives only after V
+      // tile jn[t] and K tile jn[t] + 1 have landed, so a step costs the issuer a single
+      // barrier probe.  The thread probes the tiles in turn and issues whichever
+      // step is ready, so one tile's softmax never holds back the other tile's MMAs.
+      // After the last row tile's step j one commit completes step record j + 1.
+      int jn[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) jn[t] = 0;
+      int left = NT * T;
+      uint32_t idle = 0;
+      uint64_t idle_since = 0;
+      while (left > 0) {
+        bool progressed = false;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int j = jn[t];
+          if (j >= T) continue;
+          if (!mbar_try_wait(&p_full[t], static_cast<uint32_t>(j) & 1u)) continue;
+          bool last = true;                  // the other row tiles are past key tile j
+#pragma unroll
+          for (int u = 0; u < NT; ++u)
+            if (u != t && jn[u] <= j) last = false;
           tc_fence_after();
-          issue_pv(t, st, j > 0);
-          if (t == NT - 1) mma_commit(&v_empty[st]);    // V tile j no longer needed
+          issue_pv(t, j % SV, j > 0);
+          if (j + 1 < T) {
+            issue_s(t, (j + 1) % SK);
+            mma_commit(&s_full[t]);
+          }
+          if (last) mma_commit(&step_done[(j + 1) % kStepRing]);
+          jn[t] = j + 1;
+          --left;
+          progressed = true;
         }
-        if (j + 1 < T) {
-          const int st1 = (j + 1) % SK;                // K stage of tile j + 1
-          if (t == 0 && !wait_warp(&k_full[st1], static_cast<uint32_t>((j + 1) / SK) & 1u, abort)) {
+        if (progressed) {
+          idle = 0;
+        } else {
+          if (idle == 0) idle_since = global_timer_ns();
+          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > kWaitLimitNs)) {
             ok = false;
             break;
           }
-          if (lane == 0) {
-            issue_s(t, st1);
-            mma_commit(&s_full[t]);
-          }
         }
       }
-      if (!ok) break;
-      if (lane == 0 && j + 1 < T) mma_commit(&k_empty[(j + 1) % SK]);
-      __syncwarp();
     }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     if (!ok) set_abort(abort, p.dev_err);
     if (lane == 0) {
       if (ok) mma_commit(&o_full);
       mma_commit(&fin);   // all MMAs done before TMEM is released
       int zero = 0;
       mbar_wait(&fin, 0, &zero);
+    }
+    __syncwarp();
+  } else if (warp >= 2 && warp < 2 + NT) {
+    // ================================================================ data vouchers
+    // Warp 2 + t adds the last arrival to p_full[t] for key tile j once V tile j, K tile
+    // j + 1 and (for the last tile) the zeroed V tail have landed, so the MMA issuer needs
+    // no probe of its own on the K/V barriers.  It waits for phase j - 1 of p_full[t]
+    // first, so its arrival cannot count toward an earlier phase.
+    const int t = warp - 2;
+    const bool tail = (k0 + T) * kKeyTile > L;
+    if (lane == 0) {
+      for (int j = 0; j < T; ++j) {
+        const bool ready =
+            (j == 0 || mbar_wait(&p_full[t], static_cast<uint32_t>(j - 1) & 1u, abort)) &&
+            mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, abort) &&
+            (j + 1 >= T ||
+             mbar_wait(&k_full[(j + 1) % SK], static_cast<uint32_t>((j + 1) / SK) & 1u, abort)) &&
+            (j + 1 < T || !tail || mbar_wait(&v_tail, 0u, abort));
+        if (!ready) {
+          set_abort(abort, p.dev_err);
+          break;
+        }
+        mbar_arrive(&p_full[t]);
+      }
     }
     __syncwarp();
   }
