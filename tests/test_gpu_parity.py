@@ -291,6 +291,10 @@ SHAPES = [  # B, N, Hq, Hkv, D, P, tree
     (1, 1024, 4, 1, 128, 64, "random"),      # many nodes, W = 16
     (2, 7, 128, 1, 64, 33, "random"),        # G = 128: one node per row tile
     (1, 2048, 2, 2, 64, 100, "random"),      # G = 1, W = 32: deep tree over many key tiles
+    (1, 1, 4, 1, 64, 20000, "chain"),        # one unit, long prefix: > 16 splits to combine
+    (1, 4, 8, 1, 128, 1500, "random"),       # one unit, 12 key tiles: 9..16 splits
+    (1, 8, 8, 1, 128, 900, "random"),        # 5..8 splits
+    (2, 8, 8, 2, 64, 800, "random"),         # 5..8 splits, D = 64
 ]
 
 

@@ -46,6 +46,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "jf_common.cuh"
 #include "jf_sm100.cuh"
@@ -153,9 +154,10 @@ __device__ __forceinline__ float exp2_poly(float x) {
   return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
 }
 
-// One in kPolyEvery exponential pairs of an unmasked tile goes to exp2_poly (0: none).
+// One in kPolyEvery exponential pairs of an unmasked tile goes to the FMA pipe (0: none).
 constexpr int kPolyEvery = 0;
 constexpr int kPolyMod = kPolyEvery > 0 ? kPolyEvery : 1;
+constexpr bool kPolyPacked = true;   // paired (f32x2) evaluation of the same polynomial
 
 // Paired fp32 arithmetic (one instruction for two lanes of data) and a 3-input max.
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
@@ -180,6 +182,23 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
+}
+
+// exp2_poly on a pair of lanes with paired fp32 arithmetic: the same reduction and
+// polynomial, two results per instruction except for the clamp and the exponent add.
+__device__ __forceinline__ void exp2_poly2(float x0, float x1, float& p0, float& p1) {
+  const uint64_t x = f2(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
+  const uint64_t t = fadd2(x, f2(12582912.0f, 12582912.0f));
+  const uint64_t n = fadd2(t, f2(-12582912.0f, -12582912.0f));
+  const uint64_t f = ffma2(n, f2(-1.0f, -1.0f), x);
+  uint64_t q = ffma2(f, f2(0.0551716685f, 0.0551716685f), f2(0.2426111251f, 0.2426111251f));
+  q = ffma2(q, f, f2(0.6932609677f, 0.6932609677f));
+  q = ffma2(q, f, f2(0.9999280572f, 0.9999280572f));
+  float q0, q1, t0, t1;
+  f2_split(q, q0, q1);
+  f2_split(t, t0, t1);
+  p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+  p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
 }
 
 // Bits [rel, rel + 32) of the 192-bit little-endian window w[0..3) (zero outside it).
@@ -310,7 +329,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   volatile int* abort = &abort_flag;
-  grid_dependency_wait();
+  uint8_t* q_s = sm + C::kQOff;
+  uint8_t* k_s = sm + C::kKOff;
+  uint8_t* v_s = sm + C::kVOff;
 
   // ---- which (b, kv-head, row-tile group, split) this CTA owns; split fastest, then the
   // row-tile group, so CTAs that read the same K/V tiles run side by side.
@@ -321,41 +342,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   bid /= p.n_groups;
   const int g = bid % p.Hkv;
   const int b = bid / p.Hkv;
-
-  const int cap = p.max_pages * kPage;
-  int P = p.prefix_len[b];
-  if (P < 0 || P > cap - p.N) {
-    if (threadIdx.x == 0) report(p.dev_err, JF_DEVERR_BAD_PREFIX);
-    P = max(0, min(P, cap - p.N));
-  }
-  const int L = P + p.N;
-  const int ntiles = (L + kKeyTile - 1) / kKeyTile;
-  const int k0 = split * p.chunk_tiles;
-  const int k1 = min(ntiles, k0 + p.chunk_tiles);
-  const int T = max(0, k1 - k0);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (T == 0 && p.cluster_merge) {    // empty split: weight 0, but it joins the merge
-    for (int t = 0; t < NT; ++t)
-      for (int e = threadIdx.x; e < kRowTile; e += blockDim.x) part_lse<NT, D>(sm, t)[e] = -INFINITY;
-    merge_cluster<NT, D>(sm, p, b, g, mp, split);
-    return;
-  }
-  if (T == 0) {                         // split past the sequence: an empty partial (weight 0)
-    if (warp >= 4) {
-      const int t = (warp >> 2) - 1;
-      const int r = (mp * NT + t) * kRowTile + ((warp & 3) * 32 + lane);
-      if (r < p.M) {
-        const size_t prow = ((static_cast<size_t>(b) * p.Hkv + g) * p.splits + split) * p.M + r;
-        p.ws_lse[prow] = -INFINITY;
-        float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * D);
-        for (int d = 0; d < D / 4; ++d) dst[d] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-    return;
-  }
-
+  // Barriers and descriptor prefetches touch no input, so they overlap the tail of the
+  // previous kernel (programmatic dependent launch).
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
     mbar_init(&o_full, 1);
@@ -370,7 +361,79 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     mbar_init(&v_tail, 1);
     abort_flag = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&kmap_run);
+    tma_prefetch_desc(&vmap_run);
   }
+  grid_dependency_wait();
+
+  // Q does not depend on the sequence length: its load starts before anything is read.
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&q_full, NT * C::kTileBytes);
+    for (int t = 0; t < NT; ++t) {
+      const int node0 = ((mp * NT + t) * kRowTile) / p.G;
+      for (int hh = 0; hh < C::kHalves; ++hh)
+        tma_load_4d(q_s + t * C::kTileBytes + hh * C::kHalfBytes, &qmap, &q_full, hh * 64,
+                    g * p.G, node0, b);
+    }
+  }
+  // The first key tiles' page ids are read together with the prefix length (one round
+  // trip for both) and parked in shared memory; they are checked against the sequence end
+  // once it is known.
+  constexpr int kLookahead = 4;
+  const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
+  __shared__ int s_pid0[kLookahead][kPagesPerTile];
+  if (warp == 0 && lane < kPagesPerTile) {
+    int raw[kLookahead];
+#pragma unroll
+    for (int u = 0; u < kLookahead; ++u) {
+      const int pl = (split * p.chunk_tiles + u) * kPagesPerTile + lane;
+      raw[u] = pl < p.max_pages ? __ldg(bt + pl) : p.num_pages;
+    }
+#pragma unroll
+    for (int u = 0; u < kLookahead; ++u) s_pid0[u][lane] = raw[u];
+  }
+
+  const int cap = p.max_pages * kPage;
+  int P = p.prefix_len[b];
+  if (P < 0 || P > cap - p.N) {
+    if (threadIdx.x == 0) report(p.dev_err, JF_DEVERR_BAD_PREFIX);
+    P = max(0, min(P, cap - p.N));
+  }
+  const int L = P + p.N;
+  const int ntiles = (L + kKeyTile - 1) / kKeyTile;
+  const int k0 = split * p.chunk_tiles;
+  const int k1 = min(ntiles, k0 + p.chunk_tiles);
+  const int T = max(0, k1 - k0);
+
+  if (T == 0) {
+    // An empty split still drains its Q load before the shared memory is reused or freed.
+    if (threadIdx.x == 0) {
+      int zero = 0;
+      mbar_wait(&q_full, 0, &zero);
+    }
+    if (p.cluster_merge) {            // weight 0, but it joins the merge
+      __syncthreads();
+      for (int t = 0; t < NT; ++t)
+        for (int e = threadIdx.x; e < kRowTile; e += blockDim.x) part_lse<NT, D>(sm, t)[e] = -INFINITY;
+      merge_cluster<NT, D>(sm, p, b, g, mp, split);
+      return;
+    }
+    if (warp >= 4) {                  // split past the sequence: an empty partial (weight 0)
+      const int t = (warp >> 2) - 1;
+      const int r = (mp * NT + t) * kRowTile + ((warp & 3) * 32 + lane);
+      if (r < p.M) {
+        const size_t prow = ((static_cast<size_t>(b) * p.Hkv + g) * p.splits + split) * p.M + r;
+        p.ws_lse[prow] = -INFINITY;
+        float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * D);
+        for (int d = 0; d < D / 4; ++d) dst[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    return;
+  }
+
   if (warp == 1) {
     tmem_alloc(&tmem_slot, C::kTmemCols);
     tmem_relinquish();
@@ -380,10 +443,6 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  uint8_t* q_s = sm + C::kQOff;
-  uint8_t* k_s = sm + C::kKOff;
-  uint8_t* v_s = sm + C::kVOff;
-
   // 384 threads x 168 registers at launch (NT == 2): the control warpgroup hands
   // registers to the two softmax warpgroups (96 * 128 + 200 * 256 <= 168 * 384).  The
   // adjustment sits inside each role's branch so the compiler budgets each region.
@@ -391,26 +450,10 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
   if (warp == 0) {
     // ================================================================ TMA producer
-    const int32_t* bt = p.block_table + static_cast<size_t>(b) * p.max_pages;
-    if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      tma_prefetch_desc(&kmap_run);
-      tma_prefetch_desc(&vmap_run);
-      mbar_arrive_expect_tx(&q_full, NT * C::kTileBytes);
-      for (int t = 0; t < NT; ++t) {
-        const int node0 = ((mp * NT + t) * kRowTile) / p.G;
-        for (int hh = 0; hh < C::kHalves; ++hh)
-          tma_load_4d(q_s + t * C::kTileBytes + hh * C::kHalfBytes, &qmap, &q_full, hh * 64,
-                      g * p.G, node0, b);
-      }
-    }
     // Page ids travel through registers: lane q < 8 holds page q of the next kLookahead
     // tiles, loaded kLookahead tiles before use so the block-table latency overlaps the
     // wait for free stages.  Pages past the sequence end (and malformed ids, reported)
     // become the out-of-bounds id num_pages, which TMA fills with zeros.
-    constexpr int kLookahead = 4;
     auto load_pid = [&](int j) -> int {
       const int pl = (k0 + j) * kPagesPerTile + lane;
       if (lane >= kPagesPerTile || j >= T || pl * kPage >= L) return p.num_pages;
@@ -418,7 +461,10 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     };
     int pid[kLookahead];
 #pragma unroll
-    for (int u = 0; u < kLookahead; ++u) pid[u] = load_pid(u);
+    for (int u = 0; u < kLookahead; ++u) {
+      const int pl = (k0 + u) * kPagesPerTile + lane;
+      pid[u] = (lane >= kPagesPerTile || u >= T || pl * kPage >= L) ? p.num_pages : s_pid0[u][lane];
+    }
     int bad = 0;
     // When the tile's eight pages are consecutive in the pool (page q == page 0 + q) one
     // 128-row box per 64-column half moves the whole tile; otherwise one box per (page,
@@ -696,8 +742,12 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         f2_split(ffma2(f2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2), x0, x1);
         float p0, p1;
         if (!masked_tile && kPolyEvery > 0 && c % kPolyMod == kPolyMod - 1) {
-          p0 = exp2_poly(x0);             // finite scores only (prefix tiles)
-          p1 = exp2_poly(x1);
+          if (kPolyPacked) {               // finite scores only (prefix tiles)
+            exp2_poly2(x0, x1, p0, p1);
+          } else {
+            p0 = exp2_poly(x0);
+            p1 = exp2_poly(x1);
+          }
         } else {
           p0 = fast_exp2(x0);
           p1 = fast_exp2(x1);
@@ -793,7 +843,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           for (int hh = 0; hh < C::kHalves; ++hh)
             tma_store_4d(&omap, stg + hh * C::kHalfBytes, hh * 64, g * p.G, node_base, b);
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read_all();
         }
       } else {
         uint8_t* stg = sm + C::kKOff + t * 2 * C::kTileBytes;      // [32-col block][128 rows][128 B]
@@ -816,7 +866,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           for (int c = 0; c < D / 32; ++c)
             tma_store_3d(&wmap, stg + c * C::kHalfBytes, c * 32, tile_row0, plane);
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read_all();
         }
       }
       if (valid) {
@@ -844,13 +894,19 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
 // Merges split partials: O = sum_s 2^(lse_s - lse) O_s,  lse = log2 sum_s 2^lse_s.
 // One warp per output row, rows enumerated in the output's [B][N][Hq] order so that
 // consecutive warps write consecutive rows; each lane owns D/32 consecutive columns.
-template <int D>
+// Splits are taken kBatch at a time: lane q fetches split q's LSE while every lane fetches
+// its columns of all kBatch partial rows, so a batch costs one memory round trip.  The
+// host picks the smallest batch that covers the splits: wider batches hold more partial
+// rows in registers and leave fewer warps per SM for the bandwidth-bound many-row case.
+template <int D, int kBatch>
 __global__ void __launch_bounds__(256)
     tree_attention_combine_kernel(const float* __restrict__ ws_o,
                                   const float* __restrict__ ws_lse, int splits, int N, int Hq,
                                   int Hkv, long long rows, uint16_t* __restrict__ out,
                                   float* __restrict__ lse) {
   constexpr int E = D / 32;
+  static_assert(kBatch >= 1 && kBatch <= 16 && (kBatch & (kBatch - 1)) == 0, "batch of splits");
+  using VecE = typename std::conditional<E == 4, float4, float2>::type;
   // Launched as a programmatic dependent of the split kernel: wait for its results.
   grid_dependency_wait();
   const long long rr = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -865,28 +921,40 @@ __global__ void __launch_bounds__(256)
   const long long M = static_cast<long long>(N) * G;
   const long long r = static_cast<long long>(i) * G + (h % G);
   const long long base = (b * Hkv + g) * splits;       // partial row of split s: (base + s) * M + r
+  // With more than one batch the running maximum must be known first.
   float mx = -INFINITY;
-  for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, ws_lse[(base + s) * M + r]);
+  if (splits > kBatch) {
+    for (int s = lane; s < splits; s += 32) mx = fmaxf(mx, ws_lse[(base + s) * M + r]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   float wsum = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < splits; ++s) {
-    const long long prow = (base + s) * M + r;
-    const float l = ws_lse[prow];
-    const float w = (l == -INFINITY) ? 0.f : exp2f(l - mx);
-    wsum += w;
-    const float* o = ws_o + prow * D + lane * E;
+  for (int s0 = 0; s0 < splits; s0 += kBatch) {
+    const int sq = s0 + (lane % kBatch);
+    const float lq = sq < splits ? ws_lse[(base + sq) * M + r] : -INFINITY;
+    VecE v[kBatch];
 #pragma unroll
-    for (int e = 0; e < E; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(o + e);
-      acc[e] += w * v.x;
-      acc[e + 1] += w * v.y;
-      acc[e + 2] += w * v.z;
-      acc[e + 3] += w * v.w;
+    for (int q = 0; q < kBatch; ++q)
+      if (s0 + q < splits)
+        v[q] = *reinterpret_cast<const VecE*>(ws_o + ((base + s0 + q) * M + r) * D + lane * E);
+    if (splits <= kBatch) {
+      mx = lq;
+#pragma unroll
+      for (int o = kBatch / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const float wq = (lq == -INFINITY) ? 0.f : exp2f(lq - mx);
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const float w = __shfl_sync(0xffffffffu, wq, q);
+      if (s0 + q < splits) {
+        wsum += w;
+        const float* vf = reinterpret_cast<const float*>(&v[q]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += w * vf[e];
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -1208,9 +1276,16 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
     const int nsp = pl.splits;
     const long long nrows = static_cast<long long>(rows);
     uint16_t* o16 = static_cast<uint16_t*>(out);
+    auto pick = [&](auto kern4, auto kern8, auto kern16) {
+      return nsp <= 4   ? cudaLaunchKernelEx(&lc, kern4, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse)
+             : nsp <= 8 ? cudaLaunchKernelEx(&lc, kern8, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse)
+                        : cudaLaunchKernelEx(&lc, kern16, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse);
+    };
     const cudaError_t e =
-        D == 128 ? cudaLaunchKernelEx(&lc, tree_attention_combine_kernel<128>, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse)
-                 : cudaLaunchKernelEx(&lc, tree_attention_combine_kernel<64>, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse);
+        D == 128 ? pick(tree_attention_combine_kernel<128, 4>, tree_attention_combine_kernel<128, 8>,
+                        tree_attention_combine_kernel<128, 16>)
+                 : pick(tree_attention_combine_kernel<64, 4>, tree_attention_combine_kernel<64, 8>,
+                        tree_attention_combine_kernel<64, 16>);
     return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
   }
   return JF_OK;

@@ -147,6 +147,11 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until every committed bulk store has finished reading its shared-memory source
+// (the global writes may still be in flight; they complete before the grid does).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // ------------------------------------------------------------------------ clusters
 
