@@ -41,7 +41,13 @@ DEFAULT_CONFIG = "c2_qwen3_8b_chain16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes per attention call from the ncu captures summarised under profiles/ (None
 # until a capture of the current kernel exists for that workload).
-NCU_TRAFFIC_BYTES = {}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one jf_tree_attention call
+# (split kernel + combine) from `ncu --set full` captures of the current kernels; see
+# profiles/tree_attention_<workload>_full.md for the commands.
+NCU_TRAFFIC_BYTES = {
+    "c2_qwen3_8b_chain16": 8666112 + 2403840,
+    "c5_qwen3_30b_b8_tree256_32k": 634844672 + 130994944 + 135288576 + 9617408,
+}
 
 
 # ----------------------------------------------------------------------------- work model
