@@ -59,6 +59,7 @@ constexpr int kRowTile = 128;     // rows per tensor-core tile (TMEM lanes)
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kKeyTile / kPage;
 constexpr float kRescaleThreshold = 8.0f;               // log2 units
+constexpr int kLptMaxB = 256;                           // longest-first dispatch up to this B
 
 // Step records: record i completes once step i - 1 (every row tile's PV of key tile i - 1
 // and S of key tile i) has finished on the tensor cores; record 0 marks the first S MMAs.
@@ -308,7 +309,32 @@ __device__ void merge_cluster(uint8_t* sm, const AttnParams& p, int b, int g, in
   cluster_sync();                                        // nobody leaves while others read it
 }
 
-template <int NT, int D>
+// Longest sequences first: with one CTA per unit and ragged prefixes, CTAs are handed to
+// SMs in block order, so ordering sequences by length (descending, ties by index) keeps
+// one long sequence from starting in the last wave.  Every CTA of the grid ranks all B
+// lengths itself (the same order everywhere) and grid slot `slot` takes the sequence of
+// rank `slot`.  Kept out of line: only longest-first launches call it.
+__device__ __noinline__ int lpt_sequence(const int32_t* prefix_len, int B, int capn, int slot) {
+  __shared__ int s_len[kLptMaxB];
+  __shared__ int s_seq;
+  for (int u = threadIdx.x; u < B; u += blockDim.x) s_len[u] = max(0, min(prefix_len[u], capn));
+  __syncthreads();
+  for (int u = threadIdx.x; u < B; u += blockDim.x) {
+    const int lu = s_len[u];
+    int rank = 0;
+    for (int v = 0; v < B; ++v) {
+      const int lv = s_len[v];
+      rank += (lv > lu || (lv == lu && v < u)) ? 1 : 0;
+    }
+    if (rank == slot) s_seq = u;
+  }
+  __syncthreads();
+  return s_seq;
+}
+
+// LPT: the grid's sequence slots are length ranks (longest-first dispatch); a separate
+// instantiation, so launches without it run exactly the kernel they would otherwise.
+template <int NT, int D, bool LPT>
 __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     tree_attention_kernel(const __grid_constant__ CUtensorMap qmap,
                           const __grid_constant__ CUtensorMap kmap,
@@ -341,7 +367,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const int mp = bid % p.n_groups;
   bid /= p.n_groups;
   const int g = bid % p.Hkv;
-  const int b = bid / p.Hkv;
+  const int slot = bid / p.Hkv;          // a sequence, or its length rank under LPT
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -368,6 +394,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     tma_prefetch_desc(&vmap_run);
   }
   grid_dependency_wait();
+
+  int b = slot;
+  if constexpr (LPT) b = lpt_sequence(p.prefix_len, p.B, p.max_pages * kPage - p.N, slot);
 
   // Q does not depend on the sequence length: its load starts before anything is read.
   if (threadIdx.x == 0) {
@@ -979,7 +1008,7 @@ struct AttnPlan {
   size_t ws_bytes;
 };
 
-template <int NT, int D>
+template <int NT, int D, bool LPT>
 bool ensure_smem_attr() {
   static std::mutex mu;
   static bool done[64] = {false};
@@ -987,7 +1016,7 @@ bool ensure_smem_attr() {
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 64 && done[dev]) return true;
-  if (cudaFuncSetAttribute(tree_attention_kernel<NT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tree_attention_kernel<NT, D, LPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<NT, D>::kSmemBytes) != cudaSuccess)
     return false;
   if (dev < 64) done[dev] = true;
@@ -1011,7 +1040,7 @@ int cluster_capacity(int s) {
   }
   if (cache[dev][s] >= 0) return cache[dev][s];
   int n = 0;
-  if (ensure_smem_attr<NT, D>()) {
+  if (ensure_smem_attr<NT, D, false>()) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(s) * 64);
     cfg.blockDim = dim3(Cfg<NT, D>::kThreads);
@@ -1023,7 +1052,7 @@ int cluster_capacity(int s) {
     a.val.clusterDim.z = 1;
     cfg.attrs = &a;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, tree_attention_kernel<NT, D>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, tree_attention_kernel<NT, D, false>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -1124,12 +1153,12 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NT, int D>
+template <int NT, int D, bool LPT>
 jf_status launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                  const CUtensorMap& kr, const CUtensorMap& vr, const CUtensorMap& om,
                  const CUtensorMap& wm, const AttnParams& prm, long long grid, cudaStream_t s) {
   using C = Cfg<NT, D>;
-  if (!ensure_smem_attr<NT, D>()) return JF_ERR_CUDA;
+  if (!ensure_smem_attr<NT, D, LPT>()) return JF_ERR_CUDA;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(static_cast<unsigned>(grid));
   lc.blockDim = dim3(C::kThreads);
@@ -1148,7 +1177,7 @@ jf_status launch(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap
     lc.numAttrs = 2;
   }
   const cudaError_t e =
-      cudaLaunchKernelEx(&lc, tree_attention_kernel<NT, D>, qm, km, vm, kr, vr, om, wm, prm);
+      cudaLaunchKernelEx(&lc, tree_attention_kernel<NT, D, LPT>, qm, km, vm, kr, vr, om, wm, prm);
   return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
 
@@ -1247,17 +1276,23 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
   prm.n_groups = pl.n_groups; prm.splits = pl.splits; prm.chunk_tiles = pl.chunk_tiles;
   prm.M = N * G;
   prm.cluster_merge = pl.cluster ? 1 : 0;
+  // Longest-first dispatch when every unit is one CTA and sequence lengths may differ.
+  const bool lpt = pl.splits == 1 && B >= 2 && B <= jf::kLptMaxB;
   prm.scale_log2 = scale * 1.4426950408889634f;
   const long long grid = static_cast<long long>(B) * Hkv * pl.splits * pl.n_groups;
   if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   jf_status st;
   if (D == 128)
-    st = pl.NT == 2 ? launch<2, 128>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
-                    : launch<1, 128>(qm, km, vm, kr, vr, om, wm, prm, grid, s);
+    st = pl.NT == 2 ? (lpt ? launch<2, 128, true>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
+                           : launch<2, 128, false>(qm, km, vm, kr, vr, om, wm, prm, grid, s))
+                    : (lpt ? launch<1, 128, true>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
+                           : launch<1, 128, false>(qm, km, vm, kr, vr, om, wm, prm, grid, s));
   else
-    st = pl.NT == 2 ? launch<2, 64>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
-                    : launch<1, 64>(qm, km, vm, kr, vr, om, wm, prm, grid, s);
+    st = pl.NT == 2 ? (lpt ? launch<2, 64, true>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
+                           : launch<2, 64, false>(qm, km, vm, kr, vr, om, wm, prm, grid, s))
+                    : (lpt ? launch<1, 64, true>(qm, km, vm, kr, vr, om, wm, prm, grid, s)
+                           : launch<1, 64, false>(qm, km, vm, kr, vr, om, wm, prm, grid, s));
   if (st != JF_OK) return st;
   if (pl.splits > 1 && !pl.cluster) {
     const long long nb = (static_cast<long long>(rows) + 7) / 8;

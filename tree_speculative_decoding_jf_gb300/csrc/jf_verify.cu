@@ -145,6 +145,11 @@ __global__ void __launch_bounds__(kArgmaxThreads)
   grid_dependents_launch();
 }
 
+// Threads of a walk block: the tree rounded up to whole warps, at least four warps (the
+// chunk-key merge wants loads in flight) and at most kWalkThreads, so small trees pay for
+// cheap barriers.  With fewer than kWalkThreads threads, N fits in one pass of the block.
+inline int walk_threads(int N) { return std::min(kWalkThreads, std::max(128, (N + 31) / 32 * 32)); }
+
 __global__ void __launch_bounds__(kWalkThreads)
     tree_walk_kernel(const uint64_t* __restrict__ part, int chunks,
                      const int32_t* __restrict__ draft, const int32_t* __restrict__ parent,
@@ -167,33 +172,65 @@ __global__ void __launch_bounds__(kWalkThreads)
   grid_dependency_wait();
   const int b = blockIdx.x;
   const size_t rb = static_cast<size_t>(b) * N;
+  // The block is sized to the tree (threadIdx.x + k * blockDim.x covers every node for
+  // k < kPer).  Parents and drafts are requested first and stay in flight while the
+  // chunk keys are merged, so both arrive in one memory round trip.
+  constexpr int kPer = (JF_MAX_NODES + kWalkThreads - 1) / kWalkThreads;
+  int r_par[kPer], r_draft[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < N) {
+      r_par[k] = parent[rb + i];
+      r_draft[k] = draft[rb + i];
+    }
+  }
   // Chunk keys of every row, all loads in flight together: (row, chunk) pairs spread over
   // the block, combined per row with a shared-memory 64-bit atomicMax.
   for (int i = threadIdx.x; i < N; i += blockDim.x) s_best[i] = 0ull;
   __syncthreads();
   {
+    // Keys are fetched kKeyBatch per thread before any is merged, so a block of 128
+    // threads has 1024 of them in flight per round trip.
+    constexpr int kKeyBatch = 8;
     const int total = N * chunks;
     const uint64_t* pk = part + rb * chunks;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) atomicMax(&s_best[e / chunks], pk[e]);
+    for (int e0 = threadIdx.x; e0 < total; e0 += blockDim.x * kKeyBatch) {
+      uint64_t kv[kKeyBatch];
+#pragma unroll
+      for (int u = 0; u < kKeyBatch; ++u) {
+        const int e = e0 + u * static_cast<int>(blockDim.x);
+        kv[u] = e < total ? pk[e] : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kKeyBatch; ++u) {
+        const int e = e0 + u * static_cast<int>(blockDim.x);
+        if (e < total) atomicMax(&s_best[e / chunks], kv[u]);
+      }
+    }
+  }
+  int bad_parent = 0, bad_token = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < N) {
+      int p = r_par[k];
+      const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+      if (!ok) { bad_parent = 1; p = -1; }
+      s_par[i] = p;
+      s_anc[i] = p;
+      s_dep[i] = p >= 0 ? 1 : 0;
+      s_key[i] = 0u;
+      const int d = r_draft[k];
+      s_draft[i] = d;
+      if (i > 0 && (d < 0 || d >= V)) bad_token = 1;
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     const int am = static_cast<int>(~static_cast<uint32_t>(s_best[i] & 0xFFFFFFFFull));
     s_am[i] = am;
     if (argmax_out != nullptr) argmax_out[rb + i] = am;
-  }
-  int bad_parent = 0, bad_token = 0;
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    int p = parent[rb + i];
-    const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
-    if (!ok) { bad_parent = 1; p = -1; }
-    s_par[i] = p;
-    s_anc[i] = p;
-    s_dep[i] = p >= 0 ? 1 : 0;
-    s_key[i] = 0u;
-    const int d = draft[rb + i];
-    s_draft[i] = d;
-    if (i > 0 && (d < 0 || d >= V)) bad_token = 1;
   }
   bad_parent = __syncthreads_or(bad_parent);
   bad_token = __syncthreads_or(bad_token);
@@ -203,13 +240,12 @@ __global__ void __launch_bounds__(kWalkThreads)
   }
 
   // Depth by pointer jumping: dep[i] += dep[anc[i]], anc[i] = anc[anc[i]].
-  constexpr int kPer = (JF_MAX_NODES + kWalkThreads - 1) / kWalkThreads;
   for (int round = 0; round < 32; ++round) {
     int nd[kPer], na[kPer];
     int any = 0;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * kWalkThreads;
+      const int i = threadIdx.x + k * blockDim.x;
       if (i < N) {
         const int a = s_anc[i];
         nd[k] = s_dep[i];
@@ -224,7 +260,7 @@ __global__ void __launch_bounds__(kWalkThreads)
     if (!__syncthreads_or(any)) break;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-      const int i = threadIdx.x + k * kWalkThreads;
+      const int i = threadIdx.x + k * blockDim.x;
       if (i < N) { s_dep[i] = nd[k]; s_anc[i] = na[k]; }
     }
     __syncthreads();
@@ -333,7 +369,7 @@ extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int
                              static_cast<int>(smem)) != cudaSuccess)
       return JF_ERR_CUDA;
   }
-  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::kWalkThreads), smem,
+  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::walk_threads(N)), smem,
                                         s, static_cast<const uint64_t*>(part), p.chunks, draft,
                                         parent, N, V, argmax, accept_len, path, bonus, dev_err);
   return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
@@ -404,7 +440,7 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
       cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return JF_ERR_CUDA;
-  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::kWalkThreads), smem,
+  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::walk_threads(N)), smem,
                                         s, static_cast<const uint64_t*>(part), p.chunks, draft,
                                         parent, N, V, argmax, accept_len, path, bonus, dev_err);
   return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
