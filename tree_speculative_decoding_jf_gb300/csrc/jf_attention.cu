@@ -240,8 +240,15 @@ __device__ __forceinline__ float* part_lse(uint8_t* sm, int t) {
   return reinterpret_cast<float*>(sm + Cfg<NT, D>::kPartLseOff + t * kRowTile * 4);
 }
 
+// Out of line: the merge runs once per CTA and its code stays out of the hot loops' way.
+struct MergeArgs {
+  uint16_t* out;
+  float* lse;
+  int N, Hq, G, M, splits;
+};
+
 template <int NT, int D>
-__device__ void merge_cluster(uint8_t* sm, const AttnParams& p, int b, int g, int mp, int rank) {
+__device__ __noinline__ void merge_cluster(uint8_t* sm, const MergeArgs p, int b, int g, int mp, int rank) {
   constexpr int kChunks = D / 4;                         // 16-byte chunks per fp32 row
   constexpr int kMaxSplits = 8;
   cluster_sync();                                        // every split's partial is written
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       __syncthreads();
       for (int t = 0; t < NT; ++t)
         for (int e = threadIdx.x; e < kRowTile; e += blockDim.x) part_lse<NT, D>(sm, t)[e] = -INFINITY;
-      merge_cluster<NT, D>(sm, p, b, g, mp, split);
+      merge_cluster<NT, D>(sm, MergeArgs{p.out, p.lse, p.N, p.Hq, p.G, p.M, p.splits}, b, g, mp, split);
       return;
     }
     if (warp >= 4) {                  // split past the sequence: an empty partial (weight 0)
@@ -911,7 +918,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     }
   }
 
-  if (p.cluster_merge) merge_cluster<NT, D>(sm, p, b, g, mp, split);
+  if (p.cluster_merge) merge_cluster<NT, D>(sm, MergeArgs{p.out, p.lse, p.N, p.Hq, p.G, p.M, p.splits}, b, g, mp, split);
 
   tc_fence_before();
   __syncthreads();
