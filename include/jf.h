@@ -59,6 +59,7 @@ typedef enum { JF_DTYPE_BF16 = 0, JF_DTYPE_F32 = 1 } jf_dtype;
 #define JF_DEVERR_BAD_PREFIX 0x4 /* prefix_len < 0 or prefix_len + N > max_pages * page */
 #define JF_DEVERR_BAD_TOKEN 0x8  /* draft token (non-root node) outside [0, V)          */
 #define JF_DEVERR_TIMEOUT 0x10   /* an in-kernel wait gave up after its time limit      */
+#define JF_DEVERR_BAD_PATH 0x20  /* accepted path / length malformed (KV compaction)     */
 
 /* Largest tree (nodes per sequence) any call accepts. */
 #define JF_MAX_NODES 4096
@@ -195,6 +196,38 @@ jf_status jf_tree_verify_static(const void* logits, int32_t dtype, const int32_t
                                 const int32_t* parent, int32_t B, int32_t N, int32_t V,
                                 int32_t* argmax, int32_t* accept_len, int32_t* path,
                                 int32_t* bonus, int32_t* dev_err, jf_stream_t stream);
+
+/* ---------------------------------------------------------------- after verification
+ * jf_compact_accepted_kv -- moves the K/V of the accepted draft path next to the prefix,
+ * so the next decoding step continues from one contiguous context.  JetFlow explainer
+ * ("JetFlow: Breaking the Scaling Ceiling of Speculative Decoding with Parallel Tree
+ * Drafting"), technical summary §2 "Method": draft-tree nodes keep their K/V after the
+ * prefix and the accepted branch is what the target continues from; the pages do not
+ * spell out the cache update, so the plainest reading is implemented:
+ *   for every sequence b with a = accept_len[b] and P = prefix_len[b], for k = 1..a in
+ *   increasing order, the K and V rows (all kv-heads) at logical position P + path[b][k]
+ *   are copied to position P + k; then new_prefix_len[b] = P + a + 1 (the root and the
+ *   accepted nodes join the prefix; the bonus token's K/V come from the next forward
+ *   pass).  Because path[k] >= k rises strictly, a source is never overwritten before
+ *   it is read in that order; the kernel reproduces exactly this sequential result.
+ * Arguments:
+ *   k_cache, v_cache  bf16 [num_pages][page_size][Hkv][D], modified in place.
+ *   block_table       int32 [B][max_pages]; prefix_len int32 [B] (read only).
+ *   path, accept_len  int32 [B][N] and [B], as written by jf_tree_verify.
+ *   new_prefix_len    int32 [B] out; must not alias prefix_len.
+ *   dev_err           may be NULL.
+ * Only positions P + 1 .. P + a are written.  A sequence whose prefix length, accepted
+ * length, path (path[0] == 0, strictly increasing, inside [0, N)) or block-table entries
+ * are malformed is left unchanged (new_prefix_len = P) and sets JF_DEVERR_BAD_PREFIX,
+ * JF_DEVERR_BAD_PATH or JF_DEVERR_BAD_PAGE.
+ * Limits: D in {64, 128}, page_size 16, 1 <= N <= JF_MAX_NODES, caches 16-byte aligned.
+ */
+jf_status jf_compact_accepted_kv(void* k_cache, void* v_cache, const int32_t* block_table,
+                                 const int32_t* prefix_len, const int32_t* path,
+                                 const int32_t* accept_len, int32_t B, int32_t N, int32_t Hkv,
+                                 int32_t D, int32_t page_size, int32_t max_pages,
+                                 int32_t num_pages, int32_t* new_prefix_len, int32_t* dev_err,
+                                 jf_stream_t stream);
 
 #ifdef __cplusplus
 } /* extern "C" */

@@ -45,8 +45,11 @@ def _load():
         lib.jfo_argmax_f32.argtypes = [P, i64, i64, P]
         lib.jfo_argmax_bf16.argtypes = [P, i64, i64, P]
         lib.jfo_tree_walk.argtypes = [P, P, P, i32, i32, P, P, P]
+        lib.jfo_compact_accepted_kv.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                                i32, P]
         for f in ("jfo_tree_mask", "jfo_tree_attention_rows", "jfo_attention_probs",
-                  "jfo_argmax_f32", "jfo_argmax_bf16", "jfo_tree_walk"):
+                  "jfo_argmax_f32", "jfo_argmax_bf16", "jfo_tree_walk",
+                  "jfo_compact_accepted_kv"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -163,3 +166,25 @@ def tree_verify(w):
     am = argmax(w.logits, w.logits_dtype)
     acc, path, bonus = tree_walk(am, w.draft, w.parent)
     return am, acc, path, bonus
+
+
+def compact_accepted_kv(k_cache: np.ndarray, v_cache: np.ndarray, block_table: np.ndarray,
+                        prefix_len: np.ndarray, path: np.ndarray, accept_len: np.ndarray,
+                        page: int = 16):
+    """Accepted-path KV compaction on copies of the caches (see jfo_compact_accepted_kv).
+    Returns (k_cache, v_cache, new_prefix_len, ok) where ok is False if any sequence was
+    malformed (and left unchanged)."""
+    k = np.ascontiguousarray(k_cache, dtype=np.uint16).copy()
+    v = np.ascontiguousarray(v_cache, dtype=np.uint16).copy()
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    pl = np.ascontiguousarray(prefix_len, dtype=np.int32)
+    pth = np.ascontiguousarray(path, dtype=np.int32)
+    al = np.ascontiguousarray(accept_len, dtype=np.int32)
+    B, N = pth.shape
+    num_pages, pg, Hkv, D = k.shape
+    assert pg == page
+    newp = np.empty(B, np.int32)
+    rc = _load().jfo_compact_accepted_kv(_p(k), _p(v), _p(bt), _p(pl), _p(pth), _p(al), B, N, Hkv,
+                                         D, page, bt.shape[1], num_pages, _p(newp))
+    return k, v, newp, rc == 0
+

@@ -287,3 +287,46 @@ int jfo_tree_walk(const int32_t *argmax, const int32_t *draft, const int32_t *pa
     }
     return rc;
 }
+
+/* Accepted-path KV compaction (row "accepted-path KV compaction" after verification;
+ * JetFlow explainer, technical summary §2 "Method": draft nodes keep their K/V after the
+ * prefix, the accepted branch is the context the target continues from; the cache update
+ * itself is not spelled out on the pages, so the plainest reading is taken).
+ * For sequence b with a = accept_len[b] and P = prefix_len[b], for k = 1..a in order, the
+ * K and V rows of every kv-head at logical position P + path[k] are copied to P + k;
+ * new_prefix_len[b] = P + a + 1.  A sequence with a malformed prefix length, accepted
+ * length, path (path[0] == 0, strictly increasing, inside [0, N)) or block-table entry is
+ * left unchanged with new_prefix_len[b] = P; the function then returns JFO_BAD_ARG. */
+int jfo_compact_accepted_kv(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_table,
+                            const int32_t *prefix_len, const int32_t *path,
+                            const int32_t *accept_len, int B, int N, int Hkv, int D, int page,
+                            int max_pages, int num_pages, int32_t *new_prefix_len) {
+    int rc = JFO_OK;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *bt = block_table + (long)b * max_pages;
+        const int32_t *pth = path + (long)b * N;
+        const int P = prefix_len[b], a = accept_len[b];
+        int ok = P >= 0 && (long)P + N <= (long)max_pages * page && a >= 0 && a <= N - 1;
+        for (int k = 0; ok && k <= a; ++k) {
+            if (k == 0 ? pth[0] != 0 : (pth[k] <= pth[k - 1] || pth[k] >= N)) ok = 0;
+            else {
+                const int ps = bt[(P + pth[k]) / page], pd = bt[(P + k) / page];
+                if (ps < 0 || ps >= num_pages || pd < 0 || pd >= num_pages) ok = 0;
+            }
+        }
+        new_prefix_len[b] = ok ? P + a + 1 : P;
+        if (!ok) { rc = JFO_BAD_ARG; continue; }
+        for (int k = 1; k <= a; ++k) {
+            const int ts = P + pth[k], td = P + k;
+            for (int g = 0; g < Hkv; ++g) {
+                const long src = (((long)bt[ts / page] * page + ts % page) * Hkv + g) * D;
+                const long dst = (((long)bt[td / page] * page + td % page) * Hkv + g) * D;
+                for (int d = 0; d < D; ++d) {
+                    k_cache[dst + d] = k_cache[src + d];
+                    v_cache[dst + d] = v_cache[src + d];
+                }
+            }
+        }
+    }
+    return rc;
+}

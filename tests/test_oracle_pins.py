@@ -472,3 +472,85 @@ def test_c1_config_shape_and_forcing():
     am = oracle.argmax(w.logits, "f32")
     forced = [c for c in range(1, 16) if w.draft[0, c] == am[0, w.parent[0, c]]]
     assert len(forced) >= 3
+
+
+# ---------------------------------------------------------------- accepted-path KV compaction
+
+def _logical_rows(cache, block_table, b, L, page=16):
+    """Rows of sequence b at logical positions 0..L-1, read through its block table."""
+    return np.stack([cache[block_table[b, t // page], t % page] for t in range(L)])
+
+
+def _compaction_by_lists(w, path, acc):
+    """Independent restatement: each sequence's context is a list of rows; the new context
+    keeps the prefix, then the rows of the accepted path in order, then whatever followed
+    (positions past the accepted path are not touched).  The lists are written back through
+    the block tables into copies of the pool."""
+    k, v = w.k_cache.copy(), w.v_cache.copy()
+    newp = np.empty(w.B, np.int32)
+    for b in range(w.B):
+        P, a = int(w.prefix_len[b]), int(acc[b])
+        L = P + w.N
+        ks, vs = _logical_rows(w.k_cache, w.block_table, b, L), _logical_rows(w.v_cache, w.block_table, b, L)
+        order = list(range(P)) + [P + int(path[b, j]) for j in range(a + 1)] + list(range(P + a + 1, L))
+        for t, src in enumerate(order):
+            k[w.block_table[b, t // 16], t % 16] = ks[src]
+            v[w.block_table[b, t // 16], t % 16] = vs[src]
+        newp[b] = P + a + 1
+    return k, v, newp
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_compaction_matches_list_restatement(seed):
+    w = wl.make_workload("cmp", 3, 12, 4, 2, 64, 64, np.array([5, 17, 40], np.int32),
+                         tree="random_depth_limited", permute_pages=True, seed=seed,
+                         with_logits=False)
+    path, acc = wl.random_accepted_paths(w.parent, seed)
+    k, v, newp, ok = oracle.compact_accepted_kv(w.k_cache, w.v_cache, w.block_table,
+                                                w.prefix_len, path, acc)
+    ek, ev, enewp = _compaction_by_lists(w, path, acc)
+    assert ok
+    assert (newp == enewp).all()
+    assert (k == ek).all() and (v == ev).all()
+
+
+def test_compaction_overlapping_path_reads_before_writes():
+    """path [0, 2, 3, 5]: the row that lands on position P+2 is also the source of P+1."""
+    w = wl.make_workload("ovl", 1, 8, 2, 1, 64, 64, 19, tree="chain", seed=4, with_logits=False)
+    parent = np.array([[-1, 0, 0, 2, 3, 3, 5, 6]], np.int32)
+    path = np.array([[0, 2, 3, 5, -1, -1, -1, -1]], np.int32)
+    acc = np.array([3], np.int32)
+    k, _, newp, ok = oracle.compact_accepted_kv(w.k_cache, w.v_cache, w.block_table,
+                                                w.prefix_len, path, acc)
+    assert ok and newp[0] == 19 + 4
+    rows_before = _logical_rows(w.k_cache, w.block_table, 0, 27)
+    rows_after = _logical_rows(k, w.block_table, 0, 27)
+    for j, node in enumerate([0, 2, 3, 5]):
+        assert (rows_after[19 + j] == rows_before[19 + node]).all()
+    assert (rows_after[:19] == rows_before[:19]).all()
+    assert (rows_after[23:] == rows_before[23:]).all()
+    del parent
+
+
+def test_compaction_chain_and_empty_path_are_no_ops():
+    w = wl.make_workload("noop", 2, 10, 4, 2, 128, 64, np.array([3, 33], np.int32),
+                         tree="chain", seed=5, with_logits=False)
+    chain = np.tile(np.arange(10, dtype=np.int32), (2, 1))
+    for acc in (np.array([9, 4], np.int32), np.array([0, 0], np.int32)):
+        path = np.where(np.arange(10)[None, :] <= acc[:, None], chain, -1).astype(np.int32)
+        k, v, newp, ok = oracle.compact_accepted_kv(w.k_cache, w.v_cache, w.block_table,
+                                                    w.prefix_len, path, acc)
+        assert ok and (newp == w.prefix_len + acc + 1).all()
+        assert (k == w.k_cache).all() and (v == w.v_cache).all()
+
+
+def test_compaction_rejects_malformed_and_leaves_sequence():
+    w = wl.make_workload("bad", 2, 6, 2, 1, 64, 64, np.array([4, 9], np.int32),
+                         tree="chain", seed=6, with_logits=False)
+    path = np.array([[0, 3, 2, -1, -1, -1], [0, 1, 2, -1, -1, -1]], np.int32)   # b=0 not increasing
+    acc = np.array([2, 2], np.int32)
+    k, _, newp, ok = oracle.compact_accepted_kv(w.k_cache, w.v_cache, w.block_table,
+                                                w.prefix_len, path, acc)
+    assert not ok
+    assert newp[0] == 4 and newp[1] == 9 + 3
+    assert (_logical_rows(k, w.block_table, 0, 10) == _logical_rows(w.k_cache, w.block_table, 0, 10)).all()

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "JF_OK", 1: "JF_ERR_INVALID_ARGUMENT", 2: "JF_ERR_INVALID_TRE
                 6: "JF_ERR_TIMEOUT", 7: "JF_ERR_MISALIGNED", 8: "JF_ERR_SCRATCH_CAPACITY"}
 JF_DTYPE_BF16, JF_DTYPE_F32 = 0, 1
 DEVERR_BAD_PARENT, DEVERR_BAD_PAGE, DEVERR_BAD_PREFIX = 0x1, 0x2, 0x4
-DEVERR_BAD_TOKEN, DEVERR_TIMEOUT = 0x8, 0x10
+DEVERR_BAD_TOKEN, DEVERR_TIMEOUT, DEVERR_BAD_PATH = 0x8, 0x10, 0x20
 MAX_NODES = 4096
 PAGE_SIZE = 16
 
@@ -57,6 +57,9 @@ def _load():
     lib.jf_tree_verify.restype = ctypes.c_int
     lib.jf_tree_verify_static.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P, P, P, P]
     lib.jf_tree_verify_static.restype = ctypes.c_int
+    lib.jf_compact_accepted_kv.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                           P, P, P]
+    lib.jf_compact_accepted_kv.restype = ctypes.c_int
     return lib
 
 
@@ -213,6 +216,26 @@ def jf_tree_verify_static(logits, draft, parent, accept_len, path, bonus, argmax
         _ptr(path), _ptr(bonus), _ptr(dev_err), _stream(stream)))
 
 
+def jf_compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,
+                           new_prefix_len, dev_err=None, stream=None) -> None:
+    """Moves the accepted path's K/V next to the prefix, in place (see include/jf.h)."""
+    num_pages, page, Hkv, D = k_cache.shape
+    B, N = path.shape
+    _need(k_cache, "k_cache", torch.bfloat16)
+    _need(v_cache, "v_cache", torch.bfloat16, tuple(k_cache.shape))
+    _need(block_table, "block_table", torch.int32)
+    for name, t, shape in (("prefix_len", prefix_len, (B,)), ("accept_len", accept_len, (B,)),
+                           ("new_prefix_len", new_prefix_len, (B,))):
+        _need(t, name, torch.int32, shape)
+    _need(path, "path", torch.int32, (B, N))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_compact_accepted_kv", _lib.jf_compact_accepted_kv(
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(prefix_len), _ptr(path),
+        _ptr(accept_len), B, N, Hkv, D, page, block_table.shape[1], num_pages,
+        _ptr(new_prefix_len), _ptr(dev_err), _stream(stream)))
+
+
 # ----------------------------------------------------------------------------- conveniences
 
 def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
@@ -256,3 +279,13 @@ def tree_verify(logits, draft, parent, dev_err=None, stream=None):
     ws = _workspace(jf_tree_verify_workspace_size(B, N, V), dev)
     jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax, ws, dev_err, stream)
     return argmax, accept_len, path, bonus
+
+
+def compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,
+                        dev_err=None, stream=None):
+    """In-place KV compaction after verification; returns the new prefix lengths."""
+    new_prefix_len = torch.empty_like(prefix_len)
+    jf_compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,
+                           new_prefix_len, dev_err, stream)
+    return new_prefix_len
+

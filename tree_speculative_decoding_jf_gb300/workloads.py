@@ -319,3 +319,24 @@ def device_tensors(w: Workload, device="cuda", with_logits: bool = True) -> dict
         else:
             d["logits"] = bf16(w.logits)
     return d
+
+def random_accepted_paths(parent: np.ndarray, seed: int = 0):
+    """Seeded synthetic verify outputs for the KV-compaction row: per sequence, a node
+    drawn uniformly and its root path (node ids from the root, -1 padded) with the path's
+    length in accepted draft nodes (the root excluded).  Returns (path, accept_len)."""
+    parent = np.asarray(parent, dtype=np.int32)
+    B, N = parent.shape
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x9A7E]))
+    path = np.full((B, N), -1, dtype=np.int32)
+    acc = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        node = int(rng.integers(0, N))
+        chain = []
+        while node >= 0:
+            chain.append(node)
+            node = int(parent[b, node])
+        chain.reverse()
+        path[b, :len(chain)] = chain
+        acc[b] = len(chain) - 1
+    return path, acc
+
