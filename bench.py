@@ -331,6 +331,30 @@ def run_gpu(args, w, rank, world):
             e2e_ms.append(a.elapsed_time(b_))
         e2e = {"value": statistics.mean(e2e_ms) * 1e3, "unit": "µs/call",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    # ---- before verification: best-first draft-tree construction from per-depth draft
+    # logits (16 depths, 8 candidates per depth, the workload's budget); not part of the step.
+    dl = wl.draft_logits(B, 16, V, seed=w.seed)
+    t_dl = torch.from_numpy(dl.view(np.int16)).view(torch.bfloat16).to(dev)
+    K_tree = 8
+    tree_out = dict(cand_token=torch.empty((B, 16, K_tree), dtype=torch.int32, device=dev),
+                    cand_logp=torch.empty((B, 16, K_tree), dtype=torch.float32, device=dev),
+                    parent=torch.empty((B, N), dtype=torch.int32, device=dev),
+                    draft=torch.empty((B, N), dtype=torch.int32, device=dev),
+                    depth=torch.empty((B, N), dtype=torch.int32, device=dev))
+
+    def call_tree():
+        jf.jf_build_draft_tree(t_dl, K_tree, N, tree_out["cand_token"], tree_out["cand_logp"],
+                               tree_out["parent"], tree_out["draft"], tree_out["depth"])
+
+    call_tree()
+    g_tree = capture(call_tree)
+    for k in range(args.warmup):
+        timed(g_tree, k)
+    tree_ev = [timed(g_tree, k) for k in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    tree_ms = [a.elapsed_time(b_) for a, b_ in tree_ev]
+    tree_bytes = int(t_dl.numel()) * 2
+
     # ---- after verification: accepted-path KV compaction (not part of the step).  It
     # rewrites the cache in place, so it is timed last; replays repeat the same copies.
     new_prefix = torch.empty_like(t["prefix_len"])
@@ -349,7 +373,8 @@ def run_gpu(args, w, rank, world):
         raise RuntimeError(f"device error bits {err.item():#x} in the KV compaction")
     return dict(step_ms=step_ms, mask_ms=mask_ms, attn_ms=attn_ms, ver_ms=ver_ms, clocks=clk,
                 e2e=e2e, launches=2 * launches_per_step * args.steps, ws=ws_a_bytes,
-                compact_ms=compact_ms, accepted=acc.cpu().tolist())
+                compact_ms=compact_ms, accepted=acc.cpu().tolist(), tree_ms=tree_ms,
+                tree_bytes=tree_bytes)
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -464,6 +489,9 @@ def main():
                          "verify": statistics.mean(r["ver_ms"]) * 1e3,
                          "verify_hbm_gbs": verify_algorithmic_bytes(w) /
                          (statistics.mean(r["ver_ms"]) * 1e-3) / 1e9,
+                         "draft_tree_build": statistics.mean(r["tree_ms"]) * 1e3,
+                         "draft_tree_logits_hbm_gbs": r["tree_bytes"] /
+                         (statistics.mean(r["tree_ms"]) * 1e-3) / 1e9,
                          "kv_compaction_after_verify": statistics.mean(r["compact_ms"]) * 1e3,
                          "kv_compaction_accepted_nodes": r["accepted"]},
         "roofline": roof, "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["launches"],

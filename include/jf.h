@@ -197,6 +197,34 @@ jf_status jf_tree_verify_static(const void* logits, int32_t dtype, const int32_t
                                 int32_t* argmax, int32_t* accept_len, int32_t* path,
                                 int32_t* bonus, int32_t* dev_err, jf_stream_t stream);
 
+/* ---------------------------------------------------------------- before verification
+ * jf_build_draft_tree -- builds the draft tree from per-depth draft logits.  JetFlow
+ * explainer ("JetFlow: Breaking the Scaling Ceiling of Speculative Decoding with Parallel
+ * Tree Drafting"), technical summary §2 "Method", tree construction: the draft head emits
+ * logits for every depth in one pass, a branch score (by default the cumulative draft
+ * log-probability) ranks nodes, and a best-first expansion builds the tree up to a budget.
+ * Computed here (the pages fix no more detail; this is the plainest reading):
+ *   1. candidates: for sequence b and depth d = 1..Dmax (row d-1 of draft_logits[b]), the
+ *      K tokens with the largest logits (lower token id on ties), in that order, with
+ *      log-probabilities logit - logsumexp(row), fp32 -> cand_token / cand_logp
+ *      [B][Dmax][K].
+ *   2. tree: the root (depth 0, score 0, token root_token[b]) and, below every node of
+ *      depth d < Dmax, the K depth-(d+1) candidates as children (child score =
+ *      fp32(parent score + candidate log-prob)).  Best-first expansion to N nodes takes
+ *      nodes in the order (score descending, depth ascending, rank path ascending); node
+ *      ids follow that order, so parent[i] < i.  Outputs parent (root -1), draft (token;
+ *      root_token[b] or -1 for the root when root_token is NULL), depth and score (may be
+ *      NULL), all [B][N].
+ * Arguments: draft_logits bf16 or fp32 [B][Dmax][V] (dtype JF_DTYPE_*), device pointers.
+ * Limits: 1 <= K <= 8, 1 <= Dmax <= 16, 1 <= N <= 256, N * (K + 1) <= 4096, V >= K, and
+ *   the candidate lattice must hold N nodes (1 + K + ... + K^Dmax >= N); otherwise
+ *   JF_ERR_UNSUPPORTED.  Logits must be finite.
+ */
+jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype, const int32_t* root_token,
+                              int32_t B, int32_t Dmax, int32_t V, int32_t K, int32_t N,
+                              int32_t* cand_token, float* cand_logp, int32_t* parent,
+                              int32_t* draft, int32_t* depth, float* score, jf_stream_t stream);
+
 /* ---------------------------------------------------------------- after verification
  * jf_compact_accepted_kv -- moves the K/V of the accepted draft path next to the prefix,
  * so the next decoding step continues from one contiguous context.  JetFlow explainer

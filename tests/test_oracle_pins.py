@@ -554,3 +554,82 @@ def test_compaction_rejects_malformed_and_leaves_sequence():
     assert not ok
     assert newp[0] == 4 and newp[1] == 9 + 3
     assert (_logical_rows(k, w.block_table, 0, 10) == _logical_rows(w.k_cache, w.block_table, 0, 10)).all()
+
+
+# ---------------------------------------------------------------- best-first draft tree
+
+from oracle import draft_tree as odt    # noqa: E402
+
+
+def test_draft_candidates_logp_matches_torch_log_softmax():
+    x = wl.bf16_bits_to_f32(wl.draft_logits(1, 3, 5000, seed=1))[0]
+    for d in range(3):
+        tok, lp = odt.depth_candidates(x[d], 8)
+        ref = torch.log_softmax(torch.from_numpy(x[d]).double(), dim=0).numpy()
+        assert np.allclose(lp, ref[tok], rtol=0, atol=1e-12)
+        order = np.lexsort((np.arange(x.shape[1]), -x[d].astype(np.float64)))
+        assert (tok == order[:8]).all()
+
+
+def test_draft_candidates_ties_take_lower_ids():
+    x = np.zeros(50, np.float32)
+    x[[7, 3, 40]] = 2.0
+    x[[1, 9]] = 1.0
+    tok, _ = odt.depth_candidates(x, 6)
+    assert tok.tolist() == [3, 7, 40, 1, 9, 0]
+
+
+def _lattice_brute_force(ct, lp, N, root):
+    """Every node of the lattice (rank paths up to Dmax), scored in fp32 from the root,
+    sorted by (score desc, depth, rank path); the first N with parents looked up by path."""
+    Dmax, K = ct.shape
+    lp32 = lp.astype(np.float32)
+    nodes = [((), np.float32(0.0))]
+    frontier = [((), np.float32(0.0))]
+    for d in range(Dmax):
+        nxt = []
+        for path, s in frontier:
+            for r in range(K):
+                nxt.append((path + (r,), np.float32(s + lp32[d, r])))
+        nodes += nxt
+        frontier = nxt
+    nodes.sort(key=lambda n: (-float(n[1]), len(n[0]), n[0]))
+    top = nodes[:N]
+    index = {path: i for i, (path, _) in enumerate(top)}
+    parent = [index.get(p[:-1], -2) if p else -1 for p, _ in top]
+    draft = [root if not p else int(ct[len(p) - 1, p[-1]]) for p, _ in top]
+    return (np.array(parent), np.array(draft), np.array([len(p) for p, _ in top]),
+            np.array([s for _, s in top], np.float32))
+
+
+@pytest.mark.parametrize("K,Dmax,N,seed", [(2, 4, 20, 0), (3, 3, 30, 1), (4, 3, 40, 2),
+                                           (1, 6, 7, 3), (5, 1, 6, 4)])
+def test_best_first_matches_lattice_brute_force(K, Dmax, N, seed):
+    rng = np.random.default_rng(seed)
+    ct = rng.integers(0, 1000, size=(Dmax, K))
+    lp = np.sort(rng.standard_normal((Dmax, K)) * 2 - 3, axis=1)[:, ::-1].copy()
+    got = odt.best_first_tree(ct, lp, N, root_token=77)
+    ref = _lattice_brute_force(ct, lp, N, 77)
+    for g, r in zip(got, ref):
+        assert (np.asarray(g) == np.asarray(r)).all()
+
+
+def test_best_first_equal_scores_prefer_shallow_then_small_rank():
+    ct = np.array([[10, 11], [20, 21]])
+    lp = np.zeros((2, 2))                      # every node scores 0: pure tie-breaking
+    parent, draft, depth, _ = odt.best_first_tree(ct, lp, 7, root_token=5)
+    assert depth.tolist() == [0, 1, 1, 2, 2, 2, 2]
+    assert draft.tolist() == [5, 10, 11, 20, 21, 20, 21]
+    assert parent.tolist() == [-1, 0, 0, 1, 1, 2, 2]
+
+
+def test_best_first_invariants_random():
+    x = wl.bf16_bits_to_f32(wl.draft_logits(1, 16, 2000, seed=7))[0]
+    tok, lp = odt.candidates(x[None], 8)
+    parent, draft, depth, score = odt.best_first_tree(tok[0], lp[0], 256, root_token=3)
+    assert parent[0] == -1 and depth[0] == 0 and draft[0] == 3
+    for i in range(1, 256):
+        p = parent[i]
+        assert 0 <= p < i and depth[i] == depth[p] + 1 and score[i] <= score[p]
+        assert draft[i] in tok[0, depth[i] - 1]
+    assert depth.max() <= 16

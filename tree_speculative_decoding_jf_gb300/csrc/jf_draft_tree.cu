@@ -1,0 +1,476 @@
+// jf_draft_tree.cu -- best-first draft-tree construction from per-depth draft logits.
+//
+// JetFlow explainer ("JetFlow: Breaking the Scaling Ceiling of Speculative Decoding with
+// Parallel Tree Drafting"), technical summary §2 "Method", tree construction: at inference
+// the draft head emits logits for every tree depth in one pass; nodes are ranked by a
+// branch score, by default the cumulative draft log-probability, and a best-first
+// expansion builds the candidate tree up to a token budget.
+//
+// Kernel 1, one CTA per (sequence, depth d): the K candidates of depth d are the K
+// largest logits (lower token id on ties) with their log-probabilities
+// logit - logsumexp(row), fp32.
+// Kernel 2, one CTA per sequence: every node at depth d < Dmax has the K depth-(d+1)
+// candidates as children, child score = fp32(parent score + candidate log-prob), root
+// score 0.  Best-first expansion to N nodes pops nodes in the order of the key
+// (score descending, depth ascending, rank path ascending), so the tree is the first N
+// nodes of the candidate lattice in that order (a parent always precedes its children:
+// its score is not lower and its depth is smaller).  The kernel finds them level by
+// level: the level-d candidates are the children of the chosen level-(d-1) nodes (once
+// N nodes are chosen, only those that beat the last of them), and the chosen set is the
+// best N of (chosen so far + candidates), kept sorted with a bitonic sort in shared
+// memory.  A node is identified by its rank path packed into a
+// 64-bit code (4 bits per level, first level in the top bits), so its parent's code is
+// its own with the last digit cleared.
+#include <cmath>
+
+#include "jf_common.cuh"
+#include "jf_sm100.cuh"
+
+namespace jf {
+namespace {
+
+constexpr int kTopThreads = 512;
+constexpr int kTreeThreads = 1024;
+constexpr int kMaxK = 8;
+constexpr int kMaxDepth = 16;
+constexpr int kMaxTreeN = 256;
+constexpr int kSortCap = 4096;            // >= N + N * K, a power of two
+constexpr int kRowParts = 8;             // CTAs (one cluster) per logit row
+
+// ---------------------------------------------------------------- kernel 1: candidates
+struct Cand {
+  float v;
+  int i;
+};
+// a precedes b: larger value, then lower index
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  return a.v > b.v || (a.v == b.v && a.i < b.i);
+}
+
+template <typename T>
+__device__ __forceinline__ float load_logit(const T* p, long long i);
+template <>
+__device__ __forceinline__ float load_logit<float>(const float* p, long long i) { return p[i]; }
+template <>
+__device__ __forceinline__ float load_logit<uint16_t>(const uint16_t* p, long long i) {
+  return __uint_as_float(static_cast<uint32_t>(p[i]) << 16);
+}
+
+// A warp keeps one sorted list of its kMaxK best logits, entry r in lane r (lanes >= kMaxK
+// unused); thr is the list's last.  Every lane offers one logit per call; lanes whose
+// logit beats thr are taken one at a time (lowest lane first): its rank p in the list is
+// the number of entries that beat it, entries p.. move down one lane, and it lands in
+// lane p.  After the first few hundred logits almost no lane qualifies, so the common
+// case is one vote.
+__device__ __forceinline__ void warp_offer(float v, int i, bool valid, Cand& wl, Cand& thr) {
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  unsigned mask = __ballot_sync(kAll, valid && (v > thr.v || (v == thr.v && i < thr.i)));
+  while (mask != 0u) {
+    const int L = __ffs(mask) - 1;
+    const float cv = __shfl_sync(kAll, v, L);
+    const int ci = __shfl_sync(kAll, i, L);
+    const bool ahead = lane < kMaxK && (wl.v > cv || (wl.v == cv && wl.i < ci));
+    const int p = __popc(__ballot_sync(kAll, ahead));
+    const float uv = __shfl_up_sync(kAll, wl.v, 1);
+    const int ui = __shfl_up_sync(kAll, wl.i, 1);
+    if (lane < kMaxK && lane > p) { wl.v = uv; wl.i = ui; }
+    if (lane == p) { wl.v = cv; wl.i = ci; }
+    thr.v = __shfl_sync(kAll, wl.v, kMaxK - 1);
+    thr.i = __shfl_sync(kAll, wl.i, kMaxK - 1);
+    mask &= ~(1u << L);
+    mask &= __ballot_sync(kAll, valid && (v > thr.v || (v == thr.v && i < thr.i)));
+  }
+}
+
+// One pass over this CTA's slice of a row, warp-synchronously (every lane runs every
+// step; lanes past the slice offer nothing).  PASS 1 folds the maximum into m; PASS 2
+// adds exp(x - M) into sum and offers every logit to the warp's list.  The row is read as
+// 16-byte vectors, kUnroll per thread in flight, when it starts on a 16-byte boundary;
+// otherwise element by element.
+template <int PASS>
+__device__ __forceinline__ void take(float v, int i, bool valid, float M, float& m, float& sum,
+                                     Cand& wl, Cand& thr) {
+  if constexpr (PASS == 1) {
+    if (valid) m = fmaxf(m, v);
+  } else {
+    if (valid) sum += __expf(v - M);
+    warp_offer(v, i, valid, wl, thr);
+  }
+}
+
+template <typename T, int PASS>
+__device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts, float M, float& m,
+                                         float& sum, Cand& wl, Cand& thr) {
+  constexpr int kPer = 16 / sizeof(T);          // logits per vector
+  constexpr int kUnroll = 8;
+  const int lane0 = static_cast<int>(threadIdx.x) & ~31;   // first thread of this warp
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0u) {
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    const int nvec_all = V / kPer;
+    const int per = (nvec_all + parts - 1) / parts;
+    const int vb = min(nvec_all, part * per);
+    const int nvec = min(nvec_all, vb + per);
+    // the warp loops while its first lane still has vectors, so all lanes step together
+    for (int w0 = vb + lane0; w0 < nvec; w0 += blockDim.x * kUnroll) {
+      const int v0 = w0 + (threadIdx.x & 31);
+      uint4 buf[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + u * blockDim.x;
+        buf[u] = v < nvec ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + u * blockDim.x;
+        const bool valid = v < nvec;
+        const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+          float val;
+          if constexpr (sizeof(T) == 2)
+            val = __uint_as_float(((w[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu) << 16);
+          else
+            val = __uint_as_float(w[e]);
+          take<PASS>(val, v * kPer + e, valid, M, m, sum, wl, thr);
+        }
+      }
+    }
+    if (part == parts - 1)
+      for (int b0 = nvec_all * kPer + lane0; b0 < V; b0 += blockDim.x) {
+        const int i = b0 + (threadIdx.x & 31);
+        const bool valid = i < V;
+        take<PASS>(valid ? load_logit<T>(x, i) : -INFINITY, i, valid, M, m, sum, wl, thr);
+      }
+  } else {
+    const int per = (V + parts - 1) / parts;
+    const int ib = min(V, part * per), ie = min(V, ib + per);
+    for (int b0 = ib + lane0; b0 < ie; b0 += blockDim.x) {
+      const int i = b0 + (threadIdx.x & 31);
+      const bool valid = i < ie;
+      take<PASS>(valid ? load_logit<T>(x, i) : -INFINITY, i, valid, M, m, sum, wl, thr);
+    }
+  }
+}
+
+// A cluster of kRowParts CTAs shares one row; each makes two passes over its slice: the
+// slice maximum m_c, then s_c = sum of exp(x - m_c) together with the slice's K best
+// (per warp, then merged across the CTA's warps).  The cluster's first CTA merges the
+// slices through distributed shared memory: M = max m_c, S = sum s_c * exp(m_c - M),
+// lse = M + log S, and the K best of the slices' lists.
+template <typename T>
+__global__ void __launch_bounds__(kTopThreads)
+    draft_candidates_kernel(const T* __restrict__ logits, int V, int K,
+                            int32_t* __restrict__ cand_token, float* __restrict__ cand_logp) {
+  constexpr int kWarps = kTopThreads / 32;
+  __shared__ Cand s_top[kWarps][kMaxK];
+  __shared__ float s_red[kTopThreads];
+  __shared__ float s_slice[2];                   // this slice's (max, sum)
+  grid_dependency_wait();
+  const long long row = blockIdx.x / kRowParts;
+  const int part = static_cast<int>(cluster_ctarank());
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const T* x = logits + row * V;
+  Cand wl{-INFINITY, 0x7fffffff}, thr{-INFINITY, 0x7fffffff};
+  float m = -INFINITY, sum = 0.f;
+  row_pass<T, 1>(x, V, part, kRowParts, 0.f, m, sum, wl, thr);       // slice maximum
+  s_red[threadIdx.x] = m;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_red[threadIdx.x] = fmaxf(s_red[threadIdx.x], s_red[threadIdx.x + w]);
+    __syncthreads();
+  }
+  const float M = s_red[0];
+  __syncthreads();
+  if (M != -INFINITY) row_pass<T, 2>(x, V, part, kRowParts, M, m, sum, wl, thr);
+  if (lane < kMaxK) s_top[warp][lane] = wl;
+  s_red[threadIdx.x] = sum;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
+    __syncthreads();
+  }
+  // merge the warps' lists: warp 0 takes the K best heads, one per round
+  if (warp == 0) {
+    int head = 0;                                  // lane q < kWarps walks list q
+    Cand out = Cand{-INFINITY, 0x7fffffff};
+    for (int r = 0; r < kMaxK; ++r) {
+      const Cand h = (lane < kWarps && head < kMaxK) ? s_top[lane][head] : Cand{-INFINITY, 0x7fffffff};
+      float bv = h.v;
+      int bi = h.i;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (lane < kWarps && head < kMaxK && h.v == bv && h.i == bi) ++head;
+      if (lane == r) out = Cand{bv, bi};
+    }
+    __syncwarp();
+    if (lane < kMaxK) s_top[0][lane] = out;        // this slice's K best, in order
+    if (lane == 0) {
+      s_slice[0] = M;
+      s_slice[1] = s_red[0];
+    }
+  }
+  cluster_sync();                                // every slice's result is in place
+  if (part == 0 && warp == 0) {
+    // lane q < kRowParts fetches slice q's (max, sum) and K-best list
+    float mq = -INFINITY, sq = 0.f;
+    Cand lst[kMaxK];
+    if (lane < kRowParts) {
+      mq = dsmem_ld_f32(dsmem_addr(&s_slice[0], lane));
+      sq = dsmem_ld_f32(dsmem_addr(&s_slice[1], lane));
+#pragma unroll
+      for (int r = 0; r < kMaxK; ++r) {
+        const float2 c = dsmem_ld_f32x2(dsmem_addr(&s_top[0][r], lane));
+        lst[r] = Cand{c.x, __float_as_int(c.y)};
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < kMaxK; ++r) lst[r] = Cand{-INFINITY, 0x7fffffff};
+    }
+    float Mx = mq;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+    float S = mq == -INFINITY ? 0.f : sq * __expf(mq - Mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    int head = 0;
+    for (int r = 0; r < K; ++r) {
+      Cand h = Cand{-INFINITY, 0x7fffffff};
+#pragma unroll
+      for (int q = 0; q < kMaxK; ++q)
+        if (q == head) h = lst[q];
+      float bv = h.v;
+      int bi = h.i;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (head < kMaxK && h.v == bv && h.i == bi) ++head;   // indices are unique
+      if (lane == 0) {
+        cand_token[row * K + r] = bi;
+        cand_logp[row * K + r] = bv - (Mx + __logf(S));
+      }
+    }
+  }
+  cluster_sync();                                // no CTA leaves while the first reads it
+  grid_dependents_launch();
+}
+
+// ---------------------------------------------------------------- kernel 2: best-first
+// Sort key: hi = (descending-score bits << 32) | depth, lo = rank-path code; ascending.
+__device__ __forceinline__ uint32_t desc_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  const uint32_t asc = (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // order-preserving
+  return ~asc;
+}
+__device__ __forceinline__ float from_desc_bits(uint32_t d) {
+  const uint32_t asc = ~d;
+  const uint32_t u = (asc & 0x80000000u) ? (asc & 0x7fffffffu) : ~asc;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ bool key_less(uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl) {
+  return ah < bh || (ah == bh && al < bl);
+}
+
+__device__ void bitonic_sort(uint64_t* hi, uint64_t* lo, int n) {   // n a power of two
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const bool up = (i & k) == 0;
+          const bool sw = up ? key_less(hi[l], lo[l], hi[i], lo[i]) : key_less(hi[i], lo[i], hi[l], lo[l]);
+          if (sw) {
+            const uint64_t th = hi[i], tl = lo[i];
+            hi[i] = hi[l]; lo[i] = lo[l];
+            hi[l] = th; lo[l] = tl;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTreeThreads)
+    best_first_tree_kernel(const int32_t* __restrict__ cand_token, const float* __restrict__ cand_logp,
+                           const int32_t* __restrict__ root_token, int Dmax, int K, int N,
+                           int32_t* __restrict__ parent, int32_t* __restrict__ draft,
+                           int32_t* __restrict__ depth_out, float* __restrict__ score_out) {
+  extern __shared__ uint64_t s_keys[];     // [kSortCap] hi, then [kSortCap] lo
+  uint64_t* s_hi = s_keys;
+  uint64_t* s_lo = s_keys + kSortCap;
+  __shared__ float s_lp[kMaxDepth * kMaxK];
+  __shared__ int s_tok[kMaxDepth * kMaxK];
+  __shared__ int s_cnt[kMaxTreeN];
+  __shared__ int s_scan[2][kMaxTreeN];
+  __shared__ int s_nG;
+  grid_dependency_wait();
+  const int b = blockIdx.x;
+  for (int e = threadIdx.x; e < Dmax * K; e += blockDim.x) {
+    s_lp[e] = cand_logp[static_cast<size_t>(b) * Dmax * K + e];
+    s_tok[e] = cand_token[static_cast<size_t>(b) * Dmax * K + e];
+  }
+  // the chosen set G lives in slots [0, nG), sorted; start with the root
+  if (threadIdx.x == 0) {
+    s_hi[0] = static_cast<uint64_t>(desc_bits(0.f)) << 32;
+    s_lo[0] = 0ull;
+    s_nG = 1;
+  }
+  __syncthreads();
+  for (int d = 1; d <= Dmax; ++d) {
+    const int nG = s_nG;
+    const int shift = 4 * (kMaxDepth - d);
+    // Level-d candidates: children of the chosen level-(d-1) nodes.  Once G holds N nodes
+    // a child only matters if it beats G's last; a parent's children fall in score with
+    // their rank, so those form a prefix of its K children.
+    const bool full = nG == N;
+    const uint64_t thr_hi = full ? s_hi[N - 1] : ~0ull, thr_lo = full ? s_lo[N - 1] : ~0ull;
+    for (int f = threadIdx.x; f < kMaxTreeN; f += blockDim.x) {
+      int cnt = 0;
+      if (f < nG && (s_hi[f] & 0xFFFFFFFFull) == static_cast<uint64_t>(d - 1)) {
+        const float ps = from_desc_bits(static_cast<uint32_t>(s_hi[f] >> 32));
+        for (int r = 0; r < K; ++r) {
+          const float cs = __fadd_rn(ps, s_lp[(d - 1) * K + r]);
+          const uint64_t ch = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
+          const uint64_t cl = s_lo[f] | (static_cast<uint64_t>(r) << shift);
+          if (!key_less(ch, cl, thr_hi, thr_lo)) break;
+          ++cnt;
+        }
+      }
+      s_cnt[f] = cnt;
+      s_scan[0][f] = cnt;
+    }
+    __syncthreads();
+    int src = 0;                                     // inclusive scan of the counts
+    for (int off = 1; off < kMaxTreeN; off <<= 1) {
+      for (int f = threadIdx.x; f < kMaxTreeN; f += blockDim.x)
+        s_scan[1 - src][f] = s_scan[src][f] + (f >= off ? s_scan[src][f - off] : 0);
+      src = 1 - src;
+      __syncthreads();
+    }
+    const int nC = s_scan[src][kMaxTreeN - 1];
+    if (nC == 0) break;
+    for (int f = threadIdx.x; f < nG; f += blockDim.x) {
+      const int cnt = s_cnt[f];
+      if (cnt == 0) continue;
+      const int base = nG + s_scan[src][f] - cnt;
+      const float ps = from_desc_bits(static_cast<uint32_t>(s_hi[f] >> 32));
+      const uint64_t pc = s_lo[f];
+      for (int r = 0; r < cnt; ++r) {
+        const float cs = __fadd_rn(ps, s_lp[(d - 1) * K + r]);
+        s_hi[base + r] = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
+        s_lo[base + r] = pc | (static_cast<uint64_t>(r) << shift);
+      }
+    }
+    int n = 1;
+    while (n < nG + nC) n <<= 1;
+    for (int e = nG + nC + threadIdx.x; e < n; e += blockDim.x) {
+      s_hi[e] = ~0ull;
+      s_lo[e] = ~0ull;
+    }
+    __syncthreads();
+    bitonic_sort(s_hi, s_lo, n);
+    // keep the best N; stop once no level-d node made it (deeper ones cannot either)
+    int kept_d = 0;
+    for (int e = threadIdx.x; e < min(N, nG + nC); e += blockDim.x)
+      kept_d |= static_cast<int>((s_hi[e] & 0xFFFFFFFFull) == static_cast<uint64_t>(d));
+    kept_d = __syncthreads_or(kept_d);
+    if (threadIdx.x == 0) s_nG = min(N, nG + nC);
+    __syncthreads();
+    if (!kept_d) break;
+  }
+  // G in key order is the tree in pop order: node id = slot
+  const int nG = s_nG;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    const size_t o = static_cast<size_t>(b) * N + i;
+    if (i >= nG) {                          // lattice smaller than N (rejected on the host)
+      parent[o] = -1; draft[o] = -1; depth_out[o] = -1;
+      if (score_out != nullptr) score_out[o] = -INFINITY;
+      continue;
+    }
+    const int d = static_cast<int>(s_hi[i] & 0xFFFFFFFFull);
+    const uint64_t code = s_lo[i];
+    int par = -1, tok = root_token != nullptr ? root_token[b] : -1;
+    if (d > 0) {
+      const int shift = 4 * (kMaxDepth - d);
+      const int r = static_cast<int>((code >> shift) & 0xFull);
+      tok = s_tok[(d - 1) * K + r];
+      const uint64_t pcode = code & ~(0xFull << shift);
+      for (int u = 0; u < i; ++u)
+        if (s_lo[u] == pcode && static_cast<int>(s_hi[u] & 0xFFFFFFFFull) == d - 1) { par = u; break; }
+    }
+    parent[o] = par;
+    draft[o] = tok;
+    depth_out[o] = d;
+    if (score_out != nullptr) score_out[o] = from_desc_bits(static_cast<uint32_t>(s_hi[i] >> 32));
+  }
+  grid_dependents_launch();
+}
+
+}  // namespace
+}  // namespace jf
+
+extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype,
+                                         const int32_t* root_token, int32_t B, int32_t Dmax,
+                                         int32_t V, int32_t K, int32_t N, int32_t* cand_token,
+                                         float* cand_logp, int32_t* parent, int32_t* draft,
+                                         int32_t* depth, float* score, jf_stream_t stream) {
+  if (draft_logits == nullptr || cand_token == nullptr || cand_logp == nullptr || parent == nullptr ||
+      draft == nullptr || depth == nullptr)
+    return JF_ERR_INVALID_ARGUMENT;
+  if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
+  if (B < 1 || Dmax < 1 || K < 1 || N < 1 || V < 1) return JF_ERR_INVALID_ARGUMENT;
+  if (K > jf::kMaxK || Dmax > jf::kMaxDepth || N > jf::kMaxTreeN || V < K) return JF_ERR_UNSUPPORTED;
+  if (N + N * K > jf::kSortCap) return JF_ERR_UNSUPPORTED;
+  // the lattice must hold N nodes: 1 + K + K^2 + ... + K^Dmax >= N
+  long long lattice = 1, level = 1;
+  for (int d = 1; d <= Dmax && lattice < N; ++d) {
+    level *= K;
+    lattice += level;
+  }
+  if (lattice < N) return JF_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Dmax > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (static_cast<long long>(B) * Dmax * jf::kRowParts > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(B * Dmax * jf::kRowParts));
+  lc.blockDim = dim3(jf::kTopThreads);
+  lc.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = jf::kRowParts;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  cudaError_t e =
+      dtype == JF_DTYPE_BF16
+          ? cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<uint16_t>,
+                               static_cast<const uint16_t*>(draft_logits), V, K, cand_token, cand_logp)
+          : cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<float>,
+                               static_cast<const float*>(draft_logits), V, K, cand_token, cand_logp);
+  if (e != cudaSuccess) return JF_ERR_CUDA;
+  constexpr size_t kTreeSmem = 2 * jf::kSortCap * sizeof(uint64_t);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+  if (dev >= 64 || !attr_set[dev]) {
+    if (cudaFuncSetAttribute(jf::best_first_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kTreeSmem)) != cudaSuccess)
+      return JF_ERR_CUDA;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  e = jf::launch_pdl(jf::best_first_tree_kernel, dim3(static_cast<unsigned>(B)), dim3(jf::kTreeThreads), kTreeSmem, s,
+                     static_cast<const int32_t*>(cand_token), static_cast<const float*>(cand_logp),
+                     root_token, Dmax, K, N, parent, draft, depth, score);
+  return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+}

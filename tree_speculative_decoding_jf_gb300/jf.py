@@ -60,6 +60,8 @@ def _load():
     lib.jf_compact_accepted_kv.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                            P, P, P]
     lib.jf_compact_accepted_kv.restype = ctypes.c_int
+    lib.jf_build_draft_tree.argtypes = [P, i32, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+    lib.jf_build_draft_tree.restype = ctypes.c_int
     return lib
 
 
@@ -236,6 +238,30 @@ def jf_compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, acce
         _ptr(new_prefix_len), _ptr(dev_err), _stream(stream)))
 
 
+def jf_build_draft_tree(draft_logits, K, N, cand_token, cand_logp, parent, draft, depth,
+                        root_token=None, score=None, stream=None) -> None:
+    """Best-first draft tree from per-depth draft logits (see include/jf.h)."""
+    B, Dmax, V = draft_logits.shape
+    if draft_logits.dtype == torch.bfloat16:
+        dt = JF_DTYPE_BF16
+    elif draft_logits.dtype == torch.float32:
+        dt = JF_DTYPE_F32
+    else:
+        raise TypeError("draft_logits must be bfloat16 or float32")
+    _need(draft_logits, "draft_logits", draft_logits.dtype)
+    _need(cand_token, "cand_token", torch.int32, (B, Dmax, K))
+    _need(cand_logp, "cand_logp", torch.float32, (B, Dmax, K))
+    for name, t in (("parent", parent), ("draft", draft), ("depth", depth)):
+        _need(t, name, torch.int32, (B, N))
+    if score is not None:
+        _need(score, "score", torch.float32, (B, N))
+    if root_token is not None:
+        _need(root_token, "root_token", torch.int32, (B,))
+    _check("jf_build_draft_tree", _lib.jf_build_draft_tree(
+        _ptr(draft_logits), dt, _ptr(root_token), B, Dmax, V, K, N, _ptr(cand_token),
+        _ptr(cand_logp), _ptr(parent), _ptr(draft), _ptr(depth), _ptr(score), _stream(stream)))
+
+
 # ----------------------------------------------------------------------------- conveniences
 
 def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
@@ -288,4 +314,19 @@ def compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_
     jf_compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,
                            new_prefix_len, dev_err, stream)
     return new_prefix_len
+
+
+def build_draft_tree(draft_logits, K, N, root_token=None, stream=None):
+    """Returns (parent, draft, depth, score, cand_token, cand_logp)."""
+    B, Dmax, V = draft_logits.shape
+    dev = draft_logits.device
+    cand_token = torch.empty((B, Dmax, K), dtype=torch.int32, device=dev)
+    cand_logp = torch.empty((B, Dmax, K), dtype=torch.float32, device=dev)
+    parent = torch.empty((B, N), dtype=torch.int32, device=dev)
+    draft = torch.empty((B, N), dtype=torch.int32, device=dev)
+    depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    score = torch.empty((B, N), dtype=torch.float32, device=dev)
+    jf_build_draft_tree(draft_logits, K, N, cand_token, cand_logp, parent, draft, depth,
+                        root_token, score, stream)
+    return parent, draft, depth, score, cand_token, cand_logp
 

@@ -340,3 +340,11 @@ def random_accepted_paths(parent: np.ndarray, seed: int = 0):
         acc[b] = len(chain) - 1
     return path, acc
 
+def draft_logits(B: int, Dmax: int, V: int, sigma: float = 3.0, dtype: str = "bf16",
+                 seed: int = 0) -> np.ndarray:
+    """Seeded synthetic per-depth draft logits ~ N(0, sigma) (sigma a standard deviation),
+    [B][Dmax][V]: bf16 bit patterns (uint16, round to nearest even) or float32."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0xD7AF]))
+    x = (rng.standard_normal((B, Dmax, V), dtype=np.float32) * np.float32(sigma)).astype(np.float32)
+    return to_bf16_bits(x) if dtype == "bf16" else x
+
