@@ -295,6 +295,9 @@ SHAPES = [  # B, N, Hq, Hkv, D, P, tree
     (1, 4, 8, 1, 128, 1500, "random"),       # one unit, 12 key tiles: 9..16 splits
     (1, 8, 8, 1, 128, 900, "random"),        # 5..8 splits
     (2, 8, 8, 2, 64, 800, "random"),         # 5..8 splits, D = 64
+    (20, 128, 32, 4, 64, 300, "random"),     # 4 row-tile groups, 320 units: stream-K, D = 64
+    (24, 64, 32, 4, 128, 90, "random"),      # 2 row-tile groups, 192 units: stream-K, D = 128
+    (20, 40, 32, 4, 128, 3, "random"),       # stream-K over 1..6-tile pairs: many per range
 ]
 
 

@@ -927,6 +927,671 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   grid_dependents_launch();
 }
 
+// ============================================================ stream-K variant
+// With more (sequence, kv-head, row-tile group) units than SMs, one unit (or split) per
+// CTA leaves the last wave partly idle and makes every CTA pay its own prologue and
+// epilogue.  The stream-K variant runs one CTA per SM instead.  The key tiles of all
+// (sequence, kv-head) pairs are laid end to end (sequence-major; pair (b, g) has
+// tiles(b) = ceil((P_b + N) / 128)) and cut into nvirt equal ranges; the n_groups CTAs of
+// range v (one per row-tile group) walk the same range, so the row-tile groups of a
+// kv-head keep reading each K/V tile at about the same time.  A range is a run of
+// segments, each a key-tile range of one pair: a whole pair is written straight to `out`;
+// a range's first and last segments may be pieces of a pair, which go to the range's
+// partial slots 0 and 1 and are merged by tree_attention_sk_combine_kernel.
+//
+// The roles are those of tree_attention_kernel with every counter running over the
+// range's tiles as one sequence jg = 0 .. Wc-1, and the MMA issuer runs exactly that
+// kernel's loop: it knows nothing of segments.  Step jg issues PV of tile jg and S of
+// tile jg + 1 even when that tile opens the next segment, so the segment logic sits in the
+// other roles: the producer reloads Q once step record e - 1 (S of the segment's last tile
+// e - 1 done) completes; the voucher of the last tile waits for that Q and for the tail;
+// the softmax warpgroups learn that the segment's last PV is done from the S barrier of
+// tile e (committed after it), write the segment's rows, and zero O in tensor memory
+// before they release the next segment's first tile, whose PV then accumulates onto zero.
+struct SkSched {
+  const int* pre;      // pre[b] = tiles of sequences < b (shared memory), pre[B] = S
+  int B;
+  int S;               // tiles of one kv head over all sequences
+  int q, rem;          // W = Hkv * S tiles cut into nvirt ranges: rem of q + 1 tiles, then q
+  __device__ SkSched(const int* pre_, int B_, int Hkv, int nvirt) : pre(pre_), B(B_), S(pre_[B_]) {
+    const int W = Hkv * S;
+    q = W / nvirt;
+    rem = W - q * nvirt;
+  }
+  __device__ int tiles(int b) const { return pre[b + 1] - pre[b]; }
+  __device__ int start(int b, int g) const { return g * S + pre[b]; }
+  __device__ int range_lo(int v) const { return v * q + min(v, rem); }
+  // the range containing x
+  __device__ int range_of(int x) const {
+    const int big = rem * (q + 1);
+    return x < big ? x / (q + 1) : rem + (x - big) / q;
+  }
+};
+
+// pre[0] = 0, pre[b + 1] = key tiles of sequences 0..b (prefix lengths clamped to the
+// pool, the clamp reported through `err` when given).  Every thread of the block calls it;
+// B <= kLptMaxB <= blockDim.x.  Each warp scans 32 sequences with shuffles, then adds the
+// totals of the warps before it.
+__device__ __noinline__ void sk_tile_prefix(int* pre, const int32_t* prefix_len, int B, int N, int cap,
+                                            int* err) {
+  const int u = threadIdx.x, lane = u & 31;
+  int x = 0;
+  if (u < B) {
+    int P = prefix_len[u];
+    if (P < 0 || P > cap - N) {
+      if (err != nullptr) report(err, JF_DEVERR_BAD_PREFIX);
+      P = max(0, min(P, cap - N));
+    }
+    x = (P + N + kKeyTile - 1) / kKeyTile;
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (u < B) pre[u + 1] = x;
+  if (u == 0) pre[0] = 0;
+  __syncthreads();
+  int add = 0;
+  if (u < B)
+    for (int w = 0; w < (u >> 5); ++w) add += pre[min(32 * w + 32, B)];
+  __syncthreads();
+  if (u < B) pre[u + 1] = x + add;
+  __syncthreads();
+}
+
+struct SkSeg {
+  int b, g, k0, k1, slot;   // slot -1: whole pair; 0 / 1: the range's first / last partial
+  int x1;                   // end of the segment in the global order
+};
+
+// The segment of range [lo, hi) that starts at global position x (32-bit positions keep
+// the roles' register budgets free of 64-bit division).
+__device__ __forceinline__ SkSeg sk_segment(const SkSched& s, int x, int lo, int hi) {
+  SkSeg r;
+  r.g = x / s.S;
+  const int off = x - r.g * s.S;
+  int a = 0, c = s.B;
+  while (c - a > 1) {
+    const int mid = (a + c) >> 1;
+    if (s.pre[mid] <= off) a = mid; else c = mid;
+  }
+  r.b = a;
+  r.k0 = off - s.pre[a];
+  r.x1 = min(hi, s.start(r.b, r.g) + s.tiles(r.b));
+  r.k1 = r.k0 + (r.x1 - x);
+  r.slot = (r.k0 == 0 && r.k1 == s.tiles(r.b)) ? -1 : (x == lo ? 0 : 1);
+  return r;
+}
+// The producer may finish several short segments before a voucher looks at the first, so
+// "segment s's V tail is ready" is a count (release on the producer side, acquire here)
+// rather than a phase of a reused barrier.
+__device__ __forceinline__ void count_release_add(int* c) {
+  asm volatile("red.release.cta.shared::cta.add.s32 [%0], 1;" ::"r"(smem_u32(c)) : "memory");
+}
+__device__ __forceinline__ int count_acquire(int* c) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(c)) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool wait_count_above(int* c, int target, volatile int* abort) {
+  if (count_acquire(c) > target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (count_acquire(c) > target) return true;
+    if ((it & 255u) == 0u && (*abort || global_timer_ns() - t0 > kWaitLimitNs)) return false;
+  }
+}
+
+template <int NT, int D>
+__global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
+    tree_attention_sk_kernel(const __grid_constant__ CUtensorMap qmap,
+                             const __grid_constant__ CUtensorMap kmap,
+                             const __grid_constant__ CUtensorMap vmap,
+                             const __grid_constant__ CUtensorMap kmap_run,
+                             const __grid_constant__ CUtensorMap vmap_run, const AttnParams p,
+                             int nvirt) {
+  using C = Cfg<NT, D>;
+  constexpr int SK = C::kKStages;
+  constexpr int SV = C::kVStages;
+  constexpr int R = NT * kRowTile;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t q_full, o_full, fin;
+  __shared__ uint64_t k_full[SK], v_full[SV], step_done[kStepRing];
+  __shared__ uint64_t s_full[NT], p_full[NT];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int s_tails;                    // segments whose V tail is ready
+  __shared__ int s_pre[kLptMaxB + 1];
+  volatile int* abort = &abort_flag;
+  uint8_t* q_s = sm + C::kQOff;
+  uint8_t* k_s = sm + C::kKOff;
+  uint8_t* v_s = sm + C::kVOff;
+  const int v = blockIdx.x / p.n_groups;
+  const int mp = blockIdx.x % p.n_groups;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    mbar_init(&o_full, 1);
+    mbar_init(&fin, 1);
+    for (int st = 0; st < SK; ++st) mbar_init(&k_full[st], 1);
+    for (int st = 0; st < SV; ++st) mbar_init(&v_full[st], 1);
+    for (int st = 0; st < kStepRing; ++st) mbar_init(&step_done[st], 1);
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128 + 1);   // the softmax warpgroup + its data voucher
+    }
+    s_tails = 0;
+    abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&qmap);
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&kmap_run);
+    tma_prefetch_desc(&vmap_run);
+  }
+  grid_dependency_wait();
+
+  // ---- the schedule: tiles per sequence, their running sums, this range's segments
+  const int cap = p.max_pages * kPage;
+  sk_tile_prefix(s_pre, p.prefix_len, p.B, p.N, cap, blockIdx.x == 0 ? p.dev_err : nullptr);
+  const SkSched sch(s_pre, p.B, p.Hkv, nvirt);
+  const int lo = sch.range_lo(v), hi = sch.range_lo(v + 1);
+  const int Wc = hi - lo;
+  if (Wc <= 0) return;
+  // end (exclusive, in range tiles) of the segment that starts at range tile j
+  auto seg_end = [&](int j) -> int { return sk_segment(sch, lo + j, lo, hi).x1 - lo; };
+  auto prefix_of = [&](int b) -> int { return max(0, min(p.prefix_len[b], cap - p.N)); };
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp < 4) {
+  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 96;");
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    constexpr int kLookahead = 4;
+    int k_issued = 0, v_issued = 0, q_issued = 0, bad = 0;
+    bool ok = true;
+    auto issue = [&](uint8_t* ring, const CUtensorMap* map, const CUtensorMap* map_run,
+                     uint64_t* full, int st, int page, int page0, int g, bool run) {
+      if (run) {
+        if (lane < C::kHalves)
+          tma_load_3d(ring + st * C::kTileBytes + lane * C::kHalfBytes, map_run, full, lane * 64, g,
+                      page0 * kPage);
+      } else if (lane < kPagesPerTile * C::kHalves) {
+        const int q = lane % kPagesPerTile, hh = lane / kPagesPerTile;
+        tma_load_3d(ring + st * C::kTileBytes + hh * C::kHalfBytes + q * (kPage * 128), map, full,
+                    hh * 64, g, page * kPage);
+      }
+    };
+    int jg0 = 0;
+    for (int s = 0; jg0 < Wc && ok; ++s) {
+      const SkSeg sg = sk_segment(sch, lo + jg0, lo, hi);
+      const int T = sg.k1 - sg.k0;
+      const int L = prefix_of(sg.b) + p.N;
+      const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_pages;
+      // this segment's Q, once the previous segment's S MMAs no longer read the buffer
+      int okq = 1;
+      if (lane == 0) {
+        const int rq = jg0 - 1;   // S of the previous segment's last tile: step record rq
+        if (s > 0 && !mbar_wait(&step_done[rq % kStepRing], static_cast<uint32_t>(rq / kStepRing) & 1u,
+                                abort)) {
+          okq = 0;
+        } else {
+          mbar_arrive_expect_tx(&q_full, NT * C::kTileBytes);
+          for (int t = 0; t < NT; ++t) {
+            const int node0 = ((mp * NT + t) * kRowTile) / p.G;
+            for (int hh = 0; hh < C::kHalves; ++hh)
+              tma_load_4d(q_s + t * C::kTileBytes + hh * C::kHalfBytes, &qmap, &q_full, hh * 64,
+                          sg.g * p.G, node0, sg.b);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, okq, 0)) { ok = false; break; }
+      q_issued = s + 1;
+      auto load_pid = [&](int j) -> int {
+        const int pl = (sg.k0 + j) * kPagesPerTile + lane;
+        if (lane >= kPagesPerTile || j >= T || pl * kPage >= L) return p.num_pages;
+        return __ldg(bt + pl);
+      };
+      int pid[kLookahead];
+#pragma unroll
+      for (int u = 0; u < kLookahead; ++u) pid[u] = load_pid(u);
+      for (int j = 0; j < T; ++j) {
+        const int jg = jg0 + j;
+        int mine = pid[0];
+        if (mine < 0 || mine > p.num_pages) { bad = 1; mine = p.num_pages; }
+        else if (mine == p.num_pages && lane < kPagesPerTile &&
+                 ((sg.k0 + j) * kPagesPerTile + lane) * kPage < L) bad = 1;
+        const int page = __shfl_sync(0xffffffffu, mine, lane % kPagesPerTile);
+        const int page0 = __shfl_sync(0xffffffffu, mine, 0);
+        const bool run = __all_sync(0xffffffffu, page == page0 + lane % kPagesPerTile);
+#pragma unroll
+        for (int u = 0; u < kLookahead - 1; ++u) pid[u] = pid[u + 1];
+        pid[kLookahead - 1] = load_pid(j + kLookahead);
+        const int sk = jg % SK, sv = jg % SV;
+        const int rec = jg - C::kStageLag;
+        int okl = 1;
+        if (lane == 0) {
+          if (rec >= 0 && !mbar_wait(&step_done[rec % kStepRing],
+                                     static_cast<uint32_t>(rec / kStepRing) & 1u, abort)) {
+            okl = 0;
+          } else {
+            mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
+            mbar_arrive_expect_tx(&v_full[sv], C::kTileBytes);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, okl, 0)) { ok = false; break; }
+        issue(k_s, &kmap, &kmap_run, &k_full[sk], sk, page, page0, sg.g, run);
+        k_issued = jg + 1;
+        issue(v_s, &vmap, &vmap_run, &v_full[sv], sv, page, page0, sg.g, run);
+        v_issued = jg + 1;
+      }
+      if (!ok) break;
+      // V rows past the sequence end in the segment's last tile meet a zero probability:
+      // make them zero, then release the tile to the MMA issuer's voucher (every segment).
+      const int jl = jg0 + T - 1;
+      if ((sg.k1) * kKeyTile > L) {
+        if (!wait_warp(&v_full[jl % SV], static_cast<uint32_t>(jl / SV) & 1u, abort)) { ok = false; break; }
+        const int r0 = L - (sg.k1 - 1) * kKeyTile;
+        uint8_t* vt = v_s + (jl % SV) * C::kTileBytes;
+        const int per_half = (kKeyTile - r0) * 8;
+        for (int c = lane; c < per_half * C::kHalves; c += 32) {
+          const int hh = c / per_half, rem = c % per_half;
+          *reinterpret_cast<uint4*>(vt + hh * C::kHalfBytes + (r0 + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) count_release_add(&s_tails);
+      jg0 += T;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.dev_err, JF_DEVERR_BAD_PAGE);
+    if (!ok && lane == 0) set_abort(abort, p.dev_err);
+    __syncwarp();
+    if (lane == 0) {                   // no copy may still be landing when the CTA exits
+      int zero = 0;
+      if (q_issued > 0) mbar_wait(&q_full, static_cast<uint32_t>(q_issued - 1) & 1u, &zero);
+      for (int j = max(0, k_issued - SK); j < k_issued; ++j)
+        mbar_wait(&k_full[j % SK], static_cast<uint32_t>(j / SK) & 1u, &zero);
+      for (int j = max(0, v_issued - SV); j < v_issued; ++j)
+        mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, &zero);
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idS = idesc_bf16(kRowTile, kKeyTile, false, false);
+    constexpr uint32_t idO = idesc_bf16(kRowTile, D, false, true);
+    const uint64_t dq = desc_sw128(smem_u32(q_s), 16, 1024);
+    const uint64_t dk = desc_sw128(smem_u32(k_s), 16, 1024);
+    const uint64_t dv = desc_sw128(smem_u32(v_s), C::kHalfBytes, 1024);
+    auto issue_s = [&](int t, int st) {
+      const uint64_t da = dq + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
+      const uint64_t db = dk + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+      const uint32_t d_tmem = tmem + C::kTmemS + t * 128;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4);
+        mma_ss(d_tmem, da + off, db + off, idS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int t, int st, bool acc) {
+      const uint64_t db = dv + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+      const uint32_t d_tmem = tmem + C::kTmemO + t * 128;
+      const uint32_t a_tmem = tmem + C::kTmemS + t * 128;
+#pragma unroll
+      for (int kk = 0; kk < kKeyTile / 16; ++kk)
+        mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
+               (acc || kk > 0) ? 1u : 0u);
+    };
+    bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
+    if (ok && lane == 0) {
+      tc_fence_after();
+      for (int t = 0; t < NT; ++t) {
+        issue_s(t, 0);
+        mma_commit(&s_full[t]);
+      }
+      mma_commit(&step_done[0]);
+      // The polling loop of tree_attention_kernel over the range's Wc tiles.
+      int jn[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) jn[t] = 0;
+      int left = NT * Wc;
+      uint32_t idle = 0;
+      uint64_t idle_since = 0;
+      while (left > 0) {
+        bool progressed = false;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int j = jn[t];
+          if (j >= Wc) continue;
+          if (!mbar_try_wait(&p_full[t], static_cast<uint32_t>(j) & 1u)) continue;
+          bool last = true;
+#pragma unroll
+          for (int u = 0; u < NT; ++u)
+            if (u != t && jn[u] <= j) last = false;
+          tc_fence_after();
+          issue_pv(t, j % SV, j > 0);
+          if (j + 1 < Wc) {
+            issue_s(t, (j + 1) % SK);
+            mma_commit(&s_full[t]);
+          }
+          if (last) mma_commit(&step_done[(j + 1) % kStepRing]);
+          jn[t] = j + 1;
+          --left;
+          progressed = true;
+        }
+        if (progressed) {
+          idle = 0;
+        } else {
+          if (idle == 0) idle_since = global_timer_ns();
+          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+        }
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) set_abort(abort, p.dev_err);
+    if (lane == 0) {
+      if (ok) mma_commit(&o_full);   // the range's last PV
+      mma_commit(&fin);   // all MMAs done before TMEM is released
+      int zero = 0;
+      mbar_wait(&fin, 0, &zero);
+    }
+    __syncwarp();
+  } else if (warp >= 2 && warp < 2 + NT) {
+    // ================================================================ data vouchers
+    // As in tree_attention_kernel, plus: at a segment's last tile the V tail of that
+    // segment, and, when another segment follows, that segment's Q (its first S MMAs are
+    // issued in this tile's step).
+    const int t = warp - 2;
+    if (lane == 0) {
+      int s = 0, e = seg_end(0);
+      for (int j = 0; j < Wc; ++j) {
+        const bool last_of_seg = j + 1 == e;
+        const bool ready =
+            (j == 0 || mbar_wait(&p_full[t], static_cast<uint32_t>(j - 1) & 1u, abort)) &&
+            mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, abort) &&
+            (j + 1 >= Wc ||
+             mbar_wait(&k_full[(j + 1) % SK], static_cast<uint32_t>((j + 1) / SK) & 1u, abort)) &&
+            (!last_of_seg || wait_count_above(&s_tails, s, abort)) &&
+            (!last_of_seg || j + 1 >= Wc ||
+             mbar_wait(&q_full, static_cast<uint32_t>(s + 1) & 1u, abort));
+        if (!ready) {
+          set_abort(abort, p.dev_err);
+          break;
+        }
+        mbar_arrive(&p_full[t]);
+        if (last_of_seg) {
+          ++s;
+          if (j + 1 < Wc) e = seg_end(j + 1);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  } else {
+    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 200;");
+    // ================================================================ softmax / epilogue
+    const int t = (warp >> 2) - 1;
+    const int wq = warp & 3;
+    const int rl = wq * 32 + lane;                       // row within the tile = TMEM lane
+    const int r = (mp * NT + t) * kRowTile + rl;
+    const bool valid = r < p.M;
+    const int i = r / p.G;
+    const int W = p.W;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + C::kTmemS + t * 128 + lane_off;
+    const uint32_t tO = tmem + C::kTmemO + t * 128 + lane_off;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int jg0 = 0;
+    for (int s = 0; jg0 < Wc && ok; ++s) {
+      const SkSeg sgm = sk_segment(sch, lo + jg0, lo, hi);
+      const int T = sgm.k1 - sgm.k0;
+      const int b = sgm.b, g = sgm.g;
+      const int P = prefix_of(b), L = P + p.N;
+      const int h = g * p.G + (r % p.G);
+      const uint64_t* mrow = p.mask + (static_cast<size_t>(b) * p.N + (valid ? i : 0)) * W;
+      float m_run = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < T; ++j) {
+        const int jg = jg0 + j;
+        const int key0 = (sgm.k0 + j) * kKeyTile;
+        const bool masked_tile = key0 + kKeyTile > P;
+        uint64_t mw[3] = {0ull, 0ull, 0ull};
+        const int w_lo = max(key0 - P, 0) >> 6;
+        if (masked_tile && valid) {
+#pragma unroll
+          for (int u = 0; u < 3; ++u)
+            if (w_lo + u < W) mw[u] = __ldg(reinterpret_cast<const unsigned long long*>(mrow) + w_lo + u);
+        }
+        if (!wait_warp(&s_full[t], static_cast<uint32_t>(jg) & 1u, abort)) {
+          if (lane == 0) set_abort(abort, p.dev_err);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld128(tS, sr);
+        float* sv = reinterpret_cast<float*>(sr);
+        if (masked_tile) {
+          const int pre = min(max(P - key0, 0), kKeyTile);
+          const int end = min(max(L - key0, 0), kKeyTile);
+          uint32_t vis[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int c0 = 32 * w;
+            uint32_t m = window_bits32(mw, key0 + c0 - P - 64 * w_lo);
+            const int np = min(max(pre - c0, 0), 32);
+            const int ne = min(max(end - c0, 0), 32);
+            m |= np >= 32 ? 0xFFFFFFFFu : ((1u << np) - 1u);
+            m &= ne >= 32 ? 0xFFFFFFFFu : ((1u << ne) - 1u);
+            vis[w] = m;
+          }
+#pragma unroll
+          for (int c = 0; c < kKeyTile; ++c)
+            if (!((vis[c >> 5] >> (c & 31)) & 1u)) sv[c] = -INFINITY;
+        }
+        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+        for (int c = 4; c < kKeyTile; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
+        const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+        const float mt = mx * sl2;
+        const bool raise = mt > m_run + kRescaleThreshold;
+        const float m_old = m_run;
+        if (raise) m_run = mt;
+        const float corr = raise ? fast_exp2(m_old - m_run) : 1.f;
+        const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
+        uint32_t pk[64];
+        const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
+        uint64_t ls2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float x0, x1;
+          f2_split(ffma2(f2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2), x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          ls2[c & 1] = fadd2(ls2[c & 1], f2(p0, p1));
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        float la, lb, lc, ld;
+        f2_split(ls2[0], la, lb);
+        f2_split(ls2[1], lc, ld);
+        const float ls = (la + lb) + (lc + ld);
+        l = l * corr + ls;
+        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        // O holds PV of this segment's tiles < j (complete: s_full of tile jg followed them)
+        const bool need = raise && j > 0 && m_old != -INFINITY;
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? corr : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+      }
+      // ---- the segment's rows: O / l, straight from TMEM to global memory, once its last
+      // PV is done: S of the next tile (committed after it) or, for the range's last
+      // segment, o_full.  Every warp of the warpgroup reaches this vote (all waits are
+      // bounded), so it is all-or-none.
+      const int je = jg0 + T;
+      const bool pv_done = ok && (je < Wc ? wait_warp(&s_full[t], static_cast<uint32_t>(je) & 1u, abort)
+                                          : wait_warp(&o_full, 0u, abort));
+      if (!named_bar_and(1 + t, 128, pv_done)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse2 = l > 0.f ? m_run + __log2f(l) : -INFINITY;
+      const size_t prow = (static_cast<size_t>(v * 2 + max(sgm.slot, 0)) * p.n_groups + mp) * R +
+                          t * kRowTile + rl;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait(o);
+        if (!valid) continue;
+        if (sgm.slot < 0) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            dst[q] = w;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * D + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                                 __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+        }
+      }
+      if (valid) {
+        if (sgm.slot < 0) {
+          if (p.lse != nullptr)
+            p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.N + i] = lse2 * 0.69314718055994531f;
+        } else {
+          p.ws_lse[prow] = lse2;
+        }
+      }
+      if (je < Wc) {                   // the next segment's first PV accumulates onto zero
+        uint32_t z[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0u;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_st32(tO + c * 32, z);
+      }
+      jg0 += T;
+    }
+    if (!ok) set_abort(abort, p.dev_err);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+  grid_dependents_launch();
+}
+
+// Merges the stream-K partials.  A (sequence, kv-head) pair cut by range boundaries left
+// one partial per range it touches (slot 0 where the range starts inside or at the pair,
+// slot 1 where the range ends in it); the block of the pair's first inner boundary merges
+// them.  Block (v * n_groups + mp, y) takes boundary v, row-tile group mp and rows
+// [32 y, 32 y + 32) of the group, four per warp; blocks of other boundaries exit at once.
+template <int D>
+__global__ void __launch_bounds__(256)
+    tree_attention_sk_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                                     const int32_t* __restrict__ prefix_len, int B, int N, int Hq,
+                                     int Hkv, int max_pages, int nvirt, int n_groups, int R,
+                                     uint16_t* __restrict__ out, float* __restrict__ lse) {
+  constexpr int E = D / 32;
+  __shared__ int s_pre[kLptMaxB + 1];
+  grid_dependency_wait();
+  const int v = blockIdx.x / n_groups, mp = blockIdx.x % n_groups;
+  if (v == 0) return;
+  const int cap = max_pages * kPage;
+  sk_tile_prefix(s_pre, prefix_len, B, N, cap, nullptr);
+  const SkSched sch(s_pre, B, Hkv, nvirt);
+  const int xb = sch.range_lo(v);
+  const SkSeg sg = sk_segment(sch, xb, xb, xb + 1);
+  if (sg.k0 == 0) return;                          // the boundary falls between two pairs
+  const int b = sg.b, g = sg.g;
+  const int sw = sch.start(b, g);
+  const int va = sch.range_of(sw);
+  if (va != v - 1) return;                         // not the pair's first inner boundary
+  const int vb = sch.range_of(sw + sch.tiles(b) - 1);
+  const int G = Hq / Hkv;
+  const int M = N * G;
+  const int lane = threadIdx.x & 31;
+  auto prow = [&](int vv, int rw) -> long long {
+    const int slot = sch.range_lo(vv) >= sw ? 0 : 1;
+    return (static_cast<long long>(vv * 2 + slot) * n_groups + mp) * R + rw;
+  };
+  for (int q = 0; q < 4; ++q) {
+    const int rw = blockIdx.y * 32 + (threadIdx.x >> 5) * 4 + q;
+    const int r = mp * R + rw;
+    if (rw >= R || r >= M) break;
+    const int i = r / G, h = g * G + (r % G);
+    float mx = -INFINITY;
+    for (int vv = va + lane; vv <= vb; vv += 32) mx = fmaxf(mx, ws_lse[prow(vv, rw)]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    for (int vv = va; vv <= vb; ++vv) {
+      const long long pr = prow(vv, rw);
+      const float l = ws_lse[pr];
+      const float w = (l == -INFINITY) ? 0.f : exp2f(l - mx);
+      wsum += w;
+      const float* o = ws_o + pr * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] += w * o[e];
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const long long rr = (static_cast<long long>(b) * N + i) * Hq + h;
+    uint16_t* dst = out + rr * D + lane * E;
+    uint32_t packed[E / 2];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) packed[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    }
+    if (lse != nullptr && lane == 0)
+      lse[(static_cast<long long>(b) * Hq + h) * N + i] =
+          (wsum > 0.f ? mx + __log2f(wsum) : -INFINITY) * 0.69314718055994531f;
+  }
+}
+
 // Merges split partials: O = sum_s 2^(lse_s - lse) O_s,  lse = log2 sum_s 2^lse_s.
 // One warp per output row, rows enumerated in the output's [B][N][Hq] order so that
 // consecutive warps write consecutive rows; each lane owns D/32 consecutive columns.
@@ -1012,6 +1677,8 @@ __global__ void __launch_bounds__(256)
 struct AttnPlan {
   int NT, n_groups, splits, chunk_tiles;
   bool cluster;          // splits merged through distributed shared memory (no workspace)
+  bool streamk;          // one CTA per SM over equal ranges of all key tiles (stream-K)
+  int nvirt;             // stream-K: ranges (each walked by n_groups CTAs)
   size_t ws_bytes;
 };
 
@@ -1028,6 +1695,55 @@ bool ensure_smem_attr() {
     return false;
   if (dev < 64) done[dev] = true;
   return true;
+}
+
+template <int NT, int D>
+bool ensure_smem_attr_sk() {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && done[dev]) return true;
+  if (cudaFuncSetAttribute(tree_attention_sk_kernel<NT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<NT, D>::kSmemBytes) != cudaSuccess)
+    return false;
+  if (dev < 64) done[dev] = true;
+  return true;
+}
+
+template <int D>
+jf_status launch_sk(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                    const CUtensorMap& kr, const CUtensorMap& vr, const AttnParams& prm, int nvirt,
+                    long long rows, uint16_t* out, float* lse, cudaStream_t s) {
+  using C = Cfg<2, D>;
+  if (!ensure_smem_attr_sk<2, D>()) return JF_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(static_cast<unsigned>(nvirt * prm.n_groups));
+  lc.blockDim = dim3(C::kThreads);
+  lc.dynamicSmemBytes = C::kSmemBytes;
+  lc.stream = s;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, tree_attention_sk_kernel<2, D>, qm, km, vm, kr, vr, prm, nvirt) != cudaSuccess)
+    return JF_ERR_CUDA;
+  cudaLaunchConfig_t lc2 = {};
+  lc2.gridDim = dim3(static_cast<unsigned>(nvirt * prm.n_groups), static_cast<unsigned>(2 * kRowTile / 32));
+  lc2.blockDim = dim3(256);
+  lc2.stream = s;
+  lc2.attrs = attr;
+  lc2.numAttrs = 1;
+  const float* wso = prm.ws_o;
+  const float* wsl = prm.ws_lse;
+  const int32_t* pfx = prm.prefix_len;
+  const int R = 2 * kRowTile;
+  return cudaLaunchKernelEx(&lc2, tree_attention_sk_combine_kernel<D>, wso, wsl, pfx, prm.B, prm.N, prm.Hq,
+                            prm.Hkv, prm.max_pages, nvirt, prm.n_groups, R, out, lse) == cudaSuccess
+             ? JF_OK
+             : JF_ERR_CUDA;
 }
 
 // How many clusters of `s` CTAs of this kernel fit on the current device at once
@@ -1132,6 +1848,26 @@ bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms
   pl->ws_bytes = (best_s > 1 && !best_cluster)
                      ? static_cast<size_t>(B) * Hq * N * best_s * (D + 1) * sizeof(float) + 256
                      : 0;
+  pl->streamk = false;
+  pl->nvirt = 0;
+  // Stream-K (one CTA per SM over equal ranges of all key tiles) when one unit per CTA
+  // leaves the last wave under 90% full and the work is tensor-bound: several row-tile
+  // groups read each K/V tile.  On HBM-bound work (one group) the range walk measured
+  // slower than the plain dispatch.  Positions in the range order are 32-bit.
+  const long long waves1 = (units + sms - 1) / sms;
+  const bool ragged_waves = units < waves1 * sms * 9 / 10;
+  const long long max_tiles_all =
+      static_cast<long long>(B) * Hkv * (static_cast<long long>(max_pages) * kPage / kKeyTile + 1);
+  if (pl->NT == 2 && pl->n_groups >= 2 && units >= sms && ragged_waves && B <= kLptMaxB &&
+      pl->n_groups <= sms && max_tiles_all < (1ll << 30)) {
+    pl->streamk = true;
+    pl->nvirt = sms / pl->n_groups;
+    pl->splits = 1;
+    pl->cluster = false;
+    pl->chunk_tiles = max_tiles;
+    pl->ws_bytes = static_cast<size_t>(pl->nvirt) * 2 * pl->n_groups * pl->NT * kRowTile * (D + 1) *
+                       sizeof(float) + 256;
+  }
   return true;
 }
 
@@ -1276,7 +2012,10 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
   prm.lse = lse;
   const size_t rows = static_cast<size_t>(B) * Hq * N;
   prm.ws_o = pl.ws_bytes > 0 ? static_cast<float*>(workspace) : nullptr;
-  prm.ws_lse = pl.ws_bytes > 0 ? static_cast<float*>(workspace) + rows * pl.splits * D : nullptr;
+  const size_t part_rows = pl.streamk
+                               ? static_cast<size_t>(pl.nvirt) * 2 * pl.n_groups * pl.NT * kRowTile
+                               : rows * pl.splits;
+  prm.ws_lse = pl.ws_bytes > 0 ? static_cast<float*>(workspace) + part_rows * D : nullptr;
   prm.dev_err = dev_err;
   prm.B = B; prm.N = N; prm.Hq = Hq; prm.Hkv = Hkv; prm.G = G; prm.W = (N + 63) / 64;
   prm.max_pages = max_pages; prm.num_pages = num_pages;
@@ -1286,6 +2025,13 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
   // Longest-first dispatch when every unit is one CTA and sequence lengths may differ.
   const bool lpt = pl.splits == 1 && B >= 2 && B <= jf::kLptMaxB;
   prm.scale_log2 = scale * 1.4426950408889634f;
+  if (pl.streamk) {
+    cudaStream_t s0 = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t* o16 = static_cast<uint16_t*>(out);
+    const long long nrows = static_cast<long long>(rows);
+    return D == 128 ? launch_sk<128>(qm, km, vm, kr, vr, prm, pl.nvirt, nrows, o16, lse, s0)
+                    : launch_sk<64>(qm, km, vm, kr, vr, prm, pl.nvirt, nrows, o16, lse, s0);
+  }
   const long long grid = static_cast<long long>(B) * Hkv * pl.splits * pl.n_groups;
   if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
