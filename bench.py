@@ -42,11 +42,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes per attention call from the ncu captures summarised under profiles/ (None
 # until a capture of the current kernel exists for that workload).
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one jf_tree_attention call
-# (split kernel + combine) from `ncu --set full` captures of the current kernels; see
+# (attention kernel + combine) from `ncu --set full` captures of the current kernels; see
 # profiles/tree_attention_<workload>_full.md for the commands.
 NCU_TRAFFIC_BYTES = {
     "c2_qwen3_8b_chain16": 8659712 + 2403840,
-    "c5_qwen3_30b_b8_tree256_32k": None,   # stream-K kernel: not yet captured
+    "c5_qwen3_30b_b8_tree256_32k": 567946496 + 27413248 + 38085632 + 2048,
 }
 
 
@@ -463,7 +463,7 @@ def main():
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = NCU_TRAFFIC_BYTES.get(w.name)
-    roof["kernel"] = "jf_tree_attention (split kernel + combine)"
+    roof["kernel"] = "jf_tree_attention (attention kernel + combine)"
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes"] = abytes
     roof["algorithmic_flops"] = aflops

@@ -99,6 +99,7 @@ struct AttnParams {
   float* lse;           // [B][Hq][N] or null      (splits == 1)
   float* ws_o;          // [B][Hkv][splits][M][D]  (splits > 1), row r = node * G + head
   float* ws_lse;        // [B][Hkv][splits][M]     (log2 domain)
+  int* ws_desc;         // stream-K: per range boundary, the pair it splits (8 ints)
   int32_t* dev_err;
   int B, N, Hq, Hkv, G, W, max_pages, num_pages;
   int n_groups, splits, chunk_tiles, M;
@@ -1103,6 +1104,22 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const int lo = sch.range_lo(v), hi = sch.range_lo(v + 1);
   const int Wc = hi - lo;
   if (Wc <= 0) return;
+  // Boundary v (this range's start) as the combine kernel needs it: the pair whose
+  // pieces it merges there, if v is the first boundary inside that pair.
+  if (mp == 0 && threadIdx.x == 0 && v > 0) {
+    const SkSeg f = sk_segment(sch, lo, lo, hi);
+    int4 d0 = make_int4(-1, 0, 0, 0), d1 = make_int4(0, 0, 0, 0);
+    if (f.k0 > 0) {
+      const int sw = sch.start(f.b, f.g);
+      const int va = sch.range_of(sw);
+      if (va == v - 1) {
+        d0 = make_int4(f.b, f.g, va, sch.range_of(sw + sch.tiles(f.b) - 1));
+        d1.x = sch.range_lo(va) == sw ? 0 : 1;     // slot of the first piece
+      }
+    }
+    reinterpret_cast<int4*>(p.ws_desc)[2 * v] = d0;
+    reinterpret_cast<int4*>(p.ws_desc)[2 * v + 1] = d1;
+  }
   // end (exclusive, in range tiles) of the segment that starts at range tile j
   auto seg_end = [&](int j) -> int { return sk_segment(sch, lo + j, lo, hi).x1 - lo; };
   auto prefix_of = [&](int b) -> int { return max(0, min(p.prefix_len[b], cap - p.N)); };
@@ -1521,63 +1538,79 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
 
 // Merges the stream-K partials.  A (sequence, kv-head) pair cut by range boundaries left
 // one partial per range it touches (slot 0 where the range starts inside or at the pair,
-// slot 1 where the range ends in it); the block of the pair's first inner boundary merges
-// them.  Block (v * n_groups + mp, y) takes boundary v, row-tile group mp and rows
-// [32 y, 32 y + 32) of the group, four per warp; blocks of other boundaries exit at once.
+// slot 1 where the range ends in it); the pair is merged at its first inner boundary,
+// which the split kernel described in `desc` (b, g, first range, last range; slot of the
+// first piece).  Block (v * n_groups + mp, y): boundary v, row-tile group mp, four rows
+// of the group per warp; blocks of boundaries that merge nothing exit at once.  A split
+// pair has at least two pieces: the first two of all four rows are fetched together, so
+// a warp waits about one memory round trip for the common case.
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
     tree_attention_sk_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
-                                     const int32_t* __restrict__ prefix_len, int B, int N, int Hq,
-                                     int Hkv, int max_pages, int nvirt, int n_groups, int R,
-                                     uint16_t* __restrict__ out, float* __restrict__ lse) {
+                                     const int4* __restrict__ desc, int N, int Hq, int Hkv,
+                                     int n_groups, int R, uint16_t* __restrict__ out,
+                                     float* __restrict__ lse) {
   constexpr int E = D / 32;
-  __shared__ int s_pre[kLptMaxB + 1];
+  constexpr int kRows = 4;
+  using VecE = typename std::conditional<E == 4, float4, float2>::type;
   grid_dependency_wait();
   const int v = blockIdx.x / n_groups, mp = blockIdx.x % n_groups;
   if (v == 0) return;
-  const int cap = max_pages * kPage;
-  sk_tile_prefix(s_pre, prefix_len, B, N, cap, nullptr);
-  const SkSched sch(s_pre, B, Hkv, nvirt);
-  const int xb = sch.range_lo(v);
-  const SkSeg sg = sk_segment(sch, xb, xb, xb + 1);
-  if (sg.k0 == 0) return;                          // the boundary falls between two pairs
-  const int b = sg.b, g = sg.g;
-  const int sw = sch.start(b, g);
-  const int va = sch.range_of(sw);
-  if (va != v - 1) return;                         // not the pair's first inner boundary
-  const int vb = sch.range_of(sw + sch.tiles(b) - 1);
-  const int G = Hq / Hkv;
-  const int M = N * G;
+  const int4 d0 = desc[2 * v];
+  if (d0.x < 0) return;
+  const int slot_a = desc[2 * v + 1].x;
+  const int b = d0.x, g = d0.y, va = d0.z, n = d0.w - d0.z + 1;
+  const int G = Hq / Hkv, M = N * G;
   const int lane = threadIdx.x & 31;
-  auto prow = [&](int vv, int rw) -> long long {
-    const int slot = sch.range_lo(vv) >= sw ? 0 : 1;
-    return (static_cast<long long>(vv * 2 + slot) * n_groups + mp) * R + rw;
+  const int rw0 = blockIdx.y * (8 * kRows) + (threadIdx.x >> 5) * kRows;
+  auto prow = [&](int rw, int k) -> long long {    // partial row of piece k (range va + k)
+    return (static_cast<long long>((va + k) * 2 + (k == 0 ? slot_a : 0)) * n_groups + mp) * R + rw;
   };
-  for (int q = 0; q < 4; ++q) {
-    const int rw = blockIdx.y * 32 + (threadIdx.x >> 5) * 4 + q;
+  auto ld = [&](int rw, int k) -> VecE {
+    return *reinterpret_cast<const VecE*>(ws_o + prow(rw, k) * D + lane * E);
+  };
+  float lk[kRows];
+  VecE x0[kRows], x1[kRows];
+#pragma unroll
+  for (int q = 0; q < kRows; ++q) {
+    const int rw = rw0 + q;
+    const bool ok = rw < R && mp * R + rw < M;
+    lk[q] = (ok && lane < n) ? ws_lse[prow(rw, lane)] : -INFINITY;
+    if (ok) { x0[q] = ld(rw, 0); x1[q] = ld(rw, 1); }
+  }
+#pragma unroll
+  for (int q = 0; q < kRows; ++q) {
+    const int rw = rw0 + q;
     const int r = mp * R + rw;
     if (rw >= R || r >= M) break;
-    const int i = r / G, h = g * G + (r % G);
-    float mx = -INFINITY;
-    for (int vv = va + lane; vv <= vb; vv += 32) mx = fmaxf(mx, ws_lse[prow(vv, rw)]);
+    float mx = lk[q];
+    for (int k = 32 + lane; k < n; k += 32) mx = fmaxf(mx, ws_lse[prow(rw, k)]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
     float wsum = 0.f;
-    for (int vv = va; vv <= vb; ++vv) {
-      const long long pr = prow(vv, rw);
-      const float l = ws_lse[pr];
-      const float w = (l == -INFINITY) ? 0.f : exp2f(l - mx);
-      wsum += w;
-      const float* o = ws_o + pr * D + lane * E;
+    {
+      const float wk = (lk[q] == -INFINITY) ? 0.f : exp2f(lk[q] - mx);
+      const float w0 = __shfl_sync(0xffffffffu, wk, 0), w1 = __shfl_sync(0xffffffffu, wk, 1);
+      const float* a0 = reinterpret_cast<const float*>(&x0[q]);
+      const float* a1 = reinterpret_cast<const float*>(&x1[q]);
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] += w * o[e];
+      for (int e = 0; e < E; ++e) acc[e] = w0 * a0[e] + w1 * a1[e];
+      wsum = w0 + w1;
+      for (int k = 2; k < n; ++k) {                // pairs spread over more than two ranges
+        const float lv = (k < 32) ? lk[q] : ws_lse[prow(rw, k)];
+        const float wl = (lv == -INFINITY) ? 0.f : exp2f(lv - mx);
+        const float w = k < 32 ? __shfl_sync(0xffffffffu, wl, k) : wl;
+        const VecE x = ld(rw, k);
+        const float* xs = reinterpret_cast<const float*>(&x);
+        wsum += w;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += w * xs[e];
+      }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const long long rr = (static_cast<long long>(b) * N + i) * Hq + h;
-    uint16_t* dst = out + rr * D + lane * E;
+    const int i = r / G, h = g * G + (r % G);
+    uint16_t* dst = out + ((static_cast<long long>(b) * N + i) * Hq + h) * D + lane * E;
     uint32_t packed[E / 2];
 #pragma unroll
     for (int e = 0; e < E; e += 2) packed[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
@@ -1738,10 +1771,10 @@ jf_status launch_sk(const CUtensorMap& qm, const CUtensorMap& km, const CUtensor
   lc2.numAttrs = 1;
   const float* wso = prm.ws_o;
   const float* wsl = prm.ws_lse;
-  const int32_t* pfx = prm.prefix_len;
+  const int4* dsc = reinterpret_cast<const int4*>(prm.ws_desc);
   const int R = 2 * kRowTile;
-  return cudaLaunchKernelEx(&lc2, tree_attention_sk_combine_kernel<D>, wso, wsl, pfx, prm.B, prm.N, prm.Hq,
-                            prm.Hkv, prm.max_pages, nvirt, prm.n_groups, R, out, lse) == cudaSuccess
+  return cudaLaunchKernelEx(&lc2, tree_attention_sk_combine_kernel<D>, wso, wsl, dsc, prm.N, prm.Hq,
+                            prm.Hkv, prm.n_groups, R, out, lse) == cudaSuccess
              ? JF_OK
              : JF_ERR_CUDA;
 }
@@ -1866,7 +1899,7 @@ bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms
     pl->cluster = false;
     pl->chunk_tiles = max_tiles;
     pl->ws_bytes = static_cast<size_t>(pl->nvirt) * 2 * pl->n_groups * pl->NT * kRowTile * (D + 1) *
-                       sizeof(float) + 256;
+                       sizeof(float) + static_cast<size_t>(pl->nvirt) * 8 * sizeof(int) + 256;
   }
   return true;
 }
@@ -2016,6 +2049,7 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
                                ? static_cast<size_t>(pl.nvirt) * 2 * pl.n_groups * pl.NT * kRowTile
                                : rows * pl.splits;
   prm.ws_lse = pl.ws_bytes > 0 ? static_cast<float*>(workspace) + part_rows * D : nullptr;
+  prm.ws_desc = pl.streamk ? reinterpret_cast<int*>(prm.ws_lse + part_rows) : nullptr;
   prm.dev_err = dev_err;
   prm.B = B; prm.N = N; prm.Hq = Hq; prm.Hkv = Hkv; prm.G = G; prm.W = (N + 63) / 64;
   prm.max_pages = max_pages; prm.num_pages = num_pages;
