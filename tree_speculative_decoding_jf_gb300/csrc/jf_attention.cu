@@ -1103,13 +1103,13 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const SkSched sch(s_pre, p.B, p.Hkv, nvirt);
   const int lo = sch.range_lo(v), hi = sch.range_lo(v + 1);
   const int Wc = hi - lo;
-  if (Wc <= 0) return;
   // Boundary v (this range's start) as the combine kernel needs it: the pair whose
-  // pieces it merges there, if v is the first boundary inside that pair.
+  // pieces it merges there, if v is the first boundary inside that pair.  (With fewer
+  // tiles than ranges the last ranges are empty and merge nothing.)
   if (mp == 0 && threadIdx.x == 0 && v > 0) {
-    const SkSeg f = sk_segment(sch, lo, lo, hi);
     int4 d0 = make_int4(-1, 0, 0, 0), d1 = make_int4(0, 0, 0, 0);
-    if (f.k0 > 0) {
+    const SkSeg f = Wc > 0 ? sk_segment(sch, lo, lo, hi) : SkSeg{0, 0, 0, 0, 0, 0};
+    if (Wc > 0 && f.k0 > 0) {
       const int sw = sch.start(f.b, f.g);
       const int va = sch.range_of(sw);
       if (va == v - 1) {
@@ -1120,6 +1120,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     reinterpret_cast<int4*>(p.ws_desc)[2 * v] = d0;
     reinterpret_cast<int4*>(p.ws_desc)[2 * v + 1] = d1;
   }
+  if (Wc <= 0) return;
   // end (exclusive, in range tiles) of the segment that starts at range tile j
   auto seg_end = [&](int j) -> int { return sk_segment(sch, lo + j, lo, hi).x1 - lo; };
   auto prefix_of = [&](int b) -> int { return max(0, min(p.prefix_len[b], cap - p.N)); };
