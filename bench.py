@@ -45,33 +45,36 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (attention kernel + combine) from `ncu --set full` captures of the current kernels; see
 # profiles/tree_attention_<workload>_full.md for the commands.
 NCU_TRAFFIC_BYTES = {
-    "c2_qwen3_8b_chain16": 8659712 + 2403840,
-    "c5_qwen3_30b_b8_tree256_32k": 567946496 + 27413248 + 38085632 + 2048,
+    "c2_qwen3_8b_chain16": 8659968 + 0 + 2404352 + 0,
+    "c5_qwen3_30b_b8_tree256_32k": 568709888 + 27651584 + 38085120 + 4352,
 }
 
 
 # ----------------------------------------------------------------------------- work model
 
-def attention_algorithmic_bytes(w) -> int:
+def attention_algorithmic_bytes(w, tree_len=None) -> int:
     """K/V of every visible position read once per kv-head, Q read, O written, masks and
-    block-table entries read."""
-    kv_len = w.prefix_len.astype(np.int64) + w.N
+    block-table entries read (ragged trees: the first tree_len[b] nodes of sequence b)."""
+    n = np.full(w.B, w.N, np.int64) if tree_len is None else np.asarray(tree_len, np.int64)
+    kv_len = w.prefix_len.astype(np.int64) + n
     kv = int(kv_len.sum()) * w.Hkv * w.D * 2 * 2
-    qo = 2 * w.B * w.N * w.Hq * w.D * 2
-    mask = w.B * w.N * ((w.N + 63) // 64) * 8
+    qo = 2 * int(n.sum()) * w.Hq * w.D * 2
+    mask = int(n.sum()) * ((w.N + 63) // 64) * 8
     bt = int(((kv_len + w.page - 1) // w.page).sum()) * 4
     return kv + qo + mask + bt
 
 
-def attention_algorithmic_flops(w) -> int:
-    """4 * D * Hq * sum_b (N * P_b + sum_i (depth_i + 1)): visible (query, key) pairs."""
+def attention_algorithmic_flops(w, tree_len=None) -> int:
+    """4 * D * Hq * sum_b (n_b * P_b + sum_{i < n_b} (depth_i + 1)): visible (query, key)
+    pairs, n_b = N or tree_len[b]."""
     tot = 0
     for b in range(w.B):
+        nb = w.N if tree_len is None else int(tree_len[b])
         par = w.parent[b]
-        depth = np.zeros(w.N, dtype=np.int64)
-        for i in range(1, w.N):
+        depth = np.zeros(nb, dtype=np.int64)
+        for i in range(1, nb):
             depth[i] = depth[par[i]] + 1
-        tot += w.N * int(w.prefix_len[b]) + int((depth + 1).sum())
+        tot += nb * int(w.prefix_len[b]) + int((depth + 1).sum())
     return 4 * w.D * w.Hq * tot
 
 
@@ -355,6 +358,25 @@ def run_gpu(args, w, rank, world):
     tree_ms = [a.elapsed_time(b_) for a, b_ in tree_ev]
     tree_bytes = int(t_dl.numel()) * 2
 
+    # ---- ragged trees: the same attention call with a per-sequence budget mix (seeded,
+    # uniform in [N/4, N]); its mask is built once beforehand.  Not part of the step.
+    rag_len = np.random.default_rng(w.seed + 1000).integers(max(1, N // 4), N + 1, B)
+    t_rag = torch.from_numpy(rag_len.astype(np.int32)).to(dev)
+    mask_r = torch.empty_like(mask)
+    jf.jf_build_tree_mask_ragged(t["parent"], t["prefix_len"], t_rag, mask_r, None, None, err)
+
+    def call_attn_ragged():
+        jf.jf_tree_attention_ragged(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                    t["prefix_len"], t_rag, mask_r, w.scale, out, lse, ws_a, err)
+
+    call_attn_ragged()
+    g_rag = capture(call_attn_ragged)
+    for k in range(args.warmup):
+        timed(g_rag, k)
+    rag_ev = [timed(g_rag, k) for k in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    rag_ms = [a.elapsed_time(b_) for a, b_ in rag_ev]
+
     # ---- after verification: accepted-path KV compaction (not part of the step).  It
     # rewrites the cache in place, so it is timed last; replays repeat the same copies.
     new_prefix = torch.empty_like(t["prefix_len"])
@@ -374,7 +396,7 @@ def run_gpu(args, w, rank, world):
     return dict(step_ms=step_ms, mask_ms=mask_ms, attn_ms=attn_ms, ver_ms=ver_ms, clocks=clk,
                 e2e=e2e, launches=2 * launches_per_step * args.steps, ws=ws_a_bytes,
                 compact_ms=compact_ms, accepted=acc.cpu().tolist(), tree_ms=tree_ms,
-                tree_bytes=tree_bytes)
+                tree_bytes=tree_bytes, rag_ms=rag_ms, rag_len=rag_len.tolist())
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -493,7 +515,13 @@ def main():
                          "draft_tree_logits_hbm_gbs": r["tree_bytes"] /
                          (statistics.mean(r["tree_ms"]) * 1e-3) / 1e9,
                          "kv_compaction_after_verify": statistics.mean(r["compact_ms"]) * 1e3,
-                         "kv_compaction_accepted_nodes": r["accepted"]},
+                         "kv_compaction_accepted_nodes": r["accepted"],
+                         "attention_ragged": statistics.mean(r["rag_ms"]) * 1e3,
+                         "attention_ragged_tree_len": r["rag_len"],
+                         "attention_ragged_hbm_gbs": attention_algorithmic_bytes(w, r["rag_len"]) /
+                         (statistics.mean(r["rag_ms"]) * 1e-3) / 1e9,
+                         "attention_ragged_tflops": attention_algorithmic_flops(w, r["rag_len"]) /
+                         (statistics.mean(r["rag_ms"]) * 1e-3) / 1e12},
         "roofline": roof, "cpu_baseline": cpu, "e2e": r["e2e"], "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }

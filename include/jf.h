@@ -60,6 +60,7 @@ typedef enum { JF_DTYPE_BF16 = 0, JF_DTYPE_F32 = 1 } jf_dtype;
 #define JF_DEVERR_BAD_TOKEN 0x8  /* draft token (non-root node) outside [0, V)          */
 #define JF_DEVERR_TIMEOUT 0x10   /* an in-kernel wait gave up after its time limit      */
 #define JF_DEVERR_BAD_PATH 0x20  /* accepted path / length malformed (KV compaction)     */
+#define JF_DEVERR_BAD_TREE_LEN 0x40 /* tree_len[b] outside [1, N] (ragged calls)         */
 
 /* Largest tree (nodes per sequence) any call accepts. */
 #define JF_MAX_NODES 4096
@@ -196,6 +197,45 @@ jf_status jf_tree_verify_static(const void* logits, int32_t dtype, const int32_t
                                 const int32_t* parent, int32_t B, int32_t N, int32_t V,
                                 int32_t* argmax, int32_t* accept_len, int32_t* path,
                                 int32_t* bonus, int32_t* dev_err, jf_stream_t stream);
+
+/* ---------------------------------------------------------------- ragged trees
+ * One batch may mix tree budgets: the best budget depends on the serving load (explainer
+ * §4, serving performance), so sequences of one step can carry trees of different sizes.
+ * The three calls below are jf_build_tree_mask, jf_tree_attention and jf_tree_verify with
+ * one more argument, tree_len int32 [B] (device): sequence b's tree has the nodes
+ * 0 .. n_b - 1, n_b = tree_len[b], 1 <= n_b <= N; arrays keep their [B][N] shapes and
+ * entries of nodes i >= n_b are padding.  With tree_len[b] == N for every b each call
+ * computes exactly what its fixed-size counterpart computes.  A tree_len entry outside
+ * [1, N] sets JF_DEVERR_BAD_TREE_LEN and is clamped into that range.
+ *   jf_build_tree_mask_ragged: parent[b][i] is read for i < n_b only; rows i >= n_b get
+ *     all-zero mask words and depth = pos = -1.
+ *   jf_tree_attention_ragged: the tree's keys/values are the n_b positions
+ *     P_b .. P_b + n_b - 1; block-table entries past ceil((P_b + n_b) / page_size) are
+ *     never read and K/V slots past P_b + n_b may hold anything (the padding nodes need no
+ *     K/V at all).  Rows i < n_b are as in jf_tree_attention; rows i >= n_b of out and lse
+ *     carry no meaning (they attend to what their mask row allows, the prefix with the
+ *     mask of jf_build_tree_mask_ragged).
+ *   jf_tree_verify_ragged: nodes i >= n_b are never accepted and their parent and draft
+ *     entries are not read; argmax is still written for every row, so logits rows
+ *     i >= n_b must be readable (their values do not matter).  path[b] lists nodes < n_b.
+ * Workspace sizes are those of the fixed-size calls with the same N.
+ */
+jf_status jf_build_tree_mask_ragged(const int32_t* parent, const int32_t* prefix_len,
+                                    const int32_t* tree_len, int32_t B, int32_t N,
+                                    uint64_t* mask, int32_t* depth, int32_t* pos,
+                                    int32_t* dev_err, jf_stream_t stream);
+jf_status jf_tree_attention_ragged(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* prefix_len,
+                                   const int32_t* tree_len, const uint64_t* mask, int32_t B,
+                                   int32_t N, int32_t Hq, int32_t Hkv, int32_t D,
+                                   int32_t page_size, int32_t max_pages, int32_t num_pages,
+                                   float scale, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, jf_stream_t stream);
+jf_status jf_tree_verify_ragged(const void* logits, int32_t dtype, const int32_t* draft,
+                                const int32_t* parent, const int32_t* tree_len, int32_t B,
+                                int32_t N, int32_t V, int32_t* argmax, int32_t* accept_len,
+                                int32_t* path, int32_t* bonus, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_err, jf_stream_t stream);
 
 /* ---------------------------------------------------------------- before verification
  * jf_build_draft_tree -- builds the draft tree from per-depth draft logits.  JetFlow

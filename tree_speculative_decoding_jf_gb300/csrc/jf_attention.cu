@@ -105,7 +105,14 @@ struct AttnParams {
   int n_groups, splits, chunk_tiles, M;
   int cluster_merge;    // 1: the splits of a unit form one cluster and merge through DSMEM
   float scale_log2;     // softmax scale * log2(e)
+  const int32_t* tree_len;  // ragged calls: nodes per sequence (else null: N everywhere)
 };
+
+// Nodes of sequence b's tree: N, or tree_len[b] clamped to [1, N] for ragged calls.  The
+// tree's keys are the n positions after the prefix, so the sequence has P_b + n keys.
+__device__ __forceinline__ int tree_nodes(const int32_t* tree_len, int b, int N) {
+  return tree_len == nullptr ? N : max(1, min(tree_len[b], N));
+}
 
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
   int ok = 1;
@@ -434,12 +441,15 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   }
 
   const int cap = p.max_pages * kPage;
+  const int nt = tree_nodes(p.tree_len, b, p.N);
+  if (p.tree_len != nullptr && nt != p.tree_len[b] && threadIdx.x == 0)
+    report(p.dev_err, JF_DEVERR_BAD_TREE_LEN);
   int P = p.prefix_len[b];
-  if (P < 0 || P > cap - p.N) {
+  if (P < 0 || P > cap - nt) {
     if (threadIdx.x == 0) report(p.dev_err, JF_DEVERR_BAD_PREFIX);
-    P = max(0, min(P, cap - p.N));
+    P = max(0, min(P, cap - nt));
   }
-  const int L = P + p.N;
+  const int L = P + nt;
   const int ntiles = (L + kKeyTile - 1) / kKeyTile;
   const int k0 = split * p.chunk_tiles;
   const int k1 = min(ntiles, k0 + p.chunk_tiles);
@@ -970,20 +980,23 @@ struct SkSched {
 };
 
 // pre[0] = 0, pre[b + 1] = key tiles of sequences 0..b (prefix lengths clamped to the
-// pool, the clamp reported through `err` when given).  Every thread of the block calls it;
+// pool, tree sizes to [1, N], the clamps reported through `err` when given).  Every thread of the block calls it;
 // B <= kLptMaxB <= blockDim.x.  Each warp scans 32 sequences with shuffles, then adds the
 // totals of the warps before it.
-__device__ __noinline__ void sk_tile_prefix(int* pre, const int32_t* prefix_len, int B, int N, int cap,
+__device__ __noinline__ void sk_tile_prefix(int* pre, const int32_t* prefix_len,
+                                            const int32_t* tree_len, int B, int N, int cap,
                                             int* err) {
   const int u = threadIdx.x, lane = u & 31;
   int x = 0;
   if (u < B) {
+    const int n = tree_nodes(tree_len, u, N);
+    if (tree_len != nullptr && n != tree_len[u] && err != nullptr) report(err, JF_DEVERR_BAD_TREE_LEN);
     int P = prefix_len[u];
-    if (P < 0 || P > cap - N) {
+    if (P < 0 || P > cap - n) {
       if (err != nullptr) report(err, JF_DEVERR_BAD_PREFIX);
-      P = max(0, min(P, cap - N));
+      P = max(0, min(P, cap - n));
     }
-    x = (P + N + kKeyTile - 1) / kKeyTile;
+    x = (P + n + kKeyTile - 1) / kKeyTile;
   }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -1099,7 +1112,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
 
   // ---- the schedule: tiles per sequence, their running sums, this range's segments
   const int cap = p.max_pages * kPage;
-  sk_tile_prefix(s_pre, p.prefix_len, p.B, p.N, cap, blockIdx.x == 0 ? p.dev_err : nullptr);
+  sk_tile_prefix(s_pre, p.prefix_len, p.tree_len, p.B, p.N, cap, blockIdx.x == 0 ? p.dev_err : nullptr);
   const SkSched sch(s_pre, p.B, p.Hkv, nvirt);
   const int lo = sch.range_lo(v), hi = sch.range_lo(v + 1);
   const int Wc = hi - lo;
@@ -1123,7 +1136,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   if (Wc <= 0) return;
   // end (exclusive, in range tiles) of the segment that starts at range tile j
   auto seg_end = [&](int j) -> int { return sk_segment(sch, lo + j, lo, hi).x1 - lo; };
-  auto prefix_of = [&](int b) -> int { return max(0, min(p.prefix_len[b], cap - p.N)); };
+
   if (warp == 1) {
     tmem_alloc(&tmem_slot, C::kTmemCols);
     tmem_relinquish();
@@ -1156,7 +1169,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     for (int s = 0; jg0 < Wc && ok; ++s) {
       const SkSeg sg = sk_segment(sch, lo + jg0, lo, hi);
       const int T = sg.k1 - sg.k0;
-      const int L = prefix_of(sg.b) + p.N;
+      const int nsg = tree_nodes(p.tree_len, sg.b, p.N);
+      const int L = max(0, min(p.prefix_len[sg.b], cap - nsg)) + nsg;
       const int32_t* bt = p.block_table + static_cast<size_t>(sg.b) * p.max_pages;
       // this segment's Q, once the previous segment's S MMAs no longer read the buffer
       int okq = 1;
@@ -1380,7 +1394,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const SkSeg sgm = sk_segment(sch, lo + jg0, lo, hi);
       const int T = sgm.k1 - sgm.k0;
       const int b = sgm.b, g = sgm.g;
-      const int P = prefix_of(b), L = P + p.N;
+      const int nsg = tree_nodes(p.tree_len, b, p.N);
+      const int P = max(0, min(p.prefix_len[b], cap - nsg)), L = P + nsg;
       const int h = g * p.G + (r % p.G);
       const uint64_t* mrow = p.mask + (static_cast<size_t>(b) * p.N + (valid ? i : 0)) * W;
       float m_run = -INFINITY;
@@ -1972,14 +1987,15 @@ extern "C" size_t jf_tree_attention_workspace_size(int32_t B, int32_t N, int32_t
   return pl.ws_bytes;
 }
 
-extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const void* v_cache,
-                                       const int32_t* block_table, const int32_t* prefix_len,
-                                       const uint64_t* mask, int32_t B, int32_t N, int32_t Hq,
-                                       int32_t Hkv, int32_t D, int32_t page_size,
-                                       int32_t max_pages, int32_t num_pages, float scale,
-                                       void* out, float* lse, void* workspace,
-                                       size_t workspace_bytes, int32_t* dev_err,
-                                       jf_stream_t stream) {
+namespace {
+
+jf_status tree_attention_call(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, const int32_t* prefix_len,
+                              const int32_t* tree_len, const uint64_t* mask, int32_t B,
+                              int32_t N, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                              int32_t max_pages, int32_t num_pages, float scale, void* out,
+                              float* lse, void* workspace, size_t workspace_bytes,
+                              int32_t* dev_err, jf_stream_t stream) {
   using namespace jf;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       prefix_len == nullptr || mask == nullptr || out == nullptr)
@@ -2041,6 +2057,7 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
   AttnParams prm;
   prm.block_table = block_table;
   prm.prefix_len = prefix_len;
+  prm.tree_len = tree_len;
   prm.mask = mask;
   prm.out = static_cast<uint16_t*>(out);
   prm.lse = lse;
@@ -2112,4 +2129,34 @@ extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const
     return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
   }
   return JF_OK;
+}
+
+}  // namespace
+
+extern "C" jf_status jf_tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_table, const int32_t* prefix_len,
+                                       const uint64_t* mask, int32_t B, int32_t N, int32_t Hq,
+                                       int32_t Hkv, int32_t D, int32_t page_size,
+                                       int32_t max_pages, int32_t num_pages, float scale,
+                                       void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_err,
+                                       jf_stream_t stream) {
+  return tree_attention_call(q, k_cache, v_cache, block_table, prefix_len, nullptr, mask, B, N, Hq,
+                             Hkv, D, page_size, max_pages, num_pages, scale, out, lse, workspace,
+                             workspace_bytes, dev_err, stream);
+}
+
+extern "C" jf_status jf_tree_attention_ragged(const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_table,
+                                              const int32_t* prefix_len, const int32_t* tree_len,
+                                              const uint64_t* mask, int32_t B, int32_t N,
+                                              int32_t Hq, int32_t Hkv, int32_t D,
+                                              int32_t page_size, int32_t max_pages,
+                                              int32_t num_pages, float scale, void* out,
+                                              float* lse, void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_err, jf_stream_t stream) {
+  if (tree_len == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return tree_attention_call(q, k_cache, v_cache, block_table, prefix_len, tree_len, mask, B, N,
+                             Hq, Hkv, D, page_size, max_pages, num_pages, scale, out, lse,
+                             workspace, workspace_bytes, dev_err, stream);
 }

@@ -9,7 +9,8 @@
 // validated once; then each thread owns (node i, word w) pairs and walks i's ancestor
 // chain, setting the bits that fall into word w and stopping as soon as the chain drops
 // below the word's first node (ancestor ids decrease strictly).  The w == 0 walk reaches
-// the root, so it also yields depth and position id.
+// the root, so it also yields depth and position id.  Ragged calls give sequence b only
+// n_b nodes: rows of padding nodes (i >= n_b) get zero words and depth = pos = -1.
 #include "jf_common.cuh"
 
 namespace jf {
@@ -19,14 +20,25 @@ constexpr int kMaskThreads = 256;
 
 __global__ void __launch_bounds__(kMaskThreads)
     tree_mask_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ prefix_len,
-                     int N, int W, uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
+                     const int32_t* __restrict__ tree_len, int N, int W,
+                     uint64_t* __restrict__ mask, int32_t* __restrict__ depth,
                      int32_t* __restrict__ pos, int32_t* dev_err) {
   extern __shared__ int32_t s_par[];   // [N]; malformed entries replaced by -1
   grid_dependency_wait();
   const int b = blockIdx.x;
   const int32_t* par = parent + static_cast<size_t>(b) * N;
+  int n = N;                           // nodes of this sequence's tree
+  if (tree_len != nullptr) {
+    const int raw = tree_len[b];
+    n = max(1, min(raw, N));
+    if (raw != n && threadIdx.x == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
+  }
   int bad = 0;
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    if (i >= n) {                      // padding: never read, never an ancestor
+      s_par[i] = -1;
+      continue;
+    }
     int p = par[i];
     const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
     if (!ok) {
@@ -43,6 +55,14 @@ __global__ void __launch_bounds__(kMaskThreads)
   for (int e = threadIdx.x; e < pairs; e += blockDim.x) {
     const int i = e / W;
     const int w = e - i * W;
+    if (i >= n) {
+      mrow[e] = 0ull;
+      if (w == 0) {
+        if (depth != nullptr) depth[static_cast<size_t>(b) * N + i] = -1;
+        if (pos != nullptr) pos[static_cast<size_t>(b) * N + i] = -1;
+      }
+      continue;
+    }
     const int lo = w * 64;
     uint64_t word = 0;
     int count = 0;
@@ -67,9 +87,11 @@ __global__ void __launch_bounds__(kMaskThreads)
 }  // namespace
 }  // namespace jf
 
-extern "C" jf_status jf_build_tree_mask(const int32_t* parent, const int32_t* prefix_len,
-                                        int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
-                                        int32_t* pos, int32_t* dev_err, jf_stream_t stream) {
+namespace {
+
+jf_status build_mask(const int32_t* parent, const int32_t* prefix_len, const int32_t* tree_len,
+                     int32_t B, int32_t N, uint64_t* mask, int32_t* depth, int32_t* pos,
+                     int32_t* dev_err, jf_stream_t stream) {
   if (parent == nullptr || prefix_len == nullptr || mask == nullptr) return JF_ERR_INVALID_ARGUMENT;
   if (B < 1 || N < 1) return JF_ERR_INVALID_ARGUMENT;
   if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
@@ -78,6 +100,22 @@ extern "C" jf_status jf_build_tree_mask(const int32_t* parent, const int32_t* pr
   const size_t smem = sizeof(int32_t) * static_cast<size_t>(N);
   const cudaError_t e = jf::launch_pdl(jf::tree_mask_kernel, dim3(B), dim3(jf::kMaskThreads), smem,
                                        reinterpret_cast<cudaStream_t>(stream), parent,
-                                       prefix_len, N, W, mask, depth, pos, dev_err);
+                                       prefix_len, tree_len, N, W, mask, depth, pos, dev_err);
   return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" jf_status jf_build_tree_mask(const int32_t* parent, const int32_t* prefix_len,
+                                        int32_t B, int32_t N, uint64_t* mask, int32_t* depth,
+                                        int32_t* pos, int32_t* dev_err, jf_stream_t stream) {
+  return build_mask(parent, prefix_len, nullptr, B, N, mask, depth, pos, dev_err, stream);
+}
+
+extern "C" jf_status jf_build_tree_mask_ragged(const int32_t* parent, const int32_t* prefix_len,
+                                               const int32_t* tree_len, int32_t B, int32_t N,
+                                               uint64_t* mask, int32_t* depth, int32_t* pos,
+                                               int32_t* dev_err, jf_stream_t stream) {
+  if (tree_len == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return build_mask(parent, prefix_len, tree_len, B, N, mask, depth, pos, dev_err, stream);
 }

@@ -153,7 +153,8 @@ inline int walk_threads(int N) { return std::min(kWalkThreads, std::max(128, (N 
 __global__ void __launch_bounds__(kWalkThreads)
     tree_walk_kernel(const uint64_t* __restrict__ part, int chunks,
                      const int32_t* __restrict__ draft, const int32_t* __restrict__ parent,
-                     int N, int V, int32_t* __restrict__ argmax_out,
+                     const int32_t* __restrict__ tree_len, int N, int V,
+                     int32_t* __restrict__ argmax_out,
                      int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                      int32_t* __restrict__ bonus, int32_t* dev_err) {
   extern __shared__ uint64_t sm64[];
@@ -172,6 +173,13 @@ __global__ void __launch_bounds__(kWalkThreads)
   grid_dependency_wait();
   const int b = blockIdx.x;
   const size_t rb = static_cast<size_t>(b) * N;
+  // Ragged calls: nodes >= nt are padding, never read and never accepted.
+  int nt = N;
+  if (tree_len != nullptr) {
+    const int raw = tree_len[b];
+    nt = max(1, min(raw, N));
+    if (raw != nt && threadIdx.x == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
+  }
   // The block is sized to the tree (threadIdx.x + k * blockDim.x covers every node for
   // k < kPer).  Parents and drafts are requested first and stay in flight while the
   // chunk keys are merged, so both arrive in one memory round trip.
@@ -180,7 +188,7 @@ __global__ void __launch_bounds__(kWalkThreads)
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int i = threadIdx.x + k * blockDim.x;
-    if (i < N) {
+    if (i < nt) {
       r_par[k] = parent[rb + i];
       r_draft[k] = draft[rb + i];
     }
@@ -214,16 +222,17 @@ __global__ void __launch_bounds__(kWalkThreads)
   for (int k = 0; k < kPer; ++k) {
     const int i = threadIdx.x + k * blockDim.x;
     if (i < N) {
-      int p = r_par[k];
+      int p = i < nt ? r_par[k] : -1;
       const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
-      if (!ok) { bad_parent = 1; p = -1; }
+      if (!ok && i < nt) bad_parent = 1;
+      if (!ok) p = -1;
       s_par[i] = p;
       s_anc[i] = p;
       s_dep[i] = p >= 0 ? 1 : 0;
       s_key[i] = 0u;
-      const int d = r_draft[k];
+      const int d = i < nt ? r_draft[k] : -1;
       s_draft[i] = d;
-      if (i > 0 && (d < 0 || d >= V)) bad_token = 1;
+      if (i > 0 && i < nt && (d < 0 || d >= V)) bad_token = 1;
     }
   }
   __syncthreads();
@@ -332,11 +341,13 @@ extern "C" size_t jf_tree_verify_workspace_size(int32_t B, int32_t N, int32_t V)
   return static_cast<size_t>(B) * N * p.chunks * sizeof(uint64_t);
 }
 
-extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int32_t* draft,
-                                    const int32_t* parent, int32_t B, int32_t N, int32_t V,
-                                    int32_t* argmax, int32_t* accept_len, int32_t* path,
-                                    int32_t* bonus, void* workspace, size_t workspace_bytes,
-                                    int32_t* dev_err, jf_stream_t stream) {
+namespace {
+
+jf_status tree_verify_call(const void* logits, int32_t dtype, const int32_t* draft,
+                           const int32_t* parent, const int32_t* tree_len, int32_t B, int32_t N,
+                           int32_t V, int32_t* argmax, int32_t* accept_len, int32_t* path,
+                           int32_t* bonus, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_err, jf_stream_t stream) {
   if (logits == nullptr || draft == nullptr || parent == nullptr || accept_len == nullptr ||
       path == nullptr || bonus == nullptr || workspace == nullptr)
     return JF_ERR_INVALID_ARGUMENT;
@@ -371,8 +382,30 @@ extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int
   }
   const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::walk_threads(N)), smem,
                                         s, static_cast<const uint64_t*>(part), p.chunks, draft,
-                                        parent, N, V, argmax, accept_len, path, bonus, dev_err);
+                                        parent, tree_len, N, V, argmax, accept_len, path, bonus, dev_err);
   return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int32_t* draft,
+                                    const int32_t* parent, int32_t B, int32_t N, int32_t V,
+                                    int32_t* argmax, int32_t* accept_len, int32_t* path,
+                                    int32_t* bonus, void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_err, jf_stream_t stream) {
+  return tree_verify_call(logits, dtype, draft, parent, nullptr, B, N, V, argmax, accept_len, path,
+                          bonus, workspace, workspace_bytes, dev_err, stream);
+}
+
+extern "C" jf_status jf_tree_verify_ragged(const void* logits, int32_t dtype, const int32_t* draft,
+                                           const int32_t* parent, const int32_t* tree_len,
+                                           int32_t B, int32_t N, int32_t V, int32_t* argmax,
+                                           int32_t* accept_len, int32_t* path, int32_t* bonus,
+                                           void* workspace, size_t workspace_bytes,
+                                           int32_t* dev_err, jf_stream_t stream) {
+  if (tree_len == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return tree_verify_call(logits, dtype, draft, parent, tree_len, B, N, V, argmax, accept_len,
+                          path, bonus, workspace, workspace_bytes, dev_err, stream);
 }
 
 // ------------------------------------------------------------------------ allocation-free
@@ -442,6 +475,6 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
     return JF_ERR_CUDA;
   const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::walk_threads(N)), smem,
                                         s, static_cast<const uint64_t*>(part), p.chunks, draft,
-                                        parent, N, V, argmax, accept_len, path, bonus, dev_err);
+                                        parent, nullptr, N, V, argmax, accept_len, path, bonus, dev_err);
   return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }

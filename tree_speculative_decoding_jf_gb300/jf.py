@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "JF_OK", 1: "JF_ERR_INVALID_ARGUMENT", 2: "JF_ERR_INVALID_TRE
 JF_DTYPE_BF16, JF_DTYPE_F32 = 0, 1
 DEVERR_BAD_PARENT, DEVERR_BAD_PAGE, DEVERR_BAD_PREFIX = 0x1, 0x2, 0x4
 DEVERR_BAD_TOKEN, DEVERR_TIMEOUT, DEVERR_BAD_PATH = 0x8, 0x10, 0x20
+DEVERR_BAD_TREE_LEN = 0x40
 MAX_NODES = 4096
 PAGE_SIZE = 16
 
@@ -62,6 +63,13 @@ def _load():
     lib.jf_compact_accepted_kv.restype = ctypes.c_int
     lib.jf_build_draft_tree.argtypes = [P, i32, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
     lib.jf_build_draft_tree.restype = ctypes.c_int
+    lib.jf_build_tree_mask_ragged.argtypes = [P, P, P, i32, i32, P, P, P, P, P]
+    lib.jf_build_tree_mask_ragged.restype = ctypes.c_int
+    lib.jf_tree_attention_ragged.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                             i32, i32, f32, P, P, P, sz, P, P]
+    lib.jf_tree_attention_ragged.restype = ctypes.c_int
+    lib.jf_tree_verify_ragged.argtypes = [P, i32, P, P, P, i32, i32, i32, P, P, P, P, P, sz, P, P]
+    lib.jf_tree_verify_ragged.restype = ctypes.c_int
     return lib
 
 
@@ -107,6 +115,17 @@ def jf_version() -> int:
 
 def jf_build_tree_mask(parent, prefix_len, mask, depth=None, pos=None, dev_err=None,
                        stream=None) -> None:
+    _mask_call(parent, prefix_len, None, mask, depth, pos, dev_err, stream)
+
+
+def jf_build_tree_mask_ragged(parent, prefix_len, tree_len, mask, depth=None, pos=None,
+                              dev_err=None, stream=None) -> None:
+    """Per-sequence tree sizes: nodes i >= tree_len[b] are padding (see include/jf.h)."""
+    _need(tree_len, "tree_len", torch.int32, (parent.shape[0],))
+    _mask_call(parent, prefix_len, tree_len, mask, depth, pos, dev_err, stream)
+
+
+def _mask_call(parent, prefix_len, tree_len, mask, depth, pos, dev_err, stream) -> None:
     B, N = parent.shape
     W = (N + 63) // 64
     _need(parent, "parent", torch.int32)
@@ -117,9 +136,14 @@ def jf_build_tree_mask(parent, prefix_len, mask, depth=None, pos=None, dev_err=N
             _need(t, name, torch.int32, (B, N))
     if dev_err is not None:
         _need(dev_err, "dev_err", torch.int32, (1,))
-    _check("jf_build_tree_mask", _lib.jf_build_tree_mask(
-        _ptr(parent), _ptr(prefix_len), B, N, _ptr(mask), _ptr(depth), _ptr(pos), _ptr(dev_err),
-        _stream(stream)))
+    if tree_len is None:
+        _check("jf_build_tree_mask", _lib.jf_build_tree_mask(
+            _ptr(parent), _ptr(prefix_len), B, N, _ptr(mask), _ptr(depth), _ptr(pos),
+            _ptr(dev_err), _stream(stream)))
+    else:
+        _check("jf_build_tree_mask_ragged", _lib.jf_build_tree_mask_ragged(
+            _ptr(parent), _ptr(prefix_len), _ptr(tree_len), B, N, _ptr(mask), _ptr(depth),
+            _ptr(pos), _ptr(dev_err), _stream(stream)))
 
 
 def jf_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_pages, page_size=PAGE_SIZE) -> int:
@@ -131,6 +155,21 @@ def jf_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_pages, page_size=PAGE
 
 def jf_tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale, out, lse=None,
                       workspace=None, dev_err=None, stream=None) -> None:
+    _attention_call(q, k_cache, v_cache, block_table, prefix_len, None, mask, scale, out, lse,
+                    workspace, dev_err, stream)
+
+
+def jf_tree_attention_ragged(q, k_cache, v_cache, block_table, prefix_len, tree_len, mask,
+                             scale, out, lse=None, workspace=None, dev_err=None,
+                             stream=None) -> None:
+    """Per-sequence tree sizes: sequence b's tree keys are P_b .. P_b + tree_len[b] - 1."""
+    _need(tree_len, "tree_len", torch.int32, (q.shape[0],))
+    _attention_call(q, k_cache, v_cache, block_table, prefix_len, tree_len, mask, scale, out,
+                    lse, workspace, dev_err, stream)
+
+
+def _attention_call(q, k_cache, v_cache, block_table, prefix_len, tree_len, mask, scale, out,
+                    lse, workspace, dev_err, stream) -> None:
     B, N, Hq, D = q.shape
     num_pages, page, Hkv, D2 = k_cache.shape
     max_pages = block_table.shape[1]
@@ -153,10 +192,17 @@ def jf_tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale,
         if workspace.device.type != "cuda" or not workspace.is_contiguous():
             raise ValueError("workspace must be a contiguous CUDA tensor")
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check("jf_tree_attention", _lib.jf_tree_attention(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(prefix_len), _ptr(mask),
-        B, N, Hq, Hkv, D, page, max_pages, num_pages, float(scale), _ptr(out), _ptr(lse),
-        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)))
+    if tree_len is None:
+        _check("jf_tree_attention", _lib.jf_tree_attention(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
+            _ptr(mask), B, N, Hq, Hkv, D, page, max_pages, num_pages, float(scale), _ptr(out),
+            _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)))
+    else:
+        _check("jf_tree_attention_ragged", _lib.jf_tree_attention_ragged(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
+            _ptr(tree_len), _ptr(mask), B, N, Hq, Hkv, D, page, max_pages, num_pages,
+            float(scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_err),
+            _stream(stream)))
 
 
 def jf_tree_verify_workspace_size(B, N, V) -> int:
@@ -168,6 +214,20 @@ def jf_tree_verify_workspace_size(B, N, V) -> int:
 
 def jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax=None, workspace=None,
                    dev_err=None, stream=None) -> None:
+    _verify_call(logits, draft, parent, None, accept_len, path, bonus, argmax, workspace,
+                 dev_err, stream)
+
+
+def jf_tree_verify_ragged(logits, draft, parent, tree_len, accept_len, path, bonus, argmax=None,
+                          workspace=None, dev_err=None, stream=None) -> None:
+    """Per-sequence tree sizes: nodes i >= tree_len[b] are never accepted."""
+    _need(tree_len, "tree_len", torch.int32, (logits.shape[0],))
+    _verify_call(logits, draft, parent, tree_len, accept_len, path, bonus, argmax, workspace,
+                 dev_err, stream)
+
+
+def _verify_call(logits, draft, parent, tree_len, accept_len, path, bonus, argmax, workspace,
+                 dev_err, stream) -> None:
     B, N, V = logits.shape
     if logits.dtype == torch.bfloat16:
         dt = JF_DTYPE_BF16
@@ -188,9 +248,16 @@ def jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax=None, 
     ws_bytes = 0
     if workspace is not None:
         ws_bytes = workspace.numel() * workspace.element_size()
-    _check("jf_tree_verify", _lib.jf_tree_verify(
-        _ptr(logits), dt, _ptr(draft), _ptr(parent), B, N, V, _ptr(argmax), _ptr(accept_len),
-        _ptr(path), _ptr(bonus), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)))
+    if tree_len is None:
+        _check("jf_tree_verify", _lib.jf_tree_verify(
+            _ptr(logits), dt, _ptr(draft), _ptr(parent), B, N, V, _ptr(argmax),
+            _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(workspace), ws_bytes, _ptr(dev_err),
+            _stream(stream)))
+    else:
+        _check("jf_tree_verify_ragged", _lib.jf_tree_verify_ragged(
+            _ptr(logits), dt, _ptr(draft), _ptr(parent), _ptr(tree_len), B, N, V, _ptr(argmax),
+            _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(workspace), ws_bytes, _ptr(dev_err),
+            _stream(stream)))
 
 
 def jf_tree_verify_static(logits, draft, parent, accept_len, path, bonus, argmax=None,
@@ -270,18 +337,22 @@ def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
     return torch.empty((nbytes + 15) // 16 * 16, dtype=torch.uint8, device=device)
 
 
-def build_tree_mask(parent: torch.Tensor, prefix_len: torch.Tensor, dev_err=None, stream=None):
+def build_tree_mask(parent: torch.Tensor, prefix_len: torch.Tensor, dev_err=None, stream=None,
+                    tree_len=None):
     B, N = parent.shape
     W = (N + 63) // 64
     mask = torch.empty((B, N, W), dtype=torch.int64, device=parent.device)
     depth = torch.empty((B, N), dtype=torch.int32, device=parent.device)
     pos = torch.empty((B, N), dtype=torch.int32, device=parent.device)
-    jf_build_tree_mask(parent, prefix_len, mask, depth, pos, dev_err, stream)
+    if tree_len is None:
+        jf_build_tree_mask(parent, prefix_len, mask, depth, pos, dev_err, stream)
+    else:
+        jf_build_tree_mask_ragged(parent, prefix_len, tree_len, mask, depth, pos, dev_err, stream)
     return mask, depth, pos
 
 
 def tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale=None,
-                   with_lse=False, dev_err=None, stream=None):
+                   with_lse=False, dev_err=None, stream=None, tree_len=None):
     B, N, Hq, D = q.shape
     Hkv = k_cache.shape[2]
     if scale is None:
@@ -290,12 +361,16 @@ def tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale=Non
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if with_lse else None
     ws = _workspace(jf_tree_attention_workspace_size(B, N, Hq, Hkv, D, block_table.shape[1],
                                                      k_cache.shape[1]), q.device)
-    jf_tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale, out, lse, ws,
-                      dev_err, stream)
+    if tree_len is None:
+        jf_tree_attention(q, k_cache, v_cache, block_table, prefix_len, mask, scale, out, lse, ws,
+                          dev_err, stream)
+    else:
+        jf_tree_attention_ragged(q, k_cache, v_cache, block_table, prefix_len, tree_len, mask,
+                                 scale, out, lse, ws, dev_err, stream)
     return (out, lse) if with_lse else out
 
 
-def tree_verify(logits, draft, parent, dev_err=None, stream=None):
+def tree_verify(logits, draft, parent, dev_err=None, stream=None, tree_len=None):
     B, N, V = logits.shape
     dev = logits.device
     argmax = torch.empty((B, N), dtype=torch.int32, device=dev)
@@ -303,7 +378,11 @@ def tree_verify(logits, draft, parent, dev_err=None, stream=None):
     path = torch.empty((B, N), dtype=torch.int32, device=dev)
     bonus = torch.empty((B,), dtype=torch.int32, device=dev)
     ws = _workspace(jf_tree_verify_workspace_size(B, N, V), dev)
-    jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax, ws, dev_err, stream)
+    if tree_len is None:
+        jf_tree_verify(logits, draft, parent, accept_len, path, bonus, argmax, ws, dev_err, stream)
+    else:
+        jf_tree_verify_ragged(logits, draft, parent, tree_len, accept_len, path, bonus, argmax, ws,
+                              dev_err, stream)
     return argmax, accept_len, path, bonus
 
 
