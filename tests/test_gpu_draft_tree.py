@@ -71,6 +71,23 @@ def test_equal_logits_and_scores_tie_break(jf):
     check(jf, x, "f32", 6, 150)
 
 
+@pytest.mark.parametrize("B,N", [(20, 64), (8, 256)])
+def test_many_rows_bf16(jf, B, N):
+    """16 depths for 20 (8) sequences: 320 (128) logit rows, so rows run one CTA each
+    (three CTAs per row) instead of eight-CTA clusters."""
+    check(jf, wl.draft_logits(B, 16, 151936, seed=9 + B), "bf16", 8, N)
+
+
+@pytest.mark.parametrize("B,Dmax,V", [(2, 4, 20000), (20, 16, 3000)])
+def test_two_valued_logits_overflow_the_filter(jf, B, Dmax, V):
+    """Logits in {0, 1}: about half of every slice ties at the threshold, more than the
+    candidate buffer holds, so the exact per-warp ranking runs (in clusters and with one
+    CTA per row)."""
+    rng = np.random.default_rng(B * 100 + V)
+    x = rng.integers(0, 2, size=(B, Dmax, V)).astype(np.float32)
+    check(jf, x, "f32", 8, 30)
+
+
 def test_lattice_smaller_than_budget_is_rejected(jf):
     x = torch.zeros((1, 2, 10), dtype=torch.float32, device="cuda")
     with pytest.raises(RuntimeError):

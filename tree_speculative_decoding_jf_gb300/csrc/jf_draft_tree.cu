@@ -21,6 +21,7 @@
 // memory.  A node is identified by its rank path packed into a
 // 64-bit code (4 bits per level, first level in the top bits), so its parent's code is
 // its own with the last digit cleared.
+#include <algorithm>
 #include <cmath>
 
 #include "jf_common.cuh"
@@ -35,17 +36,14 @@ constexpr int kMaxK = 8;
 constexpr int kMaxDepth = 16;
 constexpr int kMaxTreeN = 256;
 constexpr int kSortCap = 4096;            // >= N + N * K, a power of two
-constexpr int kRowParts = 8;             // CTAs (one cluster) per logit row
+constexpr int kRowParts = 8;             // most CTAs (one cluster) per logit row
+constexpr int kCandCap = 1024;           // filtered candidates a CTA keeps in shared memory
 
 // ---------------------------------------------------------------- kernel 1: candidates
 struct Cand {
   float v;
   int i;
 };
-// a precedes b: larger value, then lower index
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-  return a.v > b.v || (a.v == b.v && a.i < b.i);
-}
 
 template <typename T>
 __device__ __forceinline__ float load_logit(const T* p, long long i);
@@ -83,25 +81,42 @@ __device__ __forceinline__ void warp_offer(float v, int i, bool valid, Cand& wl,
   }
 }
 
+// State of one thread across the passes over its CTA's slice of a row.
+struct PassState {
+  float M;        // slice maximum (pass 2)
+  float tau;      // candidate threshold (pass 2)
+  float m;        // running maximum (pass 1)
+  float sum;      // running sum of exp(x - M) (pass 2)
+  Cand wl, thr;   // the warp's K-best list and its last entry (pass 3)
+  Cand* cand;     // shared candidate buffer (pass 2)
+  int* ncand;
+};
+
 // One pass over this CTA's slice of a row, warp-synchronously (every lane runs every
-// step; lanes past the slice offer nothing).  PASS 1 folds the maximum into m; PASS 2
-// adds exp(x - M) into sum and offers every logit to the warp's list.  The row is read as
-// 16-byte vectors, kUnroll per thread in flight, when it starts on a 16-byte boundary;
-// otherwise element by element.
+// step; lanes past the slice offer nothing).  PASS 1 folds the maximum into m.  PASS 2
+// adds exp(x - M) into sum and appends every logit >= tau to the shared candidate buffer.
+// PASS 3 (only when the buffer overflowed) offers every logit to the warp's K-best list.
+// The row is read as 16-byte vectors, kUnroll per thread in flight, when it starts on a
+// 16-byte boundary; otherwise element by element.
 template <int PASS>
-__device__ __forceinline__ void take(float v, int i, bool valid, float M, float& m, float& sum,
-                                     Cand& wl, Cand& thr) {
+__device__ __forceinline__ void take(float v, int i, bool valid, PassState& st) {
   if constexpr (PASS == 1) {
-    if (valid) m = fmaxf(m, v);
+    if (valid) st.m = fmaxf(st.m, v);
+  } else if constexpr (PASS == 2) {
+    if (valid) {
+      st.sum += __expf(v - st.M);
+      if (v >= st.tau) {
+        const int pos = atomicAdd(st.ncand, 1);
+        if (pos < kCandCap) st.cand[pos] = Cand{v, i};
+      }
+    }
   } else {
-    if (valid) sum += __expf(v - M);
-    warp_offer(v, i, valid, wl, thr);
+    warp_offer(v, i, valid, st.wl, st.thr);
   }
 }
 
 template <typename T, int PASS>
-__device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts, float M, float& m,
-                                         float& sum, Cand& wl, Cand& thr) {
+__device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts, PassState& st) {
   constexpr int kPer = 16 / sizeof(T);          // logits per vector
   constexpr int kUnroll = 8;
   const int lane0 = static_cast<int>(threadIdx.x) & ~31;   // first thread of this warp
@@ -132,7 +147,7 @@ __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts,
             val = __uint_as_float(((w[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu) << 16);
           else
             val = __uint_as_float(w[e]);
-          take<PASS>(val, v * kPer + e, valid, M, m, sum, wl, thr);
+          take<PASS>(val, v * kPer + e, valid, st);
         }
       }
     }
@@ -140,7 +155,7 @@ __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts,
       for (int b0 = nvec_all * kPer + lane0; b0 < V; b0 += blockDim.x) {
         const int i = b0 + (threadIdx.x & 31);
         const bool valid = i < V;
-        take<PASS>(valid ? load_logit<T>(x, i) : -INFINITY, i, valid, M, m, sum, wl, thr);
+        take<PASS>(valid ? load_logit<T>(x, i) : -INFINITY, i, valid, st);
       }
   } else {
     const int per = (V + parts - 1) / parts;
@@ -148,43 +163,110 @@ __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts,
     for (int b0 = ib + lane0; b0 < ie; b0 += blockDim.x) {
       const int i = b0 + (threadIdx.x & 31);
       const bool valid = i < ie;
-      take<PASS>(valid ? load_logit<T>(x, i) : -INFINITY, i, valid, M, m, sum, wl, thr);
+      take<PASS>(valid ? load_logit<T>(x, i) : -INFINITY, i, valid, st);
     }
   }
 }
 
-// A cluster of kRowParts CTAs shares one row; each makes two passes over its slice: the
-// slice maximum m_c, then s_c = sum of exp(x - m_c) together with the slice's K best
-// (per warp, then merged across the CTA's warps).  The cluster's first CTA merges the
-// slices through distributed shared memory: M = max m_c, S = sum s_c * exp(m_c - M),
-// lse = M + log S, and the K best of the slices' lists.
+// The k-th largest (k <= kMaxK) of one value per thread of the CTA, by repeated
+// extraction: each warp takes its k largest, then warp 0 takes the k largest of those.
+// Every thread of the CTA calls it; `scratch` holds kWarps * kMaxK floats.
+__device__ float block_kth_largest(float x, int k, float* scratch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  for (int r = 0; r < k; ++r) {
+    float b = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    const unsigned who = __ballot_sync(0xffffffffu, x == b);
+    if (lane == __ffs(who) - 1) x = -INFINITY;
+    if (lane == 0) scratch[warp * kMaxK + r] = b;
+  }
+  __syncthreads();
+  float kth = -INFINITY;
+  if (warp == 0) {
+    int head = 0;                                  // lane q < nwarps walks warp q's list
+    for (int r = 0; r < k; ++r) {
+      const float h = (lane < nwarps && head < k) ? scratch[lane * kMaxK + head] : -INFINITY;
+      float b = h;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+      const unsigned who = __ballot_sync(0xffffffffu, lane < nwarps && head < k && h == b);
+      if (lane == __ffs(who) - 1) ++head;
+      kth = b;
+    }
+    if (lane == 0) scratch[0] = kth;
+  }
+  __syncthreads();
+  kth = scratch[0];
+  __syncthreads();
+  return kth;
+}
+
+// A cluster of `parts` CTAs shares one row (parts <= kRowParts: the host splits rows only
+// as far as it takes to fill the GPU); each makes two passes over its slice: the
+// slice maximum m_c, then s_c = sum of exp(x - m_c) together with the slice's K best.
+// The K best are found by filtering: the K-th largest of the threads' pass-1 maxima is a
+// value at least K logits of the slice reach, so the slice's K best all lie at or above
+// it; pass 2 keeps only those logits (a few dozen for real logits) and one warp ranks
+// them.  When heavy ties push more than kCandCap logits over the threshold, a third pass
+// ranks the whole slice per warp instead (exact either way).  The cluster's first CTA
+// merges the slices through distributed shared memory: M = max m_c,
+// S = sum s_c * exp(m_c - M), lse = M + log S, and the K best of the slices' lists.
 template <typename T>
 __global__ void __launch_bounds__(kTopThreads)
-    draft_candidates_kernel(const T* __restrict__ logits, int V, int K,
+    draft_candidates_kernel(const T* __restrict__ logits, int V, int K, int parts,
                             int32_t* __restrict__ cand_token, float* __restrict__ cand_logp) {
   constexpr int kWarps = kTopThreads / 32;
   __shared__ Cand s_top[kWarps][kMaxK];
   __shared__ float s_red[kTopThreads];
   __shared__ float s_slice[2];                   // this slice's (max, sum)
+  __shared__ Cand s_cand[kCandCap];
+  __shared__ int s_ncand;
   grid_dependency_wait();
-  const long long row = blockIdx.x / kRowParts;
+  const long long row = blockIdx.x / parts;
   const int part = static_cast<int>(cluster_ctarank());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const T* x = logits + row * V;
-  Cand wl{-INFINITY, 0x7fffffff}, thr{-INFINITY, 0x7fffffff};
-  float m = -INFINITY, sum = 0.f;
-  row_pass<T, 1>(x, V, part, kRowParts, 0.f, m, sum, wl, thr);       // slice maximum
-  s_red[threadIdx.x] = m;
+  PassState st;
+  st.M = 0.f;
+  st.tau = INFINITY;
+  st.m = -INFINITY;
+  st.sum = 0.f;
+  st.wl = Cand{-INFINITY, 0x7fffffff};
+  st.thr = Cand{-INFINITY, 0x7fffffff};
+  st.cand = s_cand;
+  st.ncand = &s_ncand;
+  if (threadIdx.x == 0) s_ncand = 0;
+  row_pass<T, 1>(x, V, part, parts, st);                      // slice maximum
+  // threshold: the K-th largest thread maximum (-inf when the slice has fewer logits)
+  st.tau = block_kth_largest(st.m, K, s_red);
+  s_red[threadIdx.x] = st.m;
   __syncthreads();
   for (int w = blockDim.x / 2; w > 0; w >>= 1) {
     if (threadIdx.x < w) s_red[threadIdx.x] = fmaxf(s_red[threadIdx.x], s_red[threadIdx.x + w]);
     __syncthreads();
   }
   const float M = s_red[0];
+  st.M = M;
   __syncthreads();
-  if (M != -INFINITY) row_pass<T, 2>(x, V, part, kRowParts, M, m, sum, wl, thr);
-  if (lane < kMaxK) s_top[warp][lane] = wl;
-  s_red[threadIdx.x] = sum;
+  if (M != -INFINITY) row_pass<T, 2>(x, V, part, parts, st);
+  __syncthreads();
+  const int ncand = s_ncand;
+  if (ncand <= kCandCap) {
+    // rank the candidates in warp 0; the other warps' lists stay empty
+    if (warp == 0)
+      for (int j0 = 0; j0 < ncand; j0 += 32) {
+        const int j = j0 + lane;
+        const bool valid = j < ncand;
+        const Cand c = valid ? s_cand[j] : Cand{-INFINITY, 0x7fffffff};
+        warp_offer(c.v, c.i, valid, st.wl, st.thr);
+      }
+  } else if (M != -INFINITY) {
+    row_pass<T, 3>(x, V, part, parts, st);                    // every logit, per warp
+  }
+  if (lane < kMaxK) s_top[warp][lane] = st.wl;
+  s_red[threadIdx.x] = st.sum;
   __syncthreads();
   for (int w = blockDim.x / 2; w > 0; w >>= 1) {
     if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
@@ -216,10 +298,10 @@ __global__ void __launch_bounds__(kTopThreads)
   }
   cluster_sync();                                // every slice's result is in place
   if (part == 0 && warp == 0) {
-    // lane q < kRowParts fetches slice q's (max, sum) and K-best list
+    // lane q < parts fetches slice q's (max, sum) and K-best list
     float mq = -INFINITY, sq = 0.f;
     Cand lst[kMaxK];
-    if (lane < kRowParts) {
+    if (lane < parts) {
       mq = dsmem_ld_f32(dsmem_addr(&s_slice[0], lane));
       sq = dsmem_ld_f32(dsmem_addr(&s_slice[1], lane));
 #pragma unroll
@@ -438,16 +520,22 @@ extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype
   if (lattice < N) return JF_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * Dmax > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (static_cast<long long>(B) * Dmax * jf::kRowParts > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  // Rows are split over a cluster of `parts` CTAs only as far as it takes to give the GPU
+  // about two CTAs per SM: many rows run one CTA per row (no merge), few rows up to 8.
+  const int sms = jf::current_sm_count() > 0 ? jf::current_sm_count() : 148;
+  const long long rows = static_cast<long long>(B) * Dmax;
+  const int parts = static_cast<int>(std::min<long long>(
+      jf::kRowParts, std::max<long long>(1, (2LL * sms + rows - 1) / rows)));
+  if (rows * parts > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(static_cast<unsigned>(B * Dmax * jf::kRowParts));
+  lc.gridDim = dim3(static_cast<unsigned>(rows * parts));
   lc.blockDim = dim3(jf::kTopThreads);
   lc.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = jf::kRowParts;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(parts);
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
@@ -455,9 +543,11 @@ extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype
   cudaError_t e =
       dtype == JF_DTYPE_BF16
           ? cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<uint16_t>,
-                               static_cast<const uint16_t*>(draft_logits), V, K, cand_token, cand_logp)
+                               static_cast<const uint16_t*>(draft_logits), V, K, parts, cand_token,
+                               cand_logp)
           : cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<float>,
-                               static_cast<const float*>(draft_logits), V, K, cand_token, cand_logp);
+                               static_cast<const float*>(draft_logits), V, K, parts, cand_token,
+                               cand_logp);
   if (e != cudaSuccess) return JF_ERR_CUDA;
   constexpr size_t kTreeSmem = 2 * jf::kSortCap * sizeof(uint64_t);
   static bool attr_set[64] = {false};
