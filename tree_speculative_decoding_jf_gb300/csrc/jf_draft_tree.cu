@@ -360,24 +360,99 @@ __device__ __forceinline__ bool key_less(uint64_t ah, uint64_t al, uint64_t bh, 
   return ah < bh || (ah == bh && al < bl);
 }
 
-__device__ void bitonic_sort(uint64_t* hi, uint64_t* lo, int n) {   // n a power of two
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const int l = i ^ j;
-        if (l > i) {
-          const bool up = (i & k) == 0;
-          const bool sw = up ? key_less(hi[l], lo[l], hi[i], lo[i]) : key_less(hi[i], lo[i], hi[l], lo[l]);
-          if (sw) {
-            const uint64_t th = hi[i], tl = lo[i];
-            hi[i] = hi[l]; lo[i] = lo[l];
-            hi[l] = th; lo[l] = tl;
-          }
-        }
+// One compare-exchange of bitonic sorting network stage (k, j) seen from element i: keep
+// the smaller key when i is the pair's lower index in an ascending block (or the upper
+// index in a descending one), else the larger.
+__device__ __forceinline__ void cx_keep(uint64_t& h, uint64_t& l, uint64_t ph, uint64_t pl, int i,
+                                        int k, int j) {
+  const bool keep_min = ((i & k) == 0) == ((i & j) == 0);
+  const bool p_less = key_less(ph, pl, h, l);
+  if (keep_min ? p_less : !p_less && !(ph == h && pl == l)) {
+    h = ph;
+    l = pl;
+  }
+}
+
+// Stage (k, J) for partners inside one thread (J < E): compile-time register indices.
+template <int E, int J>
+__device__ __forceinline__ void reg_stage(uint64_t (&h)[E], uint64_t (&l)[E], int t, int k) {
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    if ((e ^ J) > e) {
+      const int pe = e ^ J;
+      const bool up = ((t * E + e) & k) == 0;
+      const bool sw = up ? key_less(h[pe], l[pe], h[e], l[e]) : key_less(h[e], l[e], h[pe], l[pe]);
+      if (sw) {
+        const uint64_t th = h[e], tl = l[e];
+        h[e] = h[pe]; l[e] = l[pe];
+        h[pe] = th; l[pe] = tl;
       }
-      __syncthreads();
     }
   }
+}
+
+// Bitonic sort of n = E * 1024 keys (or n <= 1024 with E = 1) held E per thread,
+// element i = thread * E + e.  Stages whose partner is in the same thread swap registers,
+// those in the same warp use shuffles, and only partners in other warps go through shared
+// memory (double-buffered, one barrier per stage); so a sort of 4096 keys takes 15
+// barriers instead of 78.  Input and output in hi/lo; bhi/blo is scratch of n keys.
+// Every thread of the block calls it.
+template <int E>
+__device__ __forceinline__ void bitonic_sort_e(uint64_t* hi, uint64_t* lo, uint64_t* bhi,
+                                               uint64_t* blo, int n) {
+  const int t = threadIdx.x;
+  uint64_t h[E], l[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = t * E + e;
+    h[e] = i < n ? hi[i] : ~0ull;
+    l[e] = i < n ? lo[i] : ~0ull;
+  }
+  int buf = 0;
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < E) {                                   // partner in this thread
+        if (j == 1) reg_stage<E, 1>(h, l, t, k);
+        else if constexpr (E > 2) reg_stage<E, 2>(h, l, t, k);
+      } else if (j < 32 * E) {                       // partner in this warp
+        const int lm = j / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const uint64_t ph = __shfl_xor_sync(0xffffffffu, h[e], lm);
+          const uint64_t pl = __shfl_xor_sync(0xffffffffu, l[e], lm);
+          cx_keep(h[e], l[e], ph, pl, t * E + e, k, j);
+        }
+      } else {                                       // partner in another warp
+        uint64_t* sh = buf ? bhi : hi;
+        uint64_t* sl = buf ? blo : lo;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = t * E + e;
+          if (i < n) { sh[i] = h[e]; sl[i] = l[e]; }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = t * E + e;
+          if (i < n) cx_keep(h[e], l[e], sh[i ^ j], sl[i ^ j], i, k, j);
+        }
+        buf ^= 1;
+      }
+    }
+  }
+  __syncthreads();                                   // every shared-memory read is done
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = t * E + e;
+    if (i < n) { hi[i] = h[e]; lo[i] = l[e]; }
+  }
+  __syncthreads();
+}
+
+__device__ void bitonic_sort(uint64_t* hi, uint64_t* lo, uint64_t* bhi, uint64_t* blo, int n) {
+  if (n <= kTreeThreads) bitonic_sort_e<1>(hi, lo, bhi, blo, n);
+  else if (n <= 2 * kTreeThreads) bitonic_sort_e<2>(hi, lo, bhi, blo, n);
+  else bitonic_sort_e<4>(hi, lo, bhi, blo, n);
 }
 
 __global__ void __launch_bounds__(kTreeThreads)
@@ -385,9 +460,11 @@ __global__ void __launch_bounds__(kTreeThreads)
                            const int32_t* __restrict__ root_token, int Dmax, int K, int N,
                            int32_t* __restrict__ parent, int32_t* __restrict__ draft,
                            int32_t* __restrict__ depth_out, float* __restrict__ score_out) {
-  extern __shared__ uint64_t s_keys[];     // [kSortCap] hi, then [kSortCap] lo
+  extern __shared__ uint64_t s_keys[];     // [kSortCap] hi, [kSortCap] lo, then the sort's scratch
   uint64_t* s_hi = s_keys;
   uint64_t* s_lo = s_keys + kSortCap;
+  uint64_t* s_bhi = s_keys + 2 * kSortCap;
+  uint64_t* s_blo = s_keys + 3 * kSortCap;
   __shared__ float s_lp[kMaxDepth * kMaxK];
   __shared__ int s_tok[kMaxDepth * kMaxK];
   __shared__ int s_cnt[kMaxTreeN];
@@ -458,7 +535,7 @@ __global__ void __launch_bounds__(kTreeThreads)
       s_lo[e] = ~0ull;
     }
     __syncthreads();
-    bitonic_sort(s_hi, s_lo, n);
+    bitonic_sort(s_hi, s_lo, s_bhi, s_blo, n);
     // keep the best N; stop once no level-d node made it (deeper ones cannot either)
     int kept_d = 0;
     for (int e = threadIdx.x; e < min(N, nG + nC); e += blockDim.x)
@@ -549,7 +626,7 @@ extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype
                                static_cast<const float*>(draft_logits), V, K, parts, cand_token,
                                cand_logp);
   if (e != cudaSuccess) return JF_ERR_CUDA;
-  constexpr size_t kTreeSmem = 2 * jf::kSortCap * sizeof(uint64_t);
+  constexpr size_t kTreeSmem = 4 * jf::kSortCap * sizeof(uint64_t);
   static bool attr_set[64] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
