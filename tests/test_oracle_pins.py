@@ -332,6 +332,28 @@ def test_attention_rows_sample_matches_full():
         assert l[n] == lse[rb[n], rh[n], ri[n]]
 
 
+def test_ragged_reading_node_rows_depend_only_on_earlier_nodes():
+    """Ragged trees are read as each sequence's first n_b nodes.  That reading is sound
+    because a node's mask row and attention row involve only itself and earlier nodes
+    (ancestors have smaller ids): the fixed-size problem restricted to rows i < n equals
+    the problem built from the first n nodes, bit for bit."""
+    import dataclasses
+    w = tiny(B=2, N=9, P=21, Hq=4, Hkv=2, D=8, seed=12)
+    full_o, full_l = oracle.tree_attention(w)
+    full_m, full_d, full_p = oracle.tree_mask(w.parent, w.prefix_len)
+    for b in range(w.B):
+        for n in (1, 4, 9):
+            ws = dataclasses.replace(w, B=1, N=n, prefix_len=w.prefix_len[b:b + 1].copy(),
+                                     parent=w.parent[b:b + 1, :n].copy(),
+                                     q=w.q[b:b + 1, :n].copy(),
+                                     block_table=w.block_table[b:b + 1].copy())
+            o, l = oracle.tree_attention(ws)
+            assert (o[0] == full_o[b, :n]).all() and (l[0] == full_l[b, :, :n]).all()
+            m, d, p = oracle.tree_mask(ws.parent, ws.prefix_len)
+            assert (m[0, :, 0] == full_m[b, :n, 0]).all()
+            assert (d[0] == full_d[b, :n]).all() and (p[0] == full_p[b, :n]).all()
+
+
 # ----------------------------------------------------------------------------- verify
 
 def _golden_argmax_rows():
