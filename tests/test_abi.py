@@ -76,3 +76,29 @@ def test_host_argument_validation_needs_no_gpu(lib):
                               1 << 20, None, None) == 1      # bad dtype
     assert lib.jf_tree_verify(fake, 0, fake, fake, 1, 4, 10, None, fake, fake, fake, None,
                               1 << 20, None, None) == 1      # missing workspace
+
+
+def test_ragged_calls_validate_host_arguments_without_gpu(lib):
+    """The ragged entry points need tree_len and share the fixed-size checks."""
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails early
+    lib.jf_build_tree_mask_ragged.argtypes = [P, P, P, i32, i32, P, P, P, P, P]
+    assert lib.jf_build_tree_mask_ragged(fake, fake, None, 1, 4, fake, None, None, None, None) == 1
+    assert lib.jf_build_tree_mask_ragged(fake, fake, fake, 1, 5000, fake, None, None, None,
+                                         None) == 3
+    lib.jf_tree_attention_ragged.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                             i32, i32, ctypes.c_float, P, P, P, ctypes.c_size_t,
+                                             P, P]
+    args = [fake] * 7 + [1, 16, 32, 8, 128, 16, 10, 10, 0.088, fake, None, None, 0, None, None]
+    no_len = list(args); no_len[5] = None
+    assert lib.jf_tree_attention_ragged(*no_len) == 1
+    bad_d = list(args); bad_d[11] = 96
+    assert lib.jf_tree_attention_ragged(*bad_d) == 3
+    mis = list(args); mis[0] = ctypes.c_void_p(0x10008)
+    assert lib.jf_tree_attention_ragged(*mis) == 7
+    lib.jf_tree_verify_ragged.argtypes = [P, i32, P, P, P, i32, i32, i32, P, P, P, P, P,
+                                          ctypes.c_size_t, P, P]
+    assert lib.jf_tree_verify_ragged(fake, 0, fake, fake, None, 1, 4, 10, None, fake, fake, fake,
+                                     fake, 1 << 20, None, None) == 1     # no tree_len
+    assert lib.jf_tree_verify_ragged(fake, 7, fake, fake, fake, 1, 4, 10, None, fake, fake, fake,
+                                     fake, 1 << 20, None, None) == 1     # bad dtype
