@@ -118,7 +118,7 @@ __device__ __forceinline__ void take(float v, int i, bool valid, PassState& st) 
 template <typename T, int PASS>
 __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts, PassState& st) {
   constexpr int kPer = 16 / sizeof(T);          // logits per vector
-  constexpr int kUnroll = 8;
+  constexpr int kUnroll = 4;
   const int lane0 = static_cast<int>(threadIdx.x) & ~31;   // first thread of this warp
   if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0u) {
     const uint4* xv = reinterpret_cast<const uint4*>(x);
