@@ -1,9 +1,25 @@
 """GPU parity for best-first draft-tree construction (jf_build_draft_tree through the C ABI).
 
-Candidates: tokens bit-exact against the fp64 oracle, log-probabilities within 5e-5
-(the kernel's log-sum-exp is fp32).  Tree: the expansion decides integers (node order,
-parents) from fp32 scores, so the oracle expands the kernel's own fp32 candidate
-log-probabilities in fp32, and parent, draft, depth and score must match exactly."""
+Everything expected comes from the fp64 oracle run on the logits alone: no value the
+kernel produced is fed back into the oracle.
+
+Candidates: tokens bit-exact, log-probabilities within 5e-5 of fp64 (the kernel's
+log-sum-exp is fp32).  Tree: the kernel orders nodes by fp32 cumulative scores, the
+oracle by fp64 ones, so two nodes whose exact scores lie within the scores' error bound
+may legitimately come out in either order.  The test therefore
+  - checks that the GPU tree is well formed (parents earlier, depths, each node's token
+    is the candidate of its rank at its depth, no rank path twice),
+  - recomputes every GPU node's exact score from its rank path and the oracle's fp64
+    log-probs, and checks the GPU's score against it,
+  - checks that the GPU's node order and node set are best-first under the exact scores
+    up to swaps of nodes closer than the error bound,
+  - cuts the oracle's ranking into near-tie clusters (runs of consecutive exact scores
+    within the bound) and requires the GPU to hold exactly the oracle's nodes at each
+    cluster's positions, in any order, and at the cluster that straddles the budget only
+    nodes of that cluster; where a cluster's scores are exactly equal in fp64 and in the
+    kernel's fp32, the tie rule (depth, then rank path) must give the GPU's order.
+Score error bound per node: 6e-5 x depth (each candidate log-prob within 5e-5, plus fp32
+rounding of a running sum of at most 16 terms of magnitude below 100)."""
 import numpy as np
 import pytest
 import torch
@@ -13,6 +29,7 @@ from tree_speculative_decoding_jf_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 LOGP_ATOL = 5e-5
+SCORE_TOL_PER_DEPTH = 6e-5
 
 
 @pytest.fixture(scope="module")
@@ -36,27 +53,97 @@ def run(jf, logits_np, dtype, K, N, roots):
     return ([x.cpu().numpy() for x in (parent, draft, depth, score, ctok, clp)], ref_in)
 
 
-def check(jf, logits_np, dtype, K, N):
+def tol(d):
+    return SCORE_TOL_PER_DEPTH * max(int(d), 1)
+
+
+def gpu_rank_paths(parent, draft, depth, rtok, root):
+    """Rank path of every GPU node, rebuilt from its parent and token against the oracle's
+    candidate lists; asserts the tree is well formed on the way."""
+    N = len(parent)
+    assert parent[0] == -1 and depth[0] == 0 and draft[0] == root
+    paths = [()]
+    for i in range(1, N):
+        p = int(parent[i])
+        assert 0 <= p < i, f"node {i}: parent {p}"
+        assert depth[i] == depth[p] + 1 and depth[i] <= rtok.shape[0]
+        hits = np.flatnonzero(rtok[depth[i] - 1] == draft[i])
+        assert len(hits) == 1, f"node {i}: token {draft[i]} is not a depth-{depth[i]} candidate"
+        paths.append(paths[p] + (int(hits[0]),))
+    assert len(set(paths)) == N, "a rank path occurs twice"
+    return paths
+
+
+def check_tree(parent, draft, depth, score, rtok, rlp, N, root):
+    """Returns the number of positions pinned to the oracle's tree (see the module doc)."""
+    Dmax, K = rtok.shape
+    paths = gpu_rank_paths(parent, draft, depth, rtok, root)
+    exact = np.array([odt.path_score(rlp, p) for p in paths])
+    err = np.abs(score.astype(np.float64) - exact)
+    assert all(err[i] <= tol(depth[i]) for i in range(N)), f"score error {err.max():.2e}"
+    # order: best-first up to near-ties
+    for i in range(1, N - 1):
+        assert exact[i] >= exact[i + 1] - tol(depth[i]) - tol(depth[i + 1]), f"order at {i}"
+    # set: no frontier node beats a chosen one by more than the bound
+    chosen = set(paths)
+    front = [p + (r,) for p in paths if len(p) < Dmax for r in range(K) if p + (r,) not in chosen]
+    if front and N > 1:
+        fs = np.array([odt.path_score(rlp, p) for p in front])
+        fb = int(fs.argmax())
+        worst = int(np.argmin(exact[1:])) + 1
+        assert fs[fb] <= exact[worst] + tol(len(front[fb])) + tol(depth[worst]), "not best-first"
+    # Near-tie clusters of the oracle's ranking (consecutive exact scores within the bound),
+    # taken past the budget until the cluster at the boundary is complete.
+    extra = 64
+    while True:
+        _, _, rdep, rs, rpaths = odt.best_first_tree(rtok, rlp, N + extra, root_token=root)
+        near = [rs[i] - rs[i + 1] <= tol(rdep[i]) + tol(rdep[i + 1]) for i in range(len(rs) - 1)]
+        j = N - 1
+        while j < len(near) and near[j]:
+            j += 1
+        if j < len(near) or len(rs) < N + extra:
+            break
+        extra *= 2
+    assert paths[0] == rpaths[0] == ()
+    pinned, a = 1, 1
+    while a < N:
+        b = a + 1
+        while b < len(rs) and near[b - 1]:
+            b += 1
+        if b <= N:       # a cluster inside the budget: the same nodes, in any order
+            assert set(paths[a:b]) == set(rpaths[a:b]), f"positions {a}..{b - 1} hold other nodes"
+            pinned += b - a
+            # exactly tied in fp64 and in the kernel's fp32: the tie rule decides the order
+            if b - a > 1 and len(set(rs[a:b])) == 1 and len(set(score[a:b].tolist())) == 1:
+                keys = [(len(p), p) for p in paths[a:b]]
+                assert keys == sorted(keys), f"tie order at {a}..{b - 1}"
+        else:            # the cluster at the budget boundary: any of its nodes may be chosen
+            assert set(paths[a:N]) <= set(rpaths[a:b]), f"positions {a}..{N - 1} outside the boundary cluster"
+        a = b
+    return pinned
+
+
+def check(jf, logits_np, dtype, K, N, min_pinned=0.0):
     B = logits_np.shape[0]
     roots = list(range(100, 100 + B))
     (parent, draft, depth, score, ctok, clp), ref_in = run(jf, logits_np, dtype, K, N, roots)
     rtok, rlp = odt.candidates(ref_in, K)
     assert (ctok == rtok).all(), "candidate tokens differ"
     assert np.abs(clp.astype(np.float64) - rlp).max() <= LOGP_ATOL
+    pinned = 0
     for b in range(B):
-        rp, rd, rdep, rs = odt.best_first_tree(ctok[b], clp[b], N, root_token=roots[b])
-        assert (parent[b] == rp).all() and (draft[b] == rd).all()
-        assert (depth[b] == rdep).all() and (score[b] == rs).all()
+        pinned += check_tree(parent[b], draft[b], depth[b], score[b], rtok[b], rlp[b], N, roots[b])
+    assert pinned >= min_pinned * B * N, f"only {pinned} of {B * N} positions pinned exactly"
 
 
 def test_budget_256_vocab_151936_bf16(jf):
-    check(jf, wl.draft_logits(2, 16, 151936, seed=1), "bf16", 8, 256)
+    check(jf, wl.draft_logits(2, 16, 151936, seed=1), "bf16", 8, 256, min_pinned=0.8)
 
 
 @pytest.mark.parametrize("B,Dmax,V,K,N,seed", [(3, 5, 1000, 4, 60, 2), (2, 16, 4096, 8, 200, 3),
                                                (1, 9, 333, 3, 100, 4)])
 def test_shapes_fp32(jf, B, Dmax, V, K, N, seed):
-    check(jf, wl.draft_logits(B, Dmax, V, dtype="f32", seed=seed), "f32", K, N)
+    check(jf, wl.draft_logits(B, Dmax, V, dtype="f32", seed=seed), "f32", K, N, min_pinned=0.8)
 
 
 def test_chain_and_star(jf):
@@ -75,7 +162,7 @@ def test_equal_logits_and_scores_tie_break(jf):
 def test_many_rows_bf16(jf, B, N):
     """16 depths for 20 (8) sequences: 320 (128) logit rows, so rows run one CTA each
     (three CTAs per row) instead of eight-CTA clusters."""
-    check(jf, wl.draft_logits(B, 16, 151936, seed=9 + B), "bf16", 8, N)
+    check(jf, wl.draft_logits(B, 16, 151936, seed=9 + B), "bf16", 8, N, min_pinned=0.8)
 
 
 @pytest.mark.parametrize("B,Dmax,V", [(2, 4, 20000), (20, 16, 3000)])

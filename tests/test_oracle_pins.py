@@ -602,26 +602,25 @@ def test_draft_candidates_ties_take_lower_ids():
 
 
 def _lattice_brute_force(ct, lp, N, root):
-    """Every node of the lattice (rank paths up to Dmax), scored in fp32 from the root,
+    """Every node of the lattice (rank paths up to Dmax), scored in fp64 from the root,
     sorted by (score desc, depth, rank path); the first N with parents looked up by path."""
     Dmax, K = ct.shape
-    lp32 = lp.astype(np.float32)
-    nodes = [((), np.float32(0.0))]
-    frontier = [((), np.float32(0.0))]
+    nodes = [((), 0.0)]
+    frontier = [((), 0.0)]
     for d in range(Dmax):
         nxt = []
         for path, s in frontier:
             for r in range(K):
-                nxt.append((path + (r,), np.float32(s + lp32[d, r])))
+                nxt.append((path + (r,), s + float(lp[d, r])))
         nodes += nxt
         frontier = nxt
-    nodes.sort(key=lambda n: (-float(n[1]), len(n[0]), n[0]))
+    nodes.sort(key=lambda n: (-n[1], len(n[0]), n[0]))
     top = nodes[:N]
     index = {path: i for i, (path, _) in enumerate(top)}
     parent = [index.get(p[:-1], -2) if p else -1 for p, _ in top]
     draft = [root if not p else int(ct[len(p) - 1, p[-1]]) for p, _ in top]
     return (np.array(parent), np.array(draft), np.array([len(p) for p, _ in top]),
-            np.array([s for _, s in top], np.float32))
+            np.array([s for _, s in top], np.float64), [p for p, _ in top])
 
 
 @pytest.mark.parametrize("K,Dmax,N,seed", [(2, 4, 20, 0), (3, 3, 30, 1), (4, 3, 40, 2),
@@ -632,14 +631,30 @@ def test_best_first_matches_lattice_brute_force(K, Dmax, N, seed):
     lp = np.sort(rng.standard_normal((Dmax, K)) * 2 - 3, axis=1)[:, ::-1].copy()
     got = odt.best_first_tree(ct, lp, N, root_token=77)
     ref = _lattice_brute_force(ct, lp, N, 77)
-    for g, r in zip(got, ref):
+    for g, r in zip(got[:4], ref[:4]):
         assert (np.asarray(g) == np.asarray(r)).all()
+    assert got[4] == ref[4]
+    for path, s in zip(got[4], got[3]):
+        assert odt.path_score(lp, path) == s
+
+
+def test_best_first_scores_are_exact_sums():
+    """Two depth-2 branches whose cumulative log-probs differ by 1e-12 (equal in fp32):
+    the exact (fp64) sum orders them, (1, 0) before (0, 1), although a tie would put the
+    smaller rank path first."""
+    ct = np.array([[1, 2], [3, 4]])
+    lp = np.array([[-1.0, -1.0 - 1e-12], [-3.0, -3.0 - 2e-12]])
+    parent, draft, depth, score, paths = odt.best_first_tree(ct, lp, 6, root_token=0)
+    assert paths == [(), (0,), (1,), (0, 0), (1, 0), (0, 1)]
+    assert parent.tolist() == [-1, 0, 0, 1, 2, 1]
+    assert draft.tolist() == [0, 1, 2, 3, 3, 4]
+    assert np.float32(score[4]) == np.float32(score[5]) and score[4] > score[5]
 
 
 def test_best_first_equal_scores_prefer_shallow_then_small_rank():
     ct = np.array([[10, 11], [20, 21]])
     lp = np.zeros((2, 2))                      # every node scores 0: pure tie-breaking
-    parent, draft, depth, _ = odt.best_first_tree(ct, lp, 7, root_token=5)
+    parent, draft, depth, _, _ = odt.best_first_tree(ct, lp, 7, root_token=5)
     assert depth.tolist() == [0, 1, 1, 2, 2, 2, 2]
     assert draft.tolist() == [5, 10, 11, 20, 21, 20, 21]
     assert parent.tolist() == [-1, 0, 0, 1, 1, 2, 2]
@@ -648,7 +663,7 @@ def test_best_first_equal_scores_prefer_shallow_then_small_rank():
 def test_best_first_invariants_random():
     x = wl.bf16_bits_to_f32(wl.draft_logits(1, 16, 2000, seed=7))[0]
     tok, lp = odt.candidates(x[None], 8)
-    parent, draft, depth, score = odt.best_first_tree(tok[0], lp[0], 256, root_token=3)
+    parent, draft, depth, score, _ = odt.best_first_tree(tok[0], lp[0], 256, root_token=3)
     assert parent[0] == -1 and depth[0] == 0 and draft[0] == 3
     for i in range(1, 256):
         p = parent[i]
