@@ -298,6 +298,10 @@ SHAPES = [  # B, N, Hq, Hkv, D, P, tree
     (20, 128, 32, 4, 64, 300, "random"),     # 4 row-tile groups, 320 units: stream-K, D = 64
     (24, 64, 32, 4, 128, 90, "random"),      # 2 row-tile groups, 192 units: stream-K, D = 128
     (20, 40, 32, 4, 128, 3, "random"),       # stream-K over 1..6-tile pairs: many per range
+    (20, 40, 32, 4, 128, 0, "random"),       # the same with sequence 0 unprefixed: 1..7-key rows
+    (1, 12, 4, 1, 128, 0, "random"),         # no prefix, G = 4: rows of 1..7 keys (depth <= 6)
+    (2, 24, 8, 1, 128, 0, "random"),         # no prefix in sequence 0, G = 8
+    (3, 9, 8, 2, 64, 0, "chain"),            # no prefix, chain: row i sees i + 1 keys, D = 64
 ]
 
 
@@ -317,6 +321,23 @@ def test_attention_shapes_full_oracle(jf, shape):
     nrows = B * N * Hq
     rows = oracle.all_rows(w) if nrows <= 8192 else sample_rows(w, 2048)
     assert_attention_close(w, out, lse, rows)
+
+
+@pytest.mark.parametrize("dispatch", ["stream_k", "splits"])
+def test_attention_tiny_prefixes_full_oracle(jf, dispatch):
+    """Prefixes of 0, 1 and 2 keys: rows see only a handful of keys, so the rounding of the
+    probabilities does not average out.  Every row against the fp64 oracle.  20 sequences of
+    40 nodes at G = 8 take the stream-K dispatch, 2 sequences the key-split one."""
+    B = 20 if dispatch == "stream_k" else 2
+    rng = np.random.default_rng(B)
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - 3), i) for i in range(1, 40)],
+                                np.int32) for _ in range(B)])
+    prefix = np.array([b % 3 for b in range(B)], np.int32)
+    w = wl.make_workload("tiny", B, 40, 32, 4, 128, 64, prefix, tree="chain", parent=parent,
+                         permute_pages=True, seed=77 + B, with_logits=False)
+    out, lse, err = gpu_attention(jf, w)
+    assert err == 0
+    assert_attention_close(w, out, lse, oracle.all_rows(w) if B <= 2 else sample_rows(w, 6000))
 
 
 def test_attention_single_root_without_prefix_is_v_root(jf):

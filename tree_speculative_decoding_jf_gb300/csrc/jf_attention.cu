@@ -146,28 +146,6 @@ __device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
   return r != 0;
 }
 
-// 2^x on the FMA pipe, to take part of the exponentials off the MUFU unit (the
-// softmax issues one exponential per score; at D = 128 the MUFU rate is as low as the
-// tensor rate).  Cody-Waite style reduction x = n + f with n = round(x), f in
-// [-0.5, 0.5] (the 1.5 * 2^23 shifter leaves n in the low mantissa bits), then a
-// degree-3 polynomial for 2^f fitted by iteratively reweighted least squares to a
-// near-minimax relative error of 7.5e-5 on [-0.5, 0.5] (below bf16's 3.9e-3), and n
-// added to the exponent field.  Inputs are finite scores; x is clamped at -126.
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -126.0f);
-  const float t = x + 12582912.0f;
-  const float f = x - (t - 12582912.0f);
-  float q = fmaf(f, 0.0551716685f, 0.2426111251f);
-  q = fmaf(q, f, 0.6932609677f);
-  q = fmaf(q, f, 0.9999280572f);
-  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
-}
-
-// One in kPolyEvery exponential pairs of an unmasked tile goes to the FMA pipe (0: none).
-constexpr int kPolyEvery = 0;
-constexpr int kPolyMod = kPolyEvery > 0 ? kPolyEvery : 1;
-constexpr bool kPolyPacked = true;   // paired (f32x2) evaluation of the same polynomial
-
 // Paired fp32 arithmetic (one instruction for two lanes of data) and a 3-input max.
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
   uint64_t r;
@@ -193,23 +171,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// exp2_poly on a pair of lanes with paired fp32 arithmetic: the same reduction and
-// polynomial, two results per instruction except for the clamp and the exponent add.
-__device__ __forceinline__ void exp2_poly2(float x0, float x1, float& p0, float& p1) {
-  const uint64_t x = f2(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
-  const uint64_t t = fadd2(x, f2(12582912.0f, 12582912.0f));
-  const uint64_t n = fadd2(t, f2(-12582912.0f, -12582912.0f));
-  const uint64_t f = ffma2(n, f2(-1.0f, -1.0f), x);
-  uint64_t q = ffma2(f, f2(0.0551716685f, 0.0551716685f), f2(0.2426111251f, 0.2426111251f));
-  q = ffma2(q, f, f2(0.6932609677f, 0.6932609677f));
-  q = ffma2(q, f, f2(0.9999280572f, 0.9999280572f));
-  float q0, q1, t0, t1;
-  f2_split(q, q0, q1);
-  f2_split(t, t0, t1);
-  p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
-  p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
-}
-
 // Bits [rel, rel + 32) of the 192-bit little-endian window w[0..3) (zero outside it).
 __device__ __forceinline__ uint32_t window_bits32(const uint64_t (&w)[3], int rel) {
   if (rel <= -32 || rel >= 192) return 0u;
@@ -232,6 +193,54 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
   tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
   tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&r[64]));
   tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+}
+
+// Probabilities of one 128-score row (log2 domain: p = 2^(s * sl2 - m)), written back to
+// the row's TMEM S columns as the bf16 A operand of the PV MMA: P in columns 0..63 (two
+// keys per 32-bit column).  With `split`, P is also stored as a second bf16 part
+// lo = bf16(p - bf16(p)) in columns 64..127 and the MMA issuer adds a PV MMA on it, so the
+// probabilities that reach the tensor cores carry a relative error of about 2^-17 instead
+// of bf16's 2^-9.  That matters on tiles that hold tree keys: a row with only a few
+// visible keys gets no averaging of the rounding errors, and the output of such a row can
+// be small where its values cancel.  Returns the fp32 row sum.
+__device__ __forceinline__ float row_probs(const float* sv, float sl2, float neg, bool split,
+                                           uint32_t tS) {
+  const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
+  uint64_t ls2[2] = {0ull, 0ull};       // paired partial row sums (0ull == {+0, +0})
+  if (split) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {        // quarters of 32 keys keep few registers live
+      uint32_t ph[16], pl[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int cc = 16 * h + c;
+        float x0, x1;
+        f2_split(ffma2(f2(sv[2 * cc], sv[2 * cc + 1]), sl2x2, negx2), x0, x1);
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        ls2[c & 1] = fadd2(ls2[c & 1], f2(p0, p1));
+        ph[c] = pack_bf16x2(p0, p1);
+        pl[c] = pack_bf16x2(p0 - __uint_as_float(ph[c] << 16), p1 - __uint_as_float(ph[c] & 0xFFFF0000u));
+      }
+      tmem_st16(tS + 16 * h, ph);
+      tmem_st16(tS + 64 + 16 * h, pl);
+    }
+  } else {
+    uint32_t pk[64];
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      float x0, x1;
+      f2_split(ffma2(f2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2), x0, x1);
+      const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+      ls2[c & 1] = fadd2(ls2[c & 1], f2(p0, p1));
+      pk[c] = pack_bf16x2(p0, p1);
+    }
+    tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+    tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+  }
+  float la, lb, lc, ld;
+  f2_split(ls2[0], la, lb);
+  f2_split(ls2[1], lc, ld);
+  return (la + lb) + (lc + ld);
 }
 
 // Split partials of one unit live in the shared memory of the cluster's CTAs: normalised
@@ -616,7 +625,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         mma_ss(d_tmem, da + off, db + off, idS, kk > 0 ? 1u : 0u);
       }
     };
-    auto issue_pv = [&](int t, int st, bool acc) {
+    // O_t (+)= P_t V; with `lo`, also O_t += P_lo V from the second bf16 part of P (columns
+    // 64..127 of the S region), issued before the next S MMA overwrites those columns.
+    auto issue_pv = [&](int t, int st, bool acc, bool lo) {
       const uint64_t db = dv + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
       const uint32_t d_tmem = tmem + C::kTmemO + t * 128;
       const uint32_t a_tmem = tmem + C::kTmemS + t * 128;
@@ -624,6 +635,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       for (int kk = 0; kk < kKeyTile / 16; ++kk)
         mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
                (acc || kk > 0) ? 1u : 0u);
+      if (lo) {
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile / 16; ++kk)
+          mma_ts(d_tmem, a_tmem + 64 + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO, 1u);
+      }
     };
     bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
     if (ok && lane == 0) {
@@ -658,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           for (int u = 0; u < NT; ++u)
             if (u != t && jn[u] <= j) last = false;
           tc_fence_after();
-          issue_pv(t, j % SV, j > 0);
+          issue_pv(t, j % SV, j > 0, (k0 + j + 1) * kKeyTile > P);
           if (j + 1 < T) {
             issue_s(t, (j + 1) % SK);
             mma_commit(&s_full[t]);
@@ -780,35 +796,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       if (raise) m_run = mt;
       const float corr = raise ? fast_exp2(m_old - m_run) : 1.f;   // 0 when m_old = -inf
       const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
-      uint32_t pk[64];
-      const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
-      uint64_t ls2[2] = {0ull, 0ull};       // paired partial row sums (0ull == {+0, +0})
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x0, x1;
-        f2_split(ffma2(f2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2), x0, x1);
-        float p0, p1;
-        if (!masked_tile && kPolyEvery > 0 && c % kPolyMod == kPolyMod - 1) {
-          if (kPolyPacked) {               // finite scores only (prefix tiles)
-            exp2_poly2(x0, x1, p0, p1);
-          } else {
-            p0 = exp2_poly(x0);
-            p1 = exp2_poly(x1);
-          }
-        } else {
-          p0 = fast_exp2(x0);
-          p1 = fast_exp2(x1);
-        }
-        ls2[c & 1] = fadd2(ls2[c & 1], f2(p0, p1));
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      float la, lb, lc, ld;
-      f2_split(ls2[0], la, lb);
-      f2_split(ls2[1], lc, ld);
-      const float ls = (la + lb) + (lc + ld);
-      l = l * corr + ls;
-      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      l = l * corr + row_probs(sv, sl2, neg, masked_tile, tS);
       // O holds PV of tiles < j (complete: s_full of tile j was committed after them).
       const bool need = raise && j > 0 && m_old != -INFINITY;
       if (__any_sync(0xffffffffu, need)) {
@@ -1078,6 +1066,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ int s_tails;                    // segments whose V tail is ready
+  __shared__ int s_lo[NT];                   // current key tile of row tile t holds tree keys
   __shared__ int s_pre[kLptMaxB + 1];
   volatile int* abort = &abort_flag;
   uint8_t* q_s = sm + C::kQOff;
@@ -1277,7 +1266,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         mma_ss(d_tmem, da + off, db + off, idS, kk > 0 ? 1u : 0u);
       }
     };
-    auto issue_pv = [&](int t, int st, bool acc) {
+    // O_t (+)= P_t V; with `lo`, also O_t += P_lo V from the second bf16 part of P (columns
+    // 64..127 of the S region), issued before the next S MMA overwrites those columns.
+    auto issue_pv = [&](int t, int st, bool acc, bool lo) {
       const uint64_t db = dv + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
       const uint32_t d_tmem = tmem + C::kTmemO + t * 128;
       const uint32_t a_tmem = tmem + C::kTmemS + t * 128;
@@ -1285,6 +1276,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       for (int kk = 0; kk < kKeyTile / 16; ++kk)
         mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
                (acc || kk > 0) ? 1u : 0u);
+      if (lo) {
+#pragma unroll
+        for (int kk = 0; kk < kKeyTile / 16; ++kk)
+          mma_ts(d_tmem, a_tmem + 64 + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO, 1u);
+      }
     };
     bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
     if (ok && lane == 0) {
@@ -1313,7 +1309,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           for (int u = 0; u < NT; ++u)
             if (u != t && jn[u] <= j) last = false;
           tc_fence_after();
-          issue_pv(t, j % SV, j > 0);
+          issue_pv(t, j % SV, j > 0, *reinterpret_cast<volatile int*>(&s_lo[t]) != 0);
           if (j + 1 < Wc) {
             issue_s(t, (j + 1) % SK);
             mma_commit(&s_full[t]);
@@ -1448,24 +1444,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         if (raise) m_run = mt;
         const float corr = raise ? fast_exp2(m_old - m_run) : 1.f;
         const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
-        uint32_t pk[64];
-        const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
-        uint64_t ls2[2] = {0ull, 0ull};
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float x0, x1;
-          f2_split(ffma2(f2(sv[2 * c], sv[2 * c + 1]), sl2x2, negx2), x0, x1);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          ls2[c & 1] = fadd2(ls2[c & 1], f2(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        float la, lb, lc, ld;
-        f2_split(ls2[0], la, lb);
-        f2_split(ls2[1], lc, ld);
-        const float ls = (la + lb) + (lc + ld);
-        l = l * corr + ls;
-        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        if (rl == 0) s_lo[t] = masked_tile ? 1 : 0;   // read by the MMA issuer after p_full
+        l = l * corr + row_probs(sv, sl2, neg, masked_tile, tS);
         // O holds PV of this segment's tiles < j (complete: s_full of tile jg followed them)
         const bool need = raise && j > 0 && m_old != -INFINITY;
         if (__any_sync(0xffffffffu, need)) {
