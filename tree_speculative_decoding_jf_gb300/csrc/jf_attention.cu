@@ -59,6 +59,10 @@ constexpr int kRowTile = 128;     // rows per tensor-core tile (TMEM lanes)
 constexpr int kPage = 16;
 constexpr int kPagesPerTile = kKeyTile / kPage;
 constexpr float kRescaleThreshold = 8.0f;               // log2 units
+// Sequences with fewer prefix keys than this store P as hi + lo bf16 parts on the key
+// tiles that hold tree keys (see row_probs); longer prefixes give every row at least this
+// many visible keys, over which the bf16 rounding of P averages out.
+constexpr int kSplitPrefix = 128;
 constexpr int kLptMaxB = 256;                           // longest-first dispatch up to this B
 
 // Step records: record i completes once step i - 1 (every row tile's PV of key tile i - 1
@@ -197,17 +201,17 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 
 // Probabilities of one 128-score row (log2 domain: p = 2^(s * sl2 - m)), written back to
 // the row's TMEM S columns as the bf16 A operand of the PV MMA: P in columns 0..63 (two
-// keys per 32-bit column).  With `split`, P is also stored as a second bf16 part
+// keys per 32-bit column).  With SPLIT, P is also stored as a second bf16 part
 // lo = bf16(p - bf16(p)) in columns 64..127 and the MMA issuer adds a PV MMA on it, so the
 // probabilities that reach the tensor cores carry a relative error of about 2^-17 instead
 // of bf16's 2^-9.  That matters on tiles that hold tree keys: a row with only a few
 // visible keys gets no averaging of the rounding errors, and the output of such a row can
 // be small where its values cancel.  Returns the fp32 row sum.
-__device__ __forceinline__ float row_probs(const float* sv, float sl2, float neg, bool split,
-                                           uint32_t tS) {
+template <bool SPLIT>
+__device__ __forceinline__ float row_probs(const float* sv, float sl2, float neg, uint32_t tS) {
   const uint64_t sl2x2 = f2(sl2, sl2), negx2 = f2(neg, neg);
   uint64_t ls2[2] = {0ull, 0ull};       // paired partial row sums (0ull == {+0, +0})
-  if (split) {
+  if constexpr (SPLIT) {
 #pragma unroll
     for (int h = 0; h < 4; ++h) {        // quarters of 32 keys keep few registers live
       uint32_t ph[16], pl[16];
@@ -241,6 +245,88 @@ __device__ __forceinline__ float row_probs(const float* sv, float sl2, float neg
   f2_split(ls2[0], la, lb);
   f2_split(ls2[1], lc, ld);
   return (la + lb) + (lc + ld);
+}
+
+// One key tile of the online softmax for the calling thread's score row (its TMEM lane):
+// waits for the tile's S, applies visibility, raises the running maximum when needed,
+// writes P back to TMEM, rescales O when the maximum moved, and arrives on p_full.
+// MASKED tiles reach positions >= P (tree keys, possibly keys past the sequence end): the
+// node's ancestor words are loaded before the wait.  SPLIT (only on masked tiles of
+// sequences with a prefix shorter than kSplitPrefix) stores P as hi + lo parts.  Prefix
+// tiles take the MASKED = false instantiation, whose loop carries none of that code.  With
+// a non-null lo_flag the writer thread records SPLIT there for the MMA issuer once the
+// tile's S has arrived.  Returns false if the wait gave up.
+template <bool MASKED, bool SPLIT, int D>
+__device__ __forceinline__ bool softmax_tile(uint64_t* s_full_bar, uint32_t parity,
+                                             volatile int* abort, uint64_t* p_full_bar,
+                                             uint32_t tS, uint32_t tO, const uint64_t* mrow,
+                                             bool valid, int W, int key0, int P, int L, float sl2,
+                                             bool not_first, volatile int* lo_flag, bool writer,
+                                             float& m_run, float& l) {
+  uint64_t mw[3] = {0ull, 0ull, 0ull};
+  const int w_lo = MASKED ? (max(key0 - P, 0) >> 6) : 0;
+  if constexpr (MASKED) {
+    if (valid) {
+#pragma unroll
+      for (int u = 0; u < 3; ++u)
+        if (w_lo + u < W) mw[u] = __ldg(reinterpret_cast<const unsigned long long*>(mrow) + w_lo + u);
+    }
+  }
+  if (!wait_warp(s_full_bar, parity, abort)) return false;
+  if (lo_flag != nullptr && writer) *lo_flag = SPLIT ? 1 : 0;
+  tc_fence_after();
+  uint32_t sr[128];
+  tmem_ld128(tS, sr);
+  float* sv = reinterpret_cast<float*>(sr);
+  if constexpr (MASKED) {
+    // Visibility of the tile's 128 keys as four 32-bit words: prefix keys always, tree key
+    // j iff bit j of the node's ancestor mask, nothing past the sequence end.
+    const int pre = min(max(P - key0, 0), kKeyTile);
+    const int end = min(max(L - key0, 0), kKeyTile);
+    uint32_t vis[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int c0 = 32 * w;
+      uint32_t m = window_bits32(mw, key0 + c0 - P - 64 * w_lo);
+      const int np = min(max(pre - c0, 0), 32);
+      const int ne = min(max(end - c0, 0), 32);
+      m |= np >= 32 ? 0xFFFFFFFFu : ((1u << np) - 1u);
+      m &= ne >= 32 ? 0xFFFFFFFFu : ((1u << ne) - 1u);
+      vis[w] = m;
+    }
+#pragma unroll
+    for (int c = 0; c < kKeyTile; ++c)
+      if (!((vis[c >> 5] >> (c & 31)) & 1u)) sv[c] = -INFINITY;
+  }
+  float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+  for (int c = 4; c < kKeyTile; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
+  const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+  const float mt = mx * sl2;
+  const bool raise = mt > m_run + kRescaleThreshold;
+  const float m_old = m_run;
+  if (raise) m_run = mt;
+  const float corr = raise ? fast_exp2(m_old - m_run) : 1.f;   // 0 when m_old = -inf
+  const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
+  l = l * corr + row_probs<SPLIT>(sv, sl2, neg, tS);
+  // O holds PV of the earlier tiles (complete: this tile's S was committed after them).
+  const bool need = raise && not_first && m_old != -INFINITY;
+  if (__any_sync(0xffffffffu, need)) {
+    const float f = need ? corr : 1.f;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + c * 32, o);
+      tmem_ld_wait(o);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+      tmem_st32(tO + c * 32, o);
+    }
+  }
+  tmem_st_wait();
+  tc_fence_before();
+  mbar_arrive(p_full_bar);
+  return true;
 }
 
 // Split partials of one unit live in the shared memory of the cluster's CTAs: normalised
@@ -331,6 +417,14 @@ __device__ __noinline__ void merge_cluster(uint8_t* sm, const MergeArgs p, int b
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
   cluster_sync();                                        // nobody leaves while others read it
+}
+
+// O += P_lo V from the second bf16 part of P (columns 64..127 of a row tile's S region).
+// Out of line: the MMA issuer's steady-state loop carries none of this code.
+__device__ __noinline__ void issue_pv_lo(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idO) {
+#pragma unroll
+  for (int kk = 0; kk < kKeyTile / 16; ++kk)
+    mma_ts(d_tmem, a_tmem + 64 + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO, 1u);
 }
 
 // Longest sequences first: with one CTA per unit and ragged prefixes, CTAs are handed to
@@ -635,11 +729,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       for (int kk = 0; kk < kKeyTile / 16; ++kk)
         mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
                (acc || kk > 0) ? 1u : 0u);
-      if (lo) {
-#pragma unroll
-        for (int kk = 0; kk < kKeyTile / 16; ++kk)
-          mma_ts(d_tmem, a_tmem + 64 + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO, 1u);
-      }
+      if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
     bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
     if (ok && lane == 0) {
@@ -656,10 +746,15 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       // barrier probe.  The thread probes the tiles in turn and issues whichever
       // step is ready, so one tile's softmax never holds back the other tile's MMAs.
       // After the last row tile's step j one commit completes step record j + 1.
+      // When P is stored as hi + lo (prefix shorter than kSplitPrefix), steps from j_tree on
+      // cover key tiles that hold tree keys: the polling loop stops before them and an
+      // ordered tail issues them with the second (lo) PV MMA, so the steady-state loop
+      // stays free of that code.
+      const int j_tree = P < kSplitPrefix ? min(max(P / kKeyTile - k0, 0), T) : T;
       int jn[NT];
 #pragma unroll
       for (int t = 0; t < NT; ++t) jn[t] = 0;
-      int left = NT * T;
+      int left = NT * j_tree;
       uint32_t idle = 0;
       uint64_t idle_since = 0;
       while (left > 0) {
@@ -667,14 +762,14 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int j = jn[t];
-          if (j >= T) continue;
+          if (j >= j_tree) continue;
           if (!mbar_try_wait(&p_full[t], static_cast<uint32_t>(j) & 1u)) continue;
           bool last = true;                  // the other row tiles are past key tile j
 #pragma unroll
           for (int u = 0; u < NT; ++u)
             if (u != t && jn[u] <= j) last = false;
           tc_fence_after();
-          issue_pv(t, j % SV, j > 0, (k0 + j + 1) * kKeyTile > P);
+          issue_pv(t, j % SV, j > 0, false);
           if (j + 1 < T) {
             issue_s(t, (j + 1) % SK);
             mma_commit(&s_full[t]);
@@ -692,6 +787,21 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
             ok = false;
             break;
           }
+        }
+      }
+      for (int j = j_tree; j < T && ok; ++j) {
+        for (int t = 0; t < NT && ok; ++t) {
+          if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j) & 1u, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, j % SV, j > 0, true);
+          if (j + 1 < T) {
+            issue_s(t, (j + 1) % SK);
+            mma_commit(&s_full[t]);
+          }
+          if (t == NT - 1) mma_commit(&step_done[(j + 1) % kStepRing]);
         }
       }
     }
@@ -751,69 +861,22 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     float m_run = -INFINITY;
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int key0 = (k0 + j) * kKeyTile;
-      const bool masked_tile = key0 + kKeyTile > P;
-      uint64_t mw[3] = {0ull, 0ull, 0ull};
-      const int w_lo = max(key0 - P, 0) >> 6;
-      if (masked_tile && valid) {
-#pragma unroll
-        for (int u = 0; u < 3; ++u)
-          if (w_lo + u < W) mw[u] = __ldg(reinterpret_cast<const unsigned long long*>(mrow) + w_lo + u);
-      }
-      if (!wait_warp(&s_full[t], static_cast<uint32_t>(j) & 1u, abort)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld128(tS, sr);
-      float* sv = reinterpret_cast<float*>(sr);
-      if (masked_tile) {
-        // Visibility of the tile's 128 keys as four 32-bit words: prefix keys always,
-        // tree key j iff bit j of the node's ancestor mask, nothing past the sequence end.
-        const int pre = min(max(P - key0, 0), kKeyTile);
-        const int end = min(max(L - key0, 0), kKeyTile);
-        uint32_t vis[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int c0 = 32 * w;
-          uint32_t m = window_bits32(mw, key0 + c0 - P - 64 * w_lo);
-          const int np = min(max(pre - c0, 0), 32);
-          const int ne = min(max(end - c0, 0), 32);
-          m |= np >= 32 ? 0xFFFFFFFFu : ((1u << np) - 1u);
-          m &= ne >= 32 ? 0xFFFFFFFFu : ((1u << ne) - 1u);
-          vis[w] = m;
-        }
-#pragma unroll
-        for (int c = 0; c < kKeyTile; ++c)
-          if (!((vis[c >> 5] >> (c & 31)) & 1u)) sv[c] = -INFINITY;
-      }
-      float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-      for (int c = 4; c < kKeyTile; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
-      const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-      const float mt = mx * sl2;
-      const bool raise = mt > m_run + kRescaleThreshold;
-      const float m_old = m_run;
-      if (raise) m_run = mt;
-      const float corr = raise ? fast_exp2(m_old - m_run) : 1.f;   // 0 when m_old = -inf
-      const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
-      l = l * corr + row_probs(sv, sl2, neg, masked_tile, tS);
-      // O holds PV of tiles < j (complete: s_full of tile j was committed after them).
-      const bool need = raise && j > 0 && m_old != -INFINITY;
-      if (__any_sync(0xffffffffu, need)) {
-        const float f = need ? corr : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-          tmem_st32(tO + c * 32, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
+    // Key tiles before jm hold prefix keys only; the rest reach the tree.
+    const int jm = min(max(P / kKeyTile - k0, 0), T);
+    for (int j = 0; j < jm && ok; ++j)
+      ok = softmax_tile<false, false, D>(&s_full[t], static_cast<uint32_t>(j) & 1u, abort, &p_full[t], tS, tO,
+                                  mrow, valid, W, (k0 + j) * kKeyTile, P, L, sl2, j > 0, nullptr,
+                                  false, m_run, l);
+    if (P < kSplitPrefix) {
+      for (int j = jm; j < T && ok; ++j)
+        ok = softmax_tile<true, true, D>(&s_full[t], static_cast<uint32_t>(j) & 1u, abort, &p_full[t], tS,
+                                         tO, mrow, valid, W, (k0 + j) * kKeyTile, P, L, sl2, j > 0,
+                                         nullptr, false, m_run, l);
+    } else {
+      for (int j = jm; j < T && ok; ++j)
+        ok = softmax_tile<true, false, D>(&s_full[t], static_cast<uint32_t>(j) & 1u, abort, &p_full[t],
+                                          tS, tO, mrow, valid, W, (k0 + j) * kKeyTile, P, L, sl2, j > 0,
+                                          nullptr, false, m_run, l);
     }
     // Every thread of the warpgroup reaches this vote (all waits are bounded), so the
     // epilogue's own barriers are entered by all of them or by none.
@@ -1276,11 +1339,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       for (int kk = 0; kk < kKeyTile / 16; ++kk)
         mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
                (acc || kk > 0) ? 1u : 0u);
-      if (lo) {
-#pragma unroll
-        for (int kk = 0; kk < kKeyTile / 16; ++kk)
-          mma_ts(d_tmem, a_tmem + 64 + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO, 1u);
-      }
+      if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
     bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
     if (ok && lane == 0) {
@@ -1396,73 +1455,27 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const uint64_t* mrow = p.mask + (static_cast<size_t>(b) * p.N + (valid ? i : 0)) * W;
       float m_run = -INFINITY;
       float l = 0.f;
-      for (int j = 0; j < T; ++j) {
-        const int jg = jg0 + j;
-        const int key0 = (sgm.k0 + j) * kKeyTile;
-        const bool masked_tile = key0 + kKeyTile > P;
-        uint64_t mw[3] = {0ull, 0ull, 0ull};
-        const int w_lo = max(key0 - P, 0) >> 6;
-        if (masked_tile && valid) {
-#pragma unroll
-          for (int u = 0; u < 3; ++u)
-            if (w_lo + u < W) mw[u] = __ldg(reinterpret_cast<const unsigned long long*>(mrow) + w_lo + u);
-        }
-        if (!wait_warp(&s_full[t], static_cast<uint32_t>(jg) & 1u, abort)) {
-          if (lane == 0) set_abort(abort, p.dev_err);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld128(tS, sr);
-        float* sv = reinterpret_cast<float*>(sr);
-        if (masked_tile) {
-          const int pre = min(max(P - key0, 0), kKeyTile);
-          const int end = min(max(L - key0, 0), kKeyTile);
-          uint32_t vis[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const int c0 = 32 * w;
-            uint32_t m = window_bits32(mw, key0 + c0 - P - 64 * w_lo);
-            const int np = min(max(pre - c0, 0), 32);
-            const int ne = min(max(end - c0, 0), 32);
-            m |= np >= 32 ? 0xFFFFFFFFu : ((1u << np) - 1u);
-            m &= ne >= 32 ? 0xFFFFFFFFu : ((1u << ne) - 1u);
-            vis[w] = m;
-          }
-#pragma unroll
-          for (int c = 0; c < kKeyTile; ++c)
-            if (!((vis[c >> 5] >> (c & 31)) & 1u)) sv[c] = -INFINITY;
-        }
-        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-        for (int c = 4; c < kKeyTile; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], sv[c], sv[c + 1]);
-        const float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-        const float mt = mx * sl2;
-        const bool raise = mt > m_run + kRescaleThreshold;
-        const float m_old = m_run;
-        if (raise) m_run = mt;
-        const float corr = raise ? fast_exp2(m_old - m_run) : 1.f;
-        const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
-        if (rl == 0) s_lo[t] = masked_tile ? 1 : 0;   // read by the MMA issuer after p_full
-        l = l * corr + row_probs(sv, sl2, neg, masked_tile, tS);
-        // O holds PV of this segment's tiles < j (complete: s_full of tile jg followed them)
-        const bool need = raise && j > 0 && m_old != -INFINITY;
-        if (__any_sync(0xffffffffu, need)) {
-          const float f = need ? corr : 1.f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-            tmem_st32(tO + c * 32, o);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&p_full[t]);
+      // Key tiles before jm hold prefix keys only; the rest reach the tree.
+      const int jm = min(max(P / kKeyTile - sgm.k0, 0), T);
+      volatile int* lo_flag = &s_lo[t];
+      for (int j = 0; j < jm && ok; ++j)
+        ok = softmax_tile<false, false, D>(&s_full[t], static_cast<uint32_t>(jg0 + j) & 1u, abort, &p_full[t],
+                                    tS, tO, mrow, valid, W, (sgm.k0 + j) * kKeyTile, P, L, sl2, j > 0,
+                                    lo_flag, rl == 0, m_run, l);
+      if (P < kSplitPrefix) {
+        for (int j = jm; j < T && ok; ++j)
+          ok = softmax_tile<true, true, D>(&s_full[t], static_cast<uint32_t>(jg0 + j) & 1u, abort,
+                                           &p_full[t], tS, tO, mrow, valid, W, (sgm.k0 + j) * kKeyTile, P,
+                                           L, sl2, j > 0, lo_flag, rl == 0, m_run, l);
+      } else {
+        for (int j = jm; j < T && ok; ++j)
+          ok = softmax_tile<true, false, D>(&s_full[t], static_cast<uint32_t>(jg0 + j) & 1u, abort,
+                                            &p_full[t], tS, tO, mrow, valid, W, (sgm.k0 + j) * kKeyTile, P,
+                                            L, sl2, j > 0, lo_flag, rl == 0, m_run, l);
+      }
+      if (!ok) {
+        if (lane == 0) set_abort(abort, p.dev_err);
+        break;
       }
       // ---- the segment's rows: O / l, straight from TMEM to global memory, once its last
       // PV is done: S of the next tile (committed after it) or, for the range's last
