@@ -3,20 +3,26 @@
 
 One step = one pass of the whole hot path over one batch of synthetic inputs already in
 HBM: tree-mask build -> tree-causal paged attention -> greedy tree verify (argmax + walk).
-Default workload: Qwen3-8B attention shape, one sequence, 2048-token prefix, 16-node
-linear draft tree, vocabulary 151936 (``--config`` picks another of the five).
+The reported metric is the tree-causal paged attention call's time (µs per call) with its
+HBM GB/s and TFLOP/s against the roofline.  Default workload: Qwen3-30B-A3B attention
+shape, 8 sequences with 32768-token prefixes, budget-256 best-first trees, vocabulary
+151936 (``--config`` picks another of the five).
 
-Timing: the step (three calls) is captured once into a CUDA graph; W untimed warm-up
-steps, then K timed replays between CUDA events on the stream the kernels run on, each
-after a 256 MiB write (twice the L2) so every step starts from a cold L2.  Each call is
-also captured alone and timed the same way (K replays each) for the per-call breakdown;
-the attention call's time is the one used for the roofline.  The e2e figure uses the plain API calls (no graphs) with pinned
-host buffers and the copies inside the timed region.  Under torchrun every rank runs its
-own replica (the path shards by sequence with no exchange), and the slowest rank's time is
-reported.
+Timing: each of the three calls is captured once into its own CUDA graph.  W untimed
+warm-up steps, then K timed steps; a step writes 256 MiB (twice the L2) so it starts from
+a cold L2, then replays the mask, attention and verify graphs with CUDA events between
+them on the stream the kernels run on.  ``value`` is the mean attention time over the K
+steps; the step time and the other calls go to ``breakdown_us``.  The same run then
+times the attention call alone for at least half a second (so the clock sampler sees
+sustained load), the attention calls of the budget-16 and budget-256 Qwen3-8B workloads,
+the draft-tree build, the ragged attention call and the KV compaction.  ``e2e`` times the
+attention call through the plain API with pinned host buffers: the copies of its inputs
+in and of its outputs back are inside the timed region.  Under torchrun every rank runs
+its own replica (the path shards by sequence with no exchange), and the slowest rank's
+time is reported.
 
-``--impl reference`` times the fp64 CPU oracle instead (on a bounded sample of the same
-workload, scaled to a full step).
+``--impl reference`` times the fp64 CPU oracle's attention instead (on a bounded sample
+of the query rows of the same workload, scaled to a full call).
 """
 from __future__ import annotations
 
@@ -37,17 +43,16 @@ sys.path.insert(0, ROOT)
 from tree_speculative_decoding_jf_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "tree-causal paged attention µs/call, HBM GB/s & TFLOP/s vs GB300 roofline"
-DEFAULT_CONFIG = "c2_qwen3_8b_chain16"
+DEFAULT_CONFIG = "c5_qwen3_30b_b8_tree256_32k"
+# Other workloads whose attention call is timed in the same run (budgets 16 and 256).
+SIDE_CONFIGS = ("c2_qwen3_8b_chain16", "c3_qwen3_8b_tree256")
+SUSTAINED_S = 0.5                      # length of the attention-only loop
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes per attention call from the ncu captures summarised under profiles/ (None
-# until a capture of the current kernel exists for that workload).
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one jf_tree_attention call
-# (attention kernel + combine) from `ncu --set full` captures of the current kernels; see
-# profiles/tree_attention_<workload>_full.md for the commands.
-NCU_TRAFFIC_BYTES = {
-    "c2_qwen3_8b_chain16": 8659968 + 0 + 2404352 + 0,
-    "c5_qwen3_30b_b8_tree256_32k": 568709888 + 27651584 + 38085120 + 4352,
-}
+# (attention kernel + combine) from ncu captures of the current kernels (None until a
+# capture of the current kernel exists for that workload); the capture commands are in
+# the profile summaries.
+NCU_TRAFFIC_BYTES: dict = {}
 
 
 # ----------------------------------------------------------------------------- work model
@@ -150,12 +155,12 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_step_time(w, budget_s: float = 20.0):
-    """Time the fp64 oracle on a bounded sample of one step and scale to a full step.
-    Returns (seconds per full step, description of the sample, threads used)."""
+def oracle_attention_time(w, budget_s: float = 20.0):
+    """Time the fp64 oracle's tree attention on a bounded sample of query rows and scale
+    by row count to one full call.  Returns (seconds per call, sample description,
+    threads used)."""
     import oracle
     rows_total = w.B * w.N * w.Hq
-    # attention: time a small probe, then size the sample to the budget
     rb, rh, ri = oracle.all_rows(w)
     rng = np.random.default_rng(0)
     order = rng.permutation(rows_total)
@@ -163,36 +168,39 @@ def oracle_step_time(w, budget_s: float = 20.0):
     t0 = time.perf_counter()
     oracle.tree_attention_rows(w, rb[order[:n_probe]], rh[order[:n_probe]], ri[order[:n_probe]])
     per_row = max((time.perf_counter() - t0) / n_probe, 1e-7)
-    n_att = int(min(rows_total, max(n_probe, budget_s * 0.7 / per_row)))
+    n_att = int(min(rows_total, max(n_probe, budget_s / per_row)))
     sel = order[:n_att]
     t0 = time.perf_counter()
     oracle.tree_attention_rows(w, rb[sel], rh[sel], ri[sel])
     t_att = (time.perf_counter() - t0) * rows_total / n_att
-    # mask: whole step (cheap)
-    t0 = time.perf_counter()
-    oracle.tree_mask(w.parent, w.prefix_len)
-    t_mask = time.perf_counter() - t0
-    # verify: argmax over a sample of rows, the walk over every sequence
-    lrows = w.logits.reshape(w.B * w.N, w.V)
-    n_lr = min(w.B * w.N, max(1, int(2e9 / max(1, w.V * 20))))
-    t0 = time.perf_counter()
-    am_part = oracle.argmax(lrows[:n_lr], w.logits_dtype)
-    t_arg = (time.perf_counter() - t0) * (w.B * w.N) / n_lr
-    am = np.zeros((w.B, w.N), np.int32)
-    am.reshape(-1)[:n_lr] = am_part
-    t0 = time.perf_counter()
-    oracle.tree_walk(am, w.draft, w.parent)
-    t_walk = time.perf_counter() - t0
-    total = t_att + t_mask + t_arg + t_walk
-    sample = (f"attention {n_att}/{rows_total} query rows, argmax {n_lr}/{w.B * w.N} logits rows, "
-              f"mask and walk in full; scaled by row count to one full step")
+    sample = (f"attention over {n_att} of {rows_total} query rows (random sample), scaled by "
+              f"row count to one full call")
     threads = int(os.environ.get("OMP_NUM_THREADS", len(os.sched_getaffinity(0))))
-    return total, sample, threads
+    return t_att, sample, threads
 
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_gpu(args, w, rank, world):
+def roofline(w, us, peaks, tree_len=None):
+    """Bound (HBM or tensor, whichever ideal time is longer), achieved rate and fraction of
+    the measured peak for an attention call of `us` microseconds."""
+    abytes = attention_algorithmic_bytes(w, tree_len)
+    aflops = attention_algorithmic_flops(w, tree_len)
+    if abytes / (peaks["hbm_gbs"] * 1e9) >= aflops / (peaks["bf16_tflops"] * 1e12):
+        r = {"bound": "hbm", "achieved": abytes / (us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"],
+             "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": aflops / (us * 1e-6) / 1e12,
+             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["algorithmic_bytes"] = abytes
+    r["algorithmic_flops"] = aflops
+    r["hbm_gbs_achieved"] = abytes / (us * 1e-6) / 1e9
+    r["tflops_achieved"] = aflops / (us * 1e-6) / 1e12
+    return r
+
+
+def run_gpu(args, w, rank, world, peaks):
     import torch
     from tree_speculative_decoding_jf_gb300 import jf
 
@@ -216,26 +224,11 @@ def run_gpu(args, w, rank, world):
     bonus = torch.empty((B,), dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    launches_per_step = 1 + (2 if ws_a_bytes > 0 else 1) + 2
+    attn_launches = 2 if ws_a_bytes > 0 else 1          # attention kernel (+ combine)
+    launches_per_step = 1 + attn_launches + 2           # mask, attention, argmax + walk
 
-    def step(tt, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        jf.jf_build_tree_mask(tt["parent"], tt["prefix_len"], mask, depth, pos, err, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        jf.jf_tree_attention(tt["q"], tt["k_cache"], tt["v_cache"], tt["block_table"],
-                             tt["prefix_len"], mask, w.scale, out, lse, ws_a, err, stream)
-        if ev is not None:
-            ev[2].record(stream)
-        jf.jf_tree_verify(tt["logits"], tt["draft"], tt["parent"], acc, path, bonus, argmax, ws_v,
-                          err, stream)
-        if ev is not None:
-            ev[3].record(stream)
-
-    # Each hot-path call is captured once into its own CUDA graph; a timed step replays the
-    # three graphs between CUDA events, so host-side argument marshalling stays out of
-    # the device timeline.
+    # Each hot-path call is captured once into its own CUDA graph, so host-side argument
+    # marshalling stays out of the device timeline.
     def call_mask():
         jf.jf_build_tree_mask(t["parent"], t["prefix_len"], mask, depth, pos, err)
 
@@ -262,21 +255,39 @@ def run_gpu(args, w, rank, world):
                 fn()
         return g
 
-    g_step = capture(call_mask, call_attn, call_verify)     # the whole hot path
-    g_parts = [capture(call_mask), capture(call_attn), capture(call_verify)]
+    g_mask, g_attn, g_ver = capture(call_mask), capture(call_attn), capture(call_verify)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def step(k):
+        """One step after an L2 eviction: mask, attention and verify graphs with events
+        between them."""
+        e = [ev() for _ in range(4)]
+        flush.fill_(k & 0xFF)
+        e[0].record(stream)
+        g_mask.replay()
+        e[1].record(stream)
+        g_attn.replay()
+        e[2].record(stream)
+        g_ver.replay()
+        e[3].record(stream)
+        return e
 
     def timed(g, k):
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b_ = ev(), ev()
         flush.fill_(k & 0xFF)                     # evict L2 before every timed replay
         a.record(stream)
         g.replay()
         b_.record(stream)
         return a, b_
 
+    def ms(pairs):
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b_) for a, b_ in pairs]
+
     for k in range(args.warmup):
-        timed(g_step, k)
-        for g in g_parts:
-            timed(g, k)
+        step(k)
     torch.cuda.synchronize(dev)
     if world > 1:
         import torch.distributed as dist
@@ -285,55 +296,92 @@ def run_gpu(args, w, rank, world):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     time.sleep(0.3)                              # let the sampler start before the loop
-    step_ev = [timed(g_step, k) for k in range(args.steps)]
-    part_ev = [[timed(g, k) for g in g_parts] for k in range(args.steps)]
+    step_ev = [step(k) for k in range(args.steps)]
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    step_ms = [a.elapsed_time(b_) for a, b_ in step_ev]
-    mask_ms = [e[0][0].elapsed_time(e[0][1]) for e in part_ev]
-    attn_ms = [e[1][0].elapsed_time(e[1][1]) for e in part_ev]
-    ver_ms = [e[2][0].elapsed_time(e[2][1]) for e in part_ev]
+    step_ms = [e[0].elapsed_time(e[3]) for e in step_ev]
+    mask_ms = [e[0].elapsed_time(e[1]) for e in step_ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in step_ev]
+    ver_ms = [e[2].elapsed_time(e[3]) for e in step_ev]
+    # Sustained: the attention call alone for at least SUSTAINED_S seconds, still inside
+    # the clock sampler's window.
+    reps = max(args.steps, int(SUSTAINED_S / max(statistics.mean(attn_ms) * 1e-3, 1e-6)) + 1)
+    sus_ms = ms([timed(g_attn, k) for k in range(reps)])
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item():#x} during the benchmark")
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    # ---- the attention calls of the budget-16 and budget-256 Qwen3-8B workloads
+    side_lines = {}
+    for name in SIDE_CONFIGS:
+        if name == w.name or world > 1:
+            continue
+        sw = wl.config(name, with_logits=False)
+        st = wl.device_tensors(sw, device=dev, with_logits=False)
+        smask = torch.empty((sw.B, sw.N, (sw.N + 63) // 64), dtype=torch.int64, device=dev)
+        jf.jf_build_tree_mask(st["parent"], st["prefix_len"], smask, None, None, err)
+        sout = torch.empty_like(st["q"])
+        slse = torch.empty((sw.B, sw.Hq, sw.N), dtype=torch.float32, device=dev)
+        nws = jf.jf_tree_attention_workspace_size(sw.B, sw.N, sw.Hq, sw.Hkv, sw.D, sw.max_pages, sw.page)
+        sws = torch.empty(max(16, nws), dtype=torch.uint8, device=dev)
+
+        def call_side(st=st, smask=smask, sout=sout, slse=slse, sws=sws, sw=sw):
+            jf.jf_tree_attention(st["q"], st["k_cache"], st["v_cache"], st["block_table"],
+                                 st["prefix_len"], smask, sw.scale, sout, slse, sws, err)
+
+        call_side()
+        g_side = capture(call_side)
+        for k in range(args.warmup):
+            timed(g_side, k)
+        side_ms = ms([timed(g_side, k) for k in range(max(args.steps, 50))])
+        us = statistics.mean(side_ms) * 1e3
+        rf = roofline(sw, us, peaks)
+        side_lines[name] = {"attention_us": us, "bound": rf["bound"], "achieved": rf["achieved"],
+                            "unit": rf["unit"], "frac": rf["frac"],
+                            "traffic": NCU_TRAFFIC_BYTES.get(name)}
+        del st, smask, sout, slse, sws, g_side
+        torch.cuda.synchronize(dev)
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed: the
+    # attention call with its inputs copied in (and its mask built) and its outputs
+    # copied back.
     e2e = None
     if not args.no_e2e:
-        host = {k: v.cpu().pin_memory() for k, v in t.items()}
+        keys = ("q", "k_cache", "v_cache", "block_table", "prefix_len", "parent")
+        host = {k: t[k].cpu().pin_memory() for k in keys}
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h_acc = torch.empty(acc.shape, dtype=acc.dtype).pin_memory()
-        h_path = torch.empty(path.shape, dtype=path.dtype).pin_memory()
-        h_bonus = torch.empty(bonus.shape, dtype=bonus.dtype).pin_memory()
-        dt = {k: torch.empty_like(v) for k, v in t.items()}
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dt = {k: torch.empty_like(t[k]) for k in keys}
         h2d = sum(v.numel() * v.element_size() for v in host.values())
-        d2h = sum(x.numel() * x.element_size() for x in (h_out, h_acc, h_path, h_bonus))
+        d2h = sum(x.numel() * x.element_size() for x in (h_out, h_lse))
 
-        def e2e_step():
-            for k in host:
+        def e2e_call():
+            for k in keys:
                 dt[k].copy_(host[k], non_blocking=True)
-            step(dt)
+            jf.jf_build_tree_mask(dt["parent"], dt["prefix_len"], mask, None, None, err)
+            jf.jf_tree_attention(dt["q"], dt["k_cache"], dt["v_cache"], dt["block_table"],
+                                 dt["prefix_len"], mask, w.scale, out, lse, ws_a, err)
             h_out.copy_(out, non_blocking=True)
-            h_acc.copy_(acc, non_blocking=True)
-            h_path.copy_(path, non_blocking=True)
-            h_bonus.copy_(bonus, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
-            e2e_step()
+            e2e_call()
         torch.cuda.synchronize(dev)
         e2e_ms = []
         for k in range(args.steps):
             flush.fill_(k & 0xFF)
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a, b_ = ev(), ev()
             a.record(stream)
-            e2e_step()
+            e2e_call()
             b_.record(stream)
             b_.synchronize()
             e2e_ms.append(a.elapsed_time(b_))
-        e2e = {"value": statistics.mean(e2e_ms) * 1e3, "unit": "µs/call",
+        e2e = {"value": max_over_ranks(statistics.mean(e2e_ms) * 1e3, world), "unit": "µs/call",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+        del host, dt
     # ---- before verification: best-first draft-tree construction from per-depth draft
     # logits (16 depths, 8 candidates per depth, the workload's budget); not part of the step.
     dl = wl.draft_logits(B, 16, V, seed=w.seed)
@@ -353,9 +401,8 @@ def run_gpu(args, w, rank, world):
     g_tree = capture(call_tree)
     for k in range(args.warmup):
         timed(g_tree, k)
-    tree_ev = [timed(g_tree, k) for k in range(args.steps)]
+    tree_ms = ms([timed(g_tree, k) for k in range(args.steps)])
     torch.cuda.synchronize(dev)
-    tree_ms = [a.elapsed_time(b_) for a, b_ in tree_ev]
     tree_bytes = int(t_dl.numel()) * 2
 
     # ---- ragged trees: the same attention call with a per-sequence budget mix (seeded,
@@ -373,9 +420,8 @@ def run_gpu(args, w, rank, world):
     g_rag = capture(call_attn_ragged)
     for k in range(args.warmup):
         timed(g_rag, k)
-    rag_ev = [timed(g_rag, k) for k in range(args.steps)]
+    rag_ms = ms([timed(g_rag, k) for k in range(args.steps)])
     torch.cuda.synchronize(dev)
-    rag_ms = [a.elapsed_time(b_) for a, b_ in rag_ev]
 
     # ---- after verification: accepted-path KV compaction (not part of the step).  It
     # rewrites the cache in place, so it is timed last; replays repeat the same copies.
@@ -388,15 +434,14 @@ def run_gpu(args, w, rank, world):
     g_compact = capture(call_compact)
     for k in range(args.warmup):
         timed(g_compact, k)
-    cmp_ev = [timed(g_compact, k) for k in range(args.steps)]
+    compact_ms = ms([timed(g_compact, k) for k in range(args.steps)])
     torch.cuda.synchronize(dev)
-    compact_ms = [a.elapsed_time(b_) for a, b_ in cmp_ev]
     if err.item() != 0:
-        raise RuntimeError(f"device error bits {err.item():#x} in the KV compaction")
-    return dict(step_ms=step_ms, mask_ms=mask_ms, attn_ms=attn_ms, ver_ms=ver_ms, clocks=clk,
-                e2e=e2e, launches=2 * launches_per_step * args.steps, ws=ws_a_bytes,
+        raise RuntimeError(f"device error bits {err.item():#x} after the benchmark's calls")
+    return dict(step_ms=step_ms, mask_ms=mask_ms, attn_ms=attn_ms, ver_ms=ver_ms, sus_ms=sus_ms,
+                clocks=clk, e2e=e2e, launches=launches_per_step * args.steps, ws=ws_a_bytes,
                 compact_ms=compact_ms, accepted=acc.cpu().tolist(), tree_ms=tree_ms,
-                tree_bytes=tree_bytes, rag_ms=rag_ms, rag_len=rag_len.tolist())
+                tree_bytes=tree_bytes, rag_ms=rag_ms, rag_len=rag_len.tolist(), side=side_lines)
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -443,20 +488,19 @@ def main():
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group(backend)
 
-    w = wl.config(args.config)
     peaks, peak_src = load_peaks()
 
     if args.impl == "reference":
         if rank != 0:
             return
-        per_step = []
+        w = wl.config(args.config, with_logits=False)
+        per_call = []
         sample = threads = None
-        for _ in range(args.warmup):
-            pass                                     # the oracle has no warm-up state
         for _ in range(args.steps):
-            s, sample, threads = oracle_step_time(w, budget_s=max(1.0, args.cpu_budget / args.steps))
-            per_step.append(s)
-        v = statistics.mean(per_step) * 1e6
+            s, sample, threads = oracle_attention_time(
+                w, budget_s=max(0.2, args.cpu_budget / args.steps))
+            per_call.append(s)
+        v = statistics.mean(per_call) * 1e6
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": v, "unit": "µs/call",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -469,48 +513,39 @@ def main():
                     "d2h_bytes_per_step": 0}}), flush=True)
         return
 
-    r = run_gpu(args, w, rank, world)
-    step_us = statistics.mean(r["step_ms"]) * 1e3
-    step_us = max_over_ranks(step_us, world)
-    attn_us = statistics.mean(r["attn_ms"]) * 1e3
-    abytes = attention_algorithmic_bytes(w)
-    aflops = attention_algorithmic_flops(w)
-    t_hbm = abytes / (peaks["hbm_gbs"] * 1e9)
-    t_tc = aflops / (peaks["bf16_tflops"] * 1e12)
-    if t_hbm >= t_tc:
-        roof = {"bound": "hbm", "achieved": abytes / (attn_us * 1e-6) / 1e9,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": aflops / (attn_us * 1e-6) / 1e12,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    w = wl.config(args.config)
+    r = run_gpu(args, w, rank, world, peaks)
+    attn_us = max_over_ranks(statistics.mean(r["attn_ms"]) * 1e3, world)
+    step_us = max_over_ranks(statistics.mean(r["step_ms"]) * 1e3, world)
+    roof = roofline(w, attn_us, peaks)
     roof["traffic"] = NCU_TRAFFIC_BYTES.get(w.name)
     roof["kernel"] = "jf_tree_attention (attention kernel + combine)"
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
-    roof["algorithmic_bytes"] = abytes
-    roof["algorithmic_flops"] = aflops
+    roof["peak_source"] = "measured (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["attention_us"] = attn_us
-    roof["hbm_gbs_achieved"] = abytes / (attn_us * 1e-6) / 1e9
-    roof["tflops_achieved"] = aflops / (attn_us * 1e-6) / 1e12
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        s, sample, threads = oracle_step_time(w, budget_s=args.cpu_budget)
+        s, sample, threads = oracle_attention_time(w, budget_s=args.cpu_budget)
         cpu = {"value": s * 1e6, "unit": "µs/call", "cores": threads, "kind": "oracle",
                "sample": sample}
+    sus_us = statistics.mean(r["sus_ms"]) * 1e3
     line = {
-        "metric": METRIC, "value": step_us, "unit": "µs/call", "n_gpus": world,
+        "metric": METRIC, "value": attn_us, "unit": "µs/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_us / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(w),
-        "breakdown_us": {"mask": statistics.mean(r["mask_ms"]) * 1e3, "attention": attn_us,
+        "breakdown_us": {"step": step_us, "step_min": min(r["step_ms"]) * 1e3,
+                         "mask": statistics.mean(r["mask_ms"]) * 1e3, "attention": attn_us,
                          "attention_min": min(r["attn_ms"]) * 1e3,
                          "attention_median": statistics.median(r["attn_ms"]) * 1e3,
-                         "step_min": min(r["step_ms"]) * 1e3,
+                         "attention_sustained": sus_us,
+                         "attention_sustained_calls": len(r["sus_ms"]),
+                         "attention_sustained_frac": roofline(w, sus_us, peaks)["frac"],
                          "verify": statistics.mean(r["ver_ms"]) * 1e3,
                          "verify_hbm_gbs": verify_algorithmic_bytes(w) /
                          (statistics.mean(r["ver_ms"]) * 1e-3) / 1e9,
+                         "other_workloads_attention": r["side"],
                          "draft_tree_build": statistics.mean(r["tree_ms"]) * 1e3,
                          "draft_tree_logits_hbm_gbs": r["tree_bytes"] /
                          (statistics.mean(r["tree_ms"]) * 1e-3) / 1e9,
