@@ -13,7 +13,8 @@
 // Kernel 2 (one CTA per sequence): merges the chunk keys into argmax (shared atomicMax),
 // finds depths by pointer jumping, computes accepted-subtree lengths level by level from
 // the deepest level up with shared-memory atomicMax on (len + 1) << 16 | (0xFFFF - child),
-// and walks the best children from the root.
+// and walks the best children from the root.  Trees of at most 64 nodes take a one-warp
+// version of the same steps with no block barriers.
 #include <algorithm>
 #include <mutex>
 
@@ -311,6 +312,161 @@ __global__ void __launch_bounds__(kWalkThreads)
   grid_dependents_launch();
 }
 
+// Small trees (N <= 64) in one warp: no block barriers, so a deep chain costs a few dozen
+// cycles per level instead of a __syncthreads each.  Lane q owns nodes q and q + 32.  Every
+// chunk key of a lane's rows is requested before any is merged (at most kSmallWalkKeys
+// loads in flight per lane), so the merge costs one memory round trip.  Depths come from
+// pointer jumping through shared memory, accepted-subtree lengths from shared-memory
+// atomicMax level by level (deepest first, a __syncwarp between levels), then lane 0
+// follows the best children from the root.
+constexpr int kSmallWalkNodes = 64;
+constexpr int kSmallWalkKeys = 48;    // keys per lane: 48 chunks of one row, or 24 of two
+
+inline bool small_walk_fits(int N, int chunks) {
+  return N <= kSmallWalkNodes &&
+         (N <= 32 ? chunks <= kSmallWalkKeys : chunks <= kSmallWalkKeys / 2);
+}
+
+__global__ void __launch_bounds__(32)
+    tree_walk_small_kernel(const uint64_t* __restrict__ part, int chunks,
+                           const int32_t* __restrict__ draft, const int32_t* __restrict__ parent,
+                           const int32_t* __restrict__ tree_len, int N, int V,
+                           int32_t* __restrict__ argmax_out, int32_t* __restrict__ accept_len,
+                           int32_t* __restrict__ path, int32_t* __restrict__ bonus,
+                           int32_t* dev_err) {
+  constexpr int H = kSmallWalkKeys / 2;
+  __shared__ int s_par[kSmallWalkNodes], s_am[kSmallWalkNodes], s_dep[kSmallWalkNodes],
+      s_anc[kSmallWalkNodes], s_path[kSmallWalkNodes];
+  __shared__ uint32_t s_key[kSmallWalkNodes];
+  grid_dependency_wait();
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const size_t rb = static_cast<size_t>(b) * N;
+  int nt = N;
+  if (tree_len != nullptr) {
+    const int raw = tree_len[b];
+    nt = max(1, min(raw, N));
+    if (raw != nt && lane == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
+  }
+  const bool two = N > 32;                          // two rows per lane
+  int r_par[2] = {-1, -1}, r_draft[2] = {-1, -1};
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = lane + 32 * k;
+    if (i < nt) {
+      r_par[k] = parent[rb + i];
+      r_draft[k] = draft[rb + i];
+    }
+  }
+  // One lane's keys: row lane's chunks 0..47, or rows lane and lane + 32 with 24 each.
+  uint64_t kv[kSmallWalkKeys];
+#pragma unroll
+  for (int u = 0; u < kSmallWalkKeys; ++u) {
+    const int i = two ? lane + 32 * (u / H) : lane;
+    const int c = two ? u % H : u;
+    kv[u] = (i < N && c < chunks) ? part[(rb + i) * chunks + c] : 0ull;
+  }
+  uint64_t best[2] = {0ull, 0ull};
+#pragma unroll
+  for (int u = 0; u < kSmallWalkKeys; ++u) {
+    const int k = two ? u / H : 0;
+    best[k] = kv[u] > best[k] ? kv[u] : best[k];
+  }
+  int bad_parent = 0, bad_token = 0;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = lane + 32 * k;
+    if (i < N) {
+      const int am = static_cast<int>(~static_cast<uint32_t>(best[k] & 0xFFFFFFFFull));
+      s_am[i] = am;
+      if (argmax_out != nullptr) argmax_out[rb + i] = am;
+      int p = i < nt ? r_par[k] : -1;
+      const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+      if (!ok && i < nt) bad_parent = 1;
+      if (!ok) p = -1;
+      s_par[i] = p;
+      s_anc[i] = p;
+      s_dep[i] = p >= 0 ? 1 : 0;
+      s_key[i] = 0u;
+      if (i > 0 && i < nt && (r_draft[k] < 0 || r_draft[k] >= V)) bad_token = 1;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad_parent) && lane == 0) report(dev_err, JF_DEVERR_BAD_PARENT);
+  if (__any_sync(0xffffffffu, bad_token) && lane == 0) report(dev_err, JF_DEVERR_BAD_TOKEN);
+  __syncwarp();
+  // depth by pointer jumping: dep[i] += dep[anc[i]], anc[i] = anc[anc[i]]
+  for (int round = 0; round < 7; ++round) {
+    int nd[2], na[2], any = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = lane + 32 * k;
+      nd[k] = 0; na[k] = -1;
+      if (i < N) {
+        const int a = s_anc[i];
+        nd[k] = s_dep[i];
+        na[k] = a;
+        if (a >= 0) {
+          nd[k] += s_dep[a];
+          na[k] = s_anc[a];
+          any = 1;
+        }
+      }
+    }
+    if (!__any_sync(0xffffffffu, any)) break;
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = lane + 32 * k;
+      if (i < N) { s_dep[i] = nd[k]; s_anc[i] = na[k]; }
+    }
+    __syncwarp();
+  }
+  int maxd = 0;
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    if (lane + 32 * k < N) maxd = max(maxd, s_dep[lane + 32 * k]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) maxd = max(maxd, __shfl_xor_sync(0xffffffffu, maxd, o));
+  // accepted-subtree lengths, deepest level first
+  int acc[2], dep[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = lane + 32 * k;
+    const int p = i < N ? s_par[i] : -1;
+    dep[k] = i < N ? s_dep[i] : -1;
+    acc[k] = (p >= 0 && i < nt && r_draft[k] == s_am[p]) ? 1 : 0;
+  }
+  for (int d = maxd; d >= 1; --d) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = lane + 32 * k;
+      if (dep[k] == d && acc[k]) {
+        const uint32_t len = (s_key[i] >> 16) + 1u;
+        atomicMax(&s_key[s_par[i]], (len << 16) | static_cast<uint32_t>(0xFFFF - i));
+      }
+    }
+    __syncwarp();
+  }
+  if (lane == 0) {
+    int cur = 0, n = 0;
+    s_path[0] = 0;
+    while (s_key[cur] != 0u && n < N - 1) {
+      cur = 0xFFFF - static_cast<int>(s_key[cur] & 0xFFFFu);
+      s_path[++n] = cur;
+    }
+    s_dep[0] = n;                     // reused: the accepted length for the other lanes
+    accept_len[b] = n;
+    bonus[b] = s_am[cur];
+  }
+  __syncwarp();
+  const int n = s_dep[0];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = lane + 32 * k;
+    if (i < N) path[rb + i] = i <= n ? s_path[i] : -1;
+  }
+  grid_dependents_launch();
+}
+
 struct VerifyPlan {
   int chunks;
   int chunk_len;
@@ -330,6 +486,28 @@ bool plan_verify(int B, int N, int V, VerifyPlan* p) {
   p->chunks = static_cast<int>(c);
   p->chunk_len = static_cast<int>(len);
   return true;
+}
+
+// Launches the walk over the argmax keys in `part`: one warp per sequence for small trees,
+// else the block-wide walk.  Both are programmatic dependents of the argmax grid.
+jf_status launch_walk(const uint64_t* part, int chunks, const int32_t* draft,
+                      const int32_t* parent, const int32_t* tree_len, int B, int N, int V,
+                      int32_t* argmax, int32_t* accept_len, int32_t* path, int32_t* bonus,
+                      int32_t* dev_err, cudaStream_t s) {
+  cudaError_t e;
+  if (small_walk_fits(N, chunks)) {
+    e = launch_pdl(tree_walk_small_kernel, dim3(B), dim3(32), 0, s, part, chunks, draft, parent,
+                   tree_len, N, V, argmax, accept_len, path, bonus, dev_err);
+  } else {
+    const size_t smem = static_cast<size_t>(N) * (7 * sizeof(int32_t) + sizeof(uint64_t));
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return JF_ERR_CUDA;
+    e = launch_pdl(tree_walk_kernel, dim3(B), dim3(walk_threads(N)), smem, s, part, chunks, draft,
+                   parent, tree_len, N, V, argmax, accept_len, path, bonus, dev_err);
+  }
+  return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
 
 }  // namespace
@@ -374,16 +552,8 @@ jf_status tree_verify_call(const void* logits, int32_t dtype, const int32_t* dra
                            dim3(jf::kArgmaxThreads), 0, s, static_cast<const float*>(logits), Vl,
                            p.chunks, p.chunk_len, part);
   if (ea != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * (7 * sizeof(int32_t) + sizeof(uint64_t));
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return JF_ERR_CUDA;
-  }
-  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::walk_threads(N)), smem,
-                                        s, static_cast<const uint64_t*>(part), p.chunks, draft,
-                                        parent, tree_len, N, V, argmax, accept_len, path, bonus, dev_err);
-  return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+  return jf::launch_walk(part, p.chunks, draft, parent, tree_len, B, N, V, argmax, accept_len, path,
+                         bonus, dev_err, s);
 }
 
 }  // namespace
@@ -468,13 +638,6 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
           : jf::launch_pdl(jf::argmax_chunk_kernel<float>, dim3(grid), dim3(jf::kArgmaxThreads), 0,
                            s, static_cast<const float*>(logits), Vl, p.chunks, p.chunk_len, part);
   if (ea != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * (7 * sizeof(int32_t) + sizeof(uint64_t));
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(jf::tree_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return JF_ERR_CUDA;
-  const cudaError_t ew = jf::launch_pdl(jf::tree_walk_kernel, dim3(B), dim3(jf::walk_threads(N)), smem,
-                                        s, static_cast<const uint64_t*>(part), p.chunks, draft,
-                                        parent, nullptr, N, V, argmax, accept_len, path, bonus, dev_err);
-  return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+  return jf::launch_walk(part, p.chunks, draft, parent, nullptr, B, N, V, argmax, accept_len, path,
+                         bonus, dev_err, s);
 }
