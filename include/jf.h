@@ -198,6 +198,22 @@ jf_status jf_tree_verify_static(const void* logits, int32_t dtype, const int32_t
                                 int32_t* argmax, int32_t* accept_len, int32_t* path,
                                 int32_t* bonus, int32_t* dev_err, jf_stream_t stream);
 
+/*
+ * jf_debug_set_wait_limit_ns -- test hook for the bounded waits (no counterpart in the
+ * paper).  Every wait of the tree-attention kernels on their own pipeline (a copy landing,
+ * a tensor-core step finishing, a softmax pass) gives up after limit_ns nanoseconds,
+ * sets JF_DEVERR_TIMEOUT in *dev_err and lets the kernel finish; the waits that drain a
+ * CTA's own copies and tensor-core work before it exits keep the default limit, so an
+ * abandoned call still returns with its shared memory and tensor memory released.
+ * With withhold_arrivals != 0 the warps that tell the tensor-core issuer "this key tile's
+ * data has landed" never do, so the issuer waits for a barrier phase nothing completes:
+ * the way to make a wait run out on purpose.  (0, 0) restores normal operation (one-second
+ * limit).  Applies to the CURRENT device and to calls launched after it returns (it
+ * synchronises with the device); not for use while other threads launch attention calls.
+ * Returns JF_ERR_CUDA if the device cannot be written.
+ */
+jf_status jf_debug_set_wait_limit_ns(uint64_t limit_ns, int32_t withhold_arrivals);
+
 /* ---------------------------------------------------------------- ragged trees
  * One batch may mix tree budgets: the best budget depends on the serving load (explainer
  * §4, serving performance), so sequences of one step can carry trees of different sizes.

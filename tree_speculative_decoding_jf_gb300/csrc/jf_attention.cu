@@ -112,15 +112,24 @@ struct AttnParams {
   const int32_t* tree_len;  // ragged calls: nodes per sequence (else null: N everywhere)
 };
 
+// Time limit of the kernels' bounded waits on their own pipeline (the waits that drain
+// copies and MMAs before a CTA exits always allow kWaitLimitNs).  Lowered only through
+// jf_debug_set_wait_limit_ns, to test the timeout path.
+__device__ uint64_t g_wait_limit_ns = kWaitLimitNs;
+// Test hook: non-zero makes the data-voucher warps withhold their arrivals, so the MMA
+// issuer waits for a barrier phase that can never complete (a wait nothing satisfies).
+__device__ int g_withhold_vouchers = 0;
+
 // Nodes of sequence b's tree: N, or tree_len[b] clamped to [1, N] for ragged calls.  The
 // tree's keys are the n positions after the prefix, so the sequence has P_b + n keys.
 __device__ __forceinline__ int tree_nodes(const int32_t* tree_len, int b, int N) {
   return tree_len == nullptr ? N : max(1, min(tree_len[b], N));
 }
 
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t wlim) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, wlim) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   return ok != 0;
 }
@@ -262,7 +271,7 @@ __device__ __forceinline__ bool softmax_tile(uint64_t* s_full_bar, uint32_t pari
                                              uint32_t tS, uint32_t tO, const uint64_t* mrow,
                                              bool valid, int W, int key0, int P, int L, float sl2,
                                              bool not_first, volatile int* lo_flag, bool writer,
-                                             float& m_run, float& l) {
+                                             float& m_run, float& l, uint64_t wlim) {
   uint64_t mw[3] = {0ull, 0ull, 0ull};
   const int w_lo = MASKED ? (max(key0 - P, 0) >> 6) : 0;
   if constexpr (MASKED) {
@@ -272,7 +281,7 @@ __device__ __forceinline__ bool softmax_tile(uint64_t* s_full_bar, uint32_t pari
         if (w_lo + u < W) mw[u] = __ldg(reinterpret_cast<const unsigned long long*>(mrow) + w_lo + u);
     }
   }
-  if (!wait_warp(s_full_bar, parity, abort)) return false;
+  if (!wait_warp(s_full_bar, parity, abort, wlim)) return false;
   if (lo_flag != nullptr && writer) *lo_flag = SPLIT ? 1 : 0;
   tc_fence_after();
   uint32_t sr[128];
@@ -511,6 +520,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     tma_prefetch_desc(&kmap_run);
     tma_prefetch_desc(&vmap_run);
   }
+  const uint64_t wlim = g_wait_limit_ns;
   grid_dependency_wait();
 
   int b = slot;
@@ -652,7 +662,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       int okl = 1;
       if (lane == 0) {
         if (rec >= 0 && !mbar_wait(&step_done[rec % kStepRing],
-                                   static_cast<uint32_t>(rec / kStepRing) & 1u, abort)) {
+                                   static_cast<uint32_t>(rec / kStepRing) & 1u, abort, wlim)) {
           okl = 0;
         } else {
           mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
@@ -672,7 +682,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     const int last_key0 = (k0 + T - 1) * kKeyTile;
     if (ok && last_key0 + kKeyTile > L) {
       const int jl = T - 1;
-      if (!wait_warp(&v_full[jl % SV], static_cast<uint32_t>(jl / SV) & 1u, abort)) {
+      if (!wait_warp(&v_full[jl % SV], static_cast<uint32_t>(jl / SV) & 1u, abort, wlim)) {
         ok = false;
       } else {
         const int r0 = L - last_key0;
@@ -731,7 +741,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                (acc || kk > 0) ? 1u : 0u);
       if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
-    bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
+    bool ok = wait_warp(&q_full, 0, abort, wlim) && wait_warp(&k_full[0], 0, abort, wlim);
     if (ok && lane == 0) {
       tc_fence_after();
       for (int t = 0; t < NT; ++t) {
@@ -783,7 +793,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           idle = 0;
         } else {
           if (idle == 0) idle_since = global_timer_ns();
-          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > kWaitLimitNs)) {
+          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > wlim)) {
             ok = false;
             break;
           }
@@ -791,7 +801,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       }
       for (int j = j_tree; j < T && ok; ++j) {
         for (int t = 0; t < NT && ok; ++t) {
-          if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j) & 1u, abort)) {
+          if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j) & 1u, abort, wlim)) {
             ok = false;
             break;
           }
@@ -822,14 +832,14 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     // first, so its arrival cannot count toward an earlier phase.
     const int t = warp - 2;
     const bool tail = (k0 + T) * kKeyTile > L;
-    if (lane == 0) {
+    if (lane == 0 && g_withhold_vouchers == 0) {
       for (int j = 0; j < T; ++j) {
         const bool ready =
-            (j == 0 || mbar_wait(&p_full[t], static_cast<uint32_t>(j - 1) & 1u, abort)) &&
-            mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, abort) &&
+            (j == 0 || mbar_wait(&p_full[t], static_cast<uint32_t>(j - 1) & 1u, abort, wlim)) &&
+            mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, abort, wlim) &&
             (j + 1 >= T ||
-             mbar_wait(&k_full[(j + 1) % SK], static_cast<uint32_t>((j + 1) / SK) & 1u, abort)) &&
-            (j + 1 < T || !tail || mbar_wait(&v_tail, 0u, abort));
+             mbar_wait(&k_full[(j + 1) % SK], static_cast<uint32_t>((j + 1) / SK) & 1u, abort, wlim)) &&
+            (j + 1 < T || !tail || mbar_wait(&v_tail, 0u, abort, wlim));
         if (!ready) {
           set_abort(abort, p.dev_err);
           break;
@@ -866,21 +876,21 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     for (int j = 0; j < jm && ok; ++j)
       ok = softmax_tile<false, false, D>(&s_full[t], static_cast<uint32_t>(j) & 1u, abort, &p_full[t], tS, tO,
                                   mrow, valid, W, (k0 + j) * kKeyTile, P, L, sl2, j > 0, nullptr,
-                                  false, m_run, l);
+                                  false, m_run, l, wlim);
     if (P < kSplitPrefix) {
       for (int j = jm; j < T && ok; ++j)
         ok = softmax_tile<true, true, D>(&s_full[t], static_cast<uint32_t>(j) & 1u, abort, &p_full[t], tS,
                                          tO, mrow, valid, W, (k0 + j) * kKeyTile, P, L, sl2, j > 0,
-                                         nullptr, false, m_run, l);
+                                         nullptr, false, m_run, l, wlim);
     } else {
       for (int j = jm; j < T && ok; ++j)
         ok = softmax_tile<true, false, D>(&s_full[t], static_cast<uint32_t>(j) & 1u, abort, &p_full[t],
                                           tS, tO, mrow, valid, W, (k0 + j) * kKeyTile, P, L, sl2, j > 0,
-                                          nullptr, false, m_run, l);
+                                          nullptr, false, m_run, l, wlim);
     }
     // Every thread of the warpgroup reaches this vote (all waits are bounded), so the
     // epilogue's own barriers are entered by all of them or by none.
-    const bool done = named_bar_and(1 + t, 128, ok && wait_warp(&o_full, 0, abort));
+    const bool done = named_bar_and(1 + t, 128, ok && wait_warp(&o_full, 0, abort, wlim));
     if (p.cluster_merge) {
       // Normalised fp32 row and its LSE stay in this CTA's shared memory for the merge.
       float lse2 = -INFINITY;
@@ -1099,12 +1109,13 @@ __device__ __forceinline__ int count_acquire(int* c) {
   asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(c)) : "memory");
   return v;
 }
-__device__ __forceinline__ bool wait_count_above(int* c, int target, volatile int* abort) {
+__device__ __forceinline__ bool wait_count_above(int* c, int target, volatile int* abort,
+                                                 uint64_t wlim) {
   if (count_acquire(c) > target) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (count_acquire(c) > target) return true;
-    if ((it & 255u) == 0u && (*abort || global_timer_ns() - t0 > kWaitLimitNs)) return false;
+    if ((it & 255u) == 0u && (*abort || global_timer_ns() - t0 > wlim)) return false;
   }
 }
 
@@ -1160,6 +1171,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     tma_prefetch_desc(&kmap_run);
     tma_prefetch_desc(&vmap_run);
   }
+  const uint64_t wlim = g_wait_limit_ns;
   grid_dependency_wait();
 
   // ---- the schedule: tiles per sequence, their running sums, this range's segments
@@ -1229,7 +1241,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       if (lane == 0) {
         const int rq = jg0 - 1;   // S of the previous segment's last tile: step record rq
         if (s > 0 && !mbar_wait(&step_done[rq % kStepRing], static_cast<uint32_t>(rq / kStepRing) & 1u,
-                                abort)) {
+                                abort, wlim)) {
           okq = 0;
         } else {
           mbar_arrive_expect_tx(&q_full, NT * C::kTileBytes);
@@ -1268,7 +1280,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         int okl = 1;
         if (lane == 0) {
           if (rec >= 0 && !mbar_wait(&step_done[rec % kStepRing],
-                                     static_cast<uint32_t>(rec / kStepRing) & 1u, abort)) {
+                                     static_cast<uint32_t>(rec / kStepRing) & 1u, abort, wlim)) {
             okl = 0;
           } else {
             mbar_arrive_expect_tx(&k_full[sk], C::kTileBytes);
@@ -1286,7 +1298,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       // make them zero, then release the tile to the MMA issuer's voucher (every segment).
       const int jl = jg0 + T - 1;
       if ((sg.k1) * kKeyTile > L) {
-        if (!wait_warp(&v_full[jl % SV], static_cast<uint32_t>(jl / SV) & 1u, abort)) { ok = false; break; }
+        if (!wait_warp(&v_full[jl % SV], static_cast<uint32_t>(jl / SV) & 1u, abort, wlim)) { ok = false; break; }
         const int r0 = L - (sg.k1 - 1) * kKeyTile;
         uint8_t* vt = v_s + (jl % SV) * C::kTileBytes;
         const int per_half = (kKeyTile - r0) * 8;
@@ -1341,7 +1353,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
                (acc || kk > 0) ? 1u : 0u);
       if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
-    bool ok = wait_warp(&q_full, 0, abort) && wait_warp(&k_full[0], 0, abort);
+    bool ok = wait_warp(&q_full, 0, abort, wlim) && wait_warp(&k_full[0], 0, abort, wlim);
     if (ok && lane == 0) {
       tc_fence_after();
       for (int t = 0; t < NT; ++t) {
@@ -1382,7 +1394,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           idle = 0;
         } else {
           if (idle == 0) idle_since = global_timer_ns();
-          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > kWaitLimitNs)) {
+          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > wlim)) {
             ok = false;
             break;
           }
@@ -1404,18 +1416,18 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     // segment, and, when another segment follows, that segment's Q (its first S MMAs are
     // issued in this tile's step).
     const int t = warp - 2;
-    if (lane == 0) {
+    if (lane == 0 && g_withhold_vouchers == 0) {
       int s = 0, e = seg_end(0);
       for (int j = 0; j < Wc; ++j) {
         const bool last_of_seg = j + 1 == e;
         const bool ready =
-            (j == 0 || mbar_wait(&p_full[t], static_cast<uint32_t>(j - 1) & 1u, abort)) &&
-            mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, abort) &&
+            (j == 0 || mbar_wait(&p_full[t], static_cast<uint32_t>(j - 1) & 1u, abort, wlim)) &&
+            mbar_wait(&v_full[j % SV], static_cast<uint32_t>(j / SV) & 1u, abort, wlim) &&
             (j + 1 >= Wc ||
-             mbar_wait(&k_full[(j + 1) % SK], static_cast<uint32_t>((j + 1) / SK) & 1u, abort)) &&
-            (!last_of_seg || wait_count_above(&s_tails, s, abort)) &&
+             mbar_wait(&k_full[(j + 1) % SK], static_cast<uint32_t>((j + 1) / SK) & 1u, abort, wlim)) &&
+            (!last_of_seg || wait_count_above(&s_tails, s, abort, wlim)) &&
             (!last_of_seg || j + 1 >= Wc ||
-             mbar_wait(&q_full, static_cast<uint32_t>(s + 1) & 1u, abort));
+             mbar_wait(&q_full, static_cast<uint32_t>(s + 1) & 1u, abort, wlim));
         if (!ready) {
           set_abort(abort, p.dev_err);
           break;
@@ -1461,29 +1473,27 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       for (int j = 0; j < jm && ok; ++j)
         ok = softmax_tile<false, false, D>(&s_full[t], static_cast<uint32_t>(jg0 + j) & 1u, abort, &p_full[t],
                                     tS, tO, mrow, valid, W, (sgm.k0 + j) * kKeyTile, P, L, sl2, j > 0,
-                                    lo_flag, rl == 0, m_run, l);
+                                    lo_flag, rl == 0, m_run, l, wlim);
       if (P < kSplitPrefix) {
         for (int j = jm; j < T && ok; ++j)
           ok = softmax_tile<true, true, D>(&s_full[t], static_cast<uint32_t>(jg0 + j) & 1u, abort,
                                            &p_full[t], tS, tO, mrow, valid, W, (sgm.k0 + j) * kKeyTile, P,
-                                           L, sl2, j > 0, lo_flag, rl == 0, m_run, l);
+                                           L, sl2, j > 0, lo_flag, rl == 0, m_run, l, wlim);
       } else {
         for (int j = jm; j < T && ok; ++j)
           ok = softmax_tile<true, false, D>(&s_full[t], static_cast<uint32_t>(jg0 + j) & 1u, abort,
                                             &p_full[t], tS, tO, mrow, valid, W, (sgm.k0 + j) * kKeyTile, P,
-                                            L, sl2, j > 0, lo_flag, rl == 0, m_run, l);
+                                            L, sl2, j > 0, lo_flag, rl == 0, m_run, l, wlim);
       }
-      if (!ok) {
-        if (lane == 0) set_abort(abort, p.dev_err);
-        break;
-      }
+      // A failed wait still reaches the warpgroup vote below (every warp must enter it).
+      if (!ok && lane == 0) set_abort(abort, p.dev_err);
       // ---- the segment's rows: O / l, straight from TMEM to global memory, once its last
       // PV is done: S of the next tile (committed after it) or, for the range's last
       // segment, o_full.  Every warp of the warpgroup reaches this vote (all waits are
       // bounded), so it is all-or-none.
       const int je = jg0 + T;
-      const bool pv_done = ok && (je < Wc ? wait_warp(&s_full[t], static_cast<uint32_t>(je) & 1u, abort)
-                                          : wait_warp(&o_full, 0u, abort));
+      const bool pv_done = ok && (je < Wc ? wait_warp(&s_full[t], static_cast<uint32_t>(je) & 1u, abort, wlim)
+                                          : wait_warp(&o_full, 0u, abort, wlim));
       if (!named_bar_and(1 + t, 128, pv_done)) {
         ok = false;
         break;
@@ -2152,4 +2162,15 @@ extern "C" jf_status jf_tree_attention_ragged(const void* q, const void* k_cache
   return tree_attention_call(q, k_cache, v_cache, block_table, prefix_len, tree_len, mask, B, N,
                              Hq, Hkv, D, page_size, max_pages, num_pages, scale, out, lse,
                              workspace, workspace_bytes, dev_err, stream);
+}
+
+extern "C" jf_status jf_debug_set_wait_limit_ns(uint64_t limit_ns, int32_t withhold_arrivals) {
+  const uint64_t v = limit_ns == 0 ? jf::kWaitLimitNs : limit_ns;
+  const int w = withhold_arrivals != 0 ? 1 : 0;
+  if (cudaMemcpyToSymbol(jf::g_wait_limit_ns, &v, sizeof(v)) != cudaSuccess ||
+      cudaMemcpyToSymbol(jf::g_withhold_vouchers, &w, sizeof(w)) != cudaSuccess) {
+    cudaGetLastError();
+    return JF_ERR_CUDA;
+  }
+  return JF_OK;
 }

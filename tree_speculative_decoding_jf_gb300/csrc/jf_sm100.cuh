@@ -58,16 +58,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s
 
 // Waits for the phase with the given parity to complete.  Gives up (returns false) when
-// *abort becomes non-zero (another role of the CTA gave up) or after kWaitLimitNs.
+// *abort becomes non-zero (another role of the CTA gave up) or after limit_ns.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort) {
+                                          volatile int* abort, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -70,6 +70,8 @@ def _load():
     lib.jf_tree_attention_ragged.restype = ctypes.c_int
     lib.jf_tree_verify_ragged.argtypes = [P, i32, P, P, P, i32, i32, i32, P, P, P, P, P, sz, P, P]
     lib.jf_tree_verify_ragged.restype = ctypes.c_int
+    lib.jf_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+    lib.jf_debug_set_wait_limit_ns.restype = ctypes.c_int
     return lib
 
 
@@ -111,6 +113,14 @@ def jf_status_string(status: int) -> str:
 
 def jf_version() -> int:
     return _lib.jf_version()
+
+
+def jf_debug_set_wait_limit_ns(limit_ns: int, withhold_arrivals: bool = False) -> None:
+    """Test hook: time limit of the attention kernels' pipeline waits on the current device,
+    optionally with the data-arrival signals withheld so a wait can never complete
+    ((0, False) restores normal operation).  See include/jf.h."""
+    _check("jf_debug_set_wait_limit_ns",
+           _lib.jf_debug_set_wait_limit_ns(int(limit_ns), 1 if withhold_arrivals else 0))
 
 
 def jf_build_tree_mask(parent, prefix_len, mask, depth=None, pos=None, dev_err=None,
