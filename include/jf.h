@@ -183,7 +183,9 @@ jf_status jf_tree_verify(const void* logits, int32_t dtype, const int32_t* draft
  * loads the library keeps until the process exits.  The call itself allocates nothing.
  *   - The first call on each device looks up the array's device address with
  *     cudaGetSymbolAddress (a runtime query, no allocation) while that device is current,
- *     and caches it; make that first call before any stream capture.
+ *     and caches it for the life of the process; make that first call before any stream
+ *     capture.  The cache does not survive a reset of the device's context
+ *     (cudaDeviceReset): do not use this call on a device after resetting it.
  *   - Capacity: B * N * chunks entries, where chunks = jf_tree_verify_workspace_size(B, N,
  *     V) / (8 * B * N).  Larger problems return JF_ERR_SCRATCH_CAPACITY and launch nothing.
  *   - The array is shared by every call and keeps the last call's contents; nothing in it

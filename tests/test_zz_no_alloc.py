@@ -1,14 +1,16 @@
 """jf_tree_verify_static -- the allocation-free verify entry point for callers that cannot
 allocate device memory on their call path -- must give the same argmax, accepted length,
-path and bonus as jf_tree_verify (integer outputs: bit-exact), on two calls in a row
-with different inputs (the shared scratch keeps the previous call's contents, which
-must not leak).  The call goes straight through the C ABI with raw device pointers."""
+path and bonus as jf_tree_verify and as the fp64 oracle (integer outputs: bit-exact), on
+two calls in a row with different inputs (the shared scratch keeps the previous call's
+contents, which must not leak).  The call goes straight through the C ABI with raw
+device pointers."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from tree_speculative_decoding_jf_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +29,7 @@ def _inputs(seed, B, N, V, dtype):
     w = wl.make_workload("noalloc", B, N, 4, 1, 64, V, 32, tree="random_depth_limited",
                          logits_dtype=dtype, forcing="half", seed=seed)
     t = wl.device_tensors(w)
-    return t["logits"], t["draft"], t["parent"]
+    return t["logits"], t["draft"], t["parent"], w
 
 
 def test_static_verify_matches_workspace_verify_twice():
@@ -37,7 +39,7 @@ def test_static_verify_matches_workspace_verify_twice():
     lib = jf._lib
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for seed, (B, N, V, dtype) in enumerate([(3, 40, 151936, "bf16"), (2, 17, 5003, "f32")]):
-        logits, draft, parent = _inputs(seed, B, N, V, dtype)
+        logits, draft, parent, w = _inputs(seed, B, N, V, dtype)
         dt = jf.JF_DTYPE_BF16 if dtype == "bf16" else jf.JF_DTYPE_F32
         # existing entry point, with its own workspace
         ref = _outputs(B, N)
@@ -56,6 +58,9 @@ def test_static_verify_matches_workspace_verify_twice():
         for a, b in zip(ref, got):
             assert torch.equal(a, b)
         assert got[4].item() == 0 and got[1].min().item() >= 0
+        ram, racc, rpath, rbonus = oracle.tree_verify(w)
+        assert (got[0].cpu().numpy() == ram).all() and (got[1].cpu().numpy() == racc).all()
+        assert (got[2].cpu().numpy() == rpath).all() and (got[3].cpu().numpy() == rbonus).all()
 
 
 def test_static_verify_rejects_sizes_beyond_its_scratch():

@@ -24,6 +24,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <mutex>
+
 #include "jf_common.cuh"
 #include "jf_sm100.cuh"
 
@@ -627,14 +629,19 @@ extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype
                                cand_logp);
   if (e != cudaSuccess) return JF_ERR_CUDA;
   constexpr size_t kTreeSmem = 4 * jf::kSortCap * sizeof(uint64_t);
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
-  if (dev >= 64 || !attr_set[dev]) {
-    if (cudaFuncSetAttribute(jf::best_first_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kTreeSmem)) != cudaSuccess)
-      return JF_ERR_CUDA;
-    if (dev < 64) attr_set[dev] = true;
+  {
+    // Once per device; host threads calling concurrently serialise on the mutex.
+    static std::mutex mu;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return JF_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 64 || !attr_set[dev]) {
+      if (cudaFuncSetAttribute(jf::best_first_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kTreeSmem)) != cudaSuccess)
+        return JF_ERR_CUDA;
+      if (dev < 64) attr_set[dev] = true;
+    }
   }
   e = jf::launch_pdl(jf::best_first_tree_kernel, dim3(static_cast<unsigned>(B)), dim3(jf::kTreeThreads), kTreeSmem, s,
                      static_cast<const int32_t*>(cand_token), static_cast<const float*>(cand_logp),
