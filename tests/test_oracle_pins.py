@@ -670,3 +670,124 @@ def test_best_first_invariants_random():
         assert 0 <= p < i and depth[i] == depth[p] + 1 and score[i] <= score[p]
         assert draft[i] in tok[0, depth[i] - 1]
     assert depth.max() <= 16
+
+
+# ---------------------------------------------------------------- stochastic verification
+
+from oracle import sampled_verify as osv    # noqa: E402
+
+
+def _golden_sampled_cases():
+    cases, cur = [], None
+    for ln in read_golden("sampled_verify.txt"):
+        key, val = ln.split(":", 1)
+        key = key.strip()
+        if key == "case":
+            cur = {"name": val.strip(), "p": []}
+            cases.append(cur)
+        elif key == "expect":
+            a, p, bo = val.split("|")
+            cur["expect"] = (int(a), [int(x) for x in p.split()], int(bo))
+        elif key.startswith("p") and key[1:].isdigit():
+            cur["p"].append([float(x) for x in val.split()])
+        elif key == "bonus_uniform":
+            cur["bonus_uniform"] = float(val)
+        else:
+            cur[key] = np.array([float(x) for x in val.split()])
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_sampled_cases(), ids=lambda c: c["name"])
+def test_sampled_verify_golden(case):
+    logits = np.log(np.array(case["p"], np.float64)).astype(np.float32)[None]
+    acc, path, bonus, margins = osv.tree_verify_sampled(
+        logits, "f32", case["draft"].astype(np.int32)[None], case["parent"].astype(np.int32)[None],
+        case["uniform"][None], np.array([case["bonus_uniform"]]), 1.0)
+    a, p, bo = case["expect"]
+    assert acc[0] == a and list(path[0]) == p and bonus[0] == bo
+    assert min(m for _, _, m in margins[0]) > 0.01      # no decision sits on a boundary
+
+
+def _chi2_ok(counts, probs, n):
+    """Pearson chi-square of observed counts against n * probs; loose bound (the seeds are
+    fixed, so this is deterministic) that still rejects a wrong distribution."""
+    exp = probs * n
+    stat = float(((counts - exp) ** 2 / np.maximum(exp, 1e-12)).sum())
+    return stat < 40.0, stat
+
+
+def test_sampled_verify_emits_the_target_distribution():
+    """Losslessness: over many draws of the random numbers, the first emitted token follows
+    p(root) and, given that child 1 (resp. 2) was accepted, the second follows p(1) (resp.
+    p(2)) -- whatever the drafted tokens are."""
+    rng = np.random.default_rng(0)
+    V, T = 6, 0.8
+    parent = np.array([-1, 0, 0, 0, 1, 1, 2], np.int32)
+    draft = np.array([0, 2, 0, 5, 1, 3, 4], np.int32)
+    N = len(parent)
+    rows = rng.standard_normal((N, V)).astype(np.float32)
+    n = 40000
+    logits = np.broadcast_to(rows, (n, N, V))
+    par = np.broadcast_to(parent, (n, N))
+    dr = np.broadcast_to(draft, (n, N))
+    acc, path, bonus, _ = osv.tree_verify_sampled(logits, "f32", dr, par, rng.random((n, N)),
+                                                  rng.random(n), T)
+    first = np.where(acc >= 1, draft[np.maximum(path[:, 1], 0)], bonus)
+    ok, stat = _chi2_ok(np.bincount(first, minlength=V), osv.target_probs(rows[0].astype(np.float64), T), n)
+    assert ok, stat
+    for c in (1, 2):
+        sel = (acc >= 1) & (path[:, 1] == c)
+        second = np.where(acc[sel] >= 2, draft[np.maximum(path[sel, 2], 0)], bonus[sel])
+        ok, stat = _chi2_ok(np.bincount(second, minlength=V),
+                            osv.target_probs(rows[c].astype(np.float64), T), int(sel.sum()))
+        assert ok, (c, stat)
+
+
+def test_sampled_verify_wrong_residual_is_detected():
+    """The distribution test has teeth: renormalising without removing rejected tokens
+    (a plausible slip) changes the first token's distribution enough to fail it."""
+    rng = np.random.default_rng(1)
+    V, T = 6, 0.8
+    rows = rng.standard_normal((4, V)).astype(np.float64)
+    p = osv.target_probs(rows[0], T)
+    drafts = [2, 0, 5]
+    n = 40000
+    counts = np.zeros(V)
+    for _ in range(n):                      # the slip: r never loses the rejected tokens
+        y = None
+        for x in drafts:
+            if rng.random() < p[x]:
+                y = x
+                break
+        if y is None:
+            y = int(np.searchsorted(np.cumsum(p), rng.random(), side="right"))
+        counts[y] += 1
+    assert not _chi2_ok(counts, p, n)[0]
+
+
+def test_sampled_verify_at_low_temperature_is_greedy():
+    """T -> 0 makes p one-hot at the argmax: a child is accepted iff its token is the
+    parent's argmax, and the bonus is the argmax at the last node -- the greedy walk (with
+    distinct sibling tokens, at most one child per node can match)."""
+    rng = np.random.default_rng(2)
+    B, N, V = 6, 24, 50
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - 4), i) for i in range(1, N)])
+                       for _ in range(B)]).astype(np.int32)
+    logits = (rng.standard_normal((B, N, V)) * 2).astype(np.float32)
+    am = logits.argmax(-1)
+    srt = np.sort(logits, -1)
+    assert (srt[..., -1] - srt[..., -2]).min() > 1e-3
+    draft = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for p_ in range(N):
+            kids = np.flatnonzero(parent[b] == p_)
+            toks = rng.permutation(V)[:len(kids)]
+            if len(kids) and rng.random() < 0.7:
+                toks[rng.integers(len(kids))] = am[b, p_] if am[b, p_] not in toks else toks[0]
+            draft[b, kids] = toks
+    acc, path, bonus, _ = osv.tree_verify_sampled(logits, "f32", draft, parent,
+                                                  rng.uniform(0.01, 0.99, (B, N)),
+                                                  rng.uniform(0.01, 0.99, B), 1e-5)
+    racc, rpath, rbonus = oracle.tree_walk(am.astype(np.int32), draft, parent)
+    assert (acc == racc).all() and (path == rpath).all() and (bonus == rbonus).all()
+    assert racc.max() >= 2
