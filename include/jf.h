@@ -216,6 +216,42 @@ jf_status jf_tree_verify_static(const void* logits, int32_t dtype, const int32_t
  */
 jf_status jf_debug_set_wait_limit_ns(uint64_t limit_ns, int32_t withhold_arrivals);
 
+/*
+ * jf_tree_verify_sampled -- lossless (stochastic) tree verification.  The pages call
+ * draft-then-verify lossless -- the output follows the target model's distribution
+ * (qxai.app commentary, "まず、何が問題なのか" and "慎重に見るべき点"; explainer §1) --
+ * without giving the rule; this call uses the multi-step speculative sampling of SpecInfer
+ * (Miao et al., ASPLOS 2024) for deterministic drafts, whose children are fixed candidate
+ * tokens (point-mass draft distributions):
+ *   p_u = softmax(logits[b][u] / temperature) at node u, starting at the root;
+ *   the children c of u are tested in increasing node id: with R the probability mass of
+ *   p_u left after removing the tokens rejected so far at u, c (token x = draft[b][c]) is
+ *   accepted iff uniform[b][c] * R < p_u(x) with x not yet removed; on acceptance the walk
+ *   continues at c, on rejection x is removed;
+ *   when no child of u is accepted (or u has none), bonus[b] = the smallest token y whose
+ *   cumulative residual probability exceeds bonus_uniform[b] * R.
+ *   accept_len[b] = accepted nodes; path[b] = root, then the accepted nodes, -1 padded.
+ * Every emitted token (accepted drafts, then the bonus) is then a sample of the target's
+ * distribution at its position.
+ *   logits         [B][N][V] bf16 or fp32 (dtype), finite.
+ *   uniform        float [B][N] in [0, 1): the number drawn when node c is tested (entry
+ *                  0 unused; each node is tested at most once).
+ *   bonus_uniform  float [B] in [0, 1).
+ *   temperature    > 0.
+ *   workspace      at least jf_tree_verify_workspace_size(B, N, V) bytes, no initialisation.
+ *   dev_err        JF_DEVERR_BAD_PARENT / _BAD_TOKEN.  May be NULL.
+ * Precision: p is computed in fp64 from per-chunk fp32 maxima and Kahan-compensated fp32
+ * sums of exponentials (relative error about 1e-6), so a decision whose threshold lies
+ * closer than that to its boundary may differ from an exact computation.
+ * Limits: 1 <= N <= JF_MAX_NODES, 1 <= V < 2^31.
+ */
+jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, const int32_t* draft,
+                                 const int32_t* parent, const float* uniform,
+                                 const float* bonus_uniform, float temperature, int32_t B,
+                                 int32_t N, int32_t V, int32_t* accept_len, int32_t* path,
+                                 int32_t* bonus, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_err, jf_stream_t stream);
+
 /* ---------------------------------------------------------------- ragged trees
  * One batch may mix tree budgets: the best budget depends on the serving load (explainer
  * §4, serving performance), so sequences of one step can carry trees of different sizes.

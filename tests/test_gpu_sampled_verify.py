@@ -1,0 +1,152 @@
+"""GPU parity for lossless (stochastic) tree verification (jf_tree_verify_sampled through
+the C ABI) against the fp64 oracle, on the same seeded logits, trees and random numbers.
+
+Each decision compares a drawn threshold with a probability.  The kernel's probabilities
+carry a relative error of about 1e-6 (fp32 chunk sums of exponentials), and its residual
+CDF an absolute error below about 1e-6 of the residual mass.  So:
+  - when every accept/reject decision of a sequence lies further than 1e-5 (relative to
+    the residual mass) from its boundary, the accepted length and path must equal the
+    oracle's;
+  - the bonus token must then equal the oracle's when its draw lies further than 1e-5 from
+    a CDF step, and otherwise (common over 151936 tokens, where one token holds about 7e-6
+    of the mass) lie in the right place: the drawn threshold inside the token's exact fp64
+    CDF interval, widened by 1e-6;
+  - a sequence with a closer accept/reject decision (rare) is checked for validity only."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sampled_verify as osv
+from tree_speculative_decoding_jf_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+MARGIN = 1e-5
+
+
+@pytest.fixture(scope="module")
+def jf():
+    from tree_speculative_decoding_jf_gb300 import build
+    build.build()
+    from tree_speculative_decoding_jf_gb300 import jf as mod
+    return mod
+
+
+def logits_tensor(x, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda()
+
+
+def check(jf, logits, dtype, draft, parent, T, seed, min_exact=0.9):
+    B, N = parent.shape
+    u, bu = wl.sampling_uniforms(B, N, seed)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc, path, bonus = jf.tree_verify_sampled(
+        logits_tensor(logits, dtype), torch.from_numpy(np.ascontiguousarray(draft, np.int32)).cuda(),
+        torch.from_numpy(np.ascontiguousarray(parent, np.int32)).cuda(), torch.from_numpy(u).cuda(),
+        torch.from_numpy(bu).cuda(), T, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    acc, path, bonus = acc.cpu().numpy(), path.cpu().numpy(), bonus.cpu().numpy()
+    racc, rpath, rbonus, margins = osv.tree_verify_sampled(logits, dtype, draft, parent, u, bu, T)
+    rows = osv._rows_f64(logits, dtype)
+    V = logits.shape[-1]
+    exact = 0
+    for b in range(B):
+        walk = [m for k, _, m in margins[b] if k != "bonus"]
+        bonus_margin = [m for k, _, m in margins[b] if k == "bonus"][0]
+        if not walk or min(walk) > MARGIN:
+            assert acc[b] == racc[b] and (path[b] == rpath[b]).all(), b
+            exact += 1
+            if bonus_margin > MARGIN:
+                assert bonus[b] == rbonus[b], b
+            else:                               # the draw sits within a CDF step of y
+                f = path[b, acc[b]]
+                r = osv.target_probs(rows[b, f], T)
+                for c in np.flatnonzero(parent[b] == f):
+                    r[draft[b, c]] = 0.0
+                cdf = np.cumsum(r)
+                y = int(bonus[b])
+                target = float(bu[b]) * r.sum()
+                lo = cdf[y - 1] if y > 0 else 0.0
+                tol = 1e-6 * r.sum()
+                assert r[y] > 0 and lo - tol <= target <= cdf[y] + tol, (b, y, rbonus[b])
+        else:                                   # a near-boundary decision: validity only
+            n = acc[b]
+            assert path[b, 0] == 0 and (path[b, n + 1:] == -1).all()
+            assert all(parent[b, path[b, k + 1]] == path[b, k] for k in range(n))
+            assert 0 <= bonus[b] < V
+    assert exact >= min_exact * B, f"only {exact} of {B} sequences decided away from boundaries"
+    return racc
+
+
+@pytest.mark.parametrize("T", [0.7, 1.0, 2.5])
+def test_small_vocab_mixed_decisions(jf, T):
+    """V = 8, each child's token drawn from its parent's target distribution: acceptances
+    and rejections mix, paths chain, and the residual bonus draw matters."""
+    rng = np.random.default_rng(int(T * 10))
+    B, N, V = 32, 48, 8
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - 5), i) for i in range(1, N)])
+                       for _ in range(B)]).astype(np.int32)
+    logits = (rng.standard_normal((B, N, V)) * 1.5).astype(np.float32)
+    draft = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for c in range(1, N):
+            p = osv.target_probs(logits[b, parent[b, c]].astype(np.float64), T)
+            draft[b, c] = rng.choice(V, p=p)
+    racc = check(jf, logits, "f32", draft, parent, T, seed=int(T * 10))
+    assert racc.max() >= 2
+
+
+@pytest.mark.parametrize("name", ["c1_tiny_random16", "c3_qwen3_8b_tree256"])
+def test_workloads_forced_drafts(jf, name):
+    """Workload logits with half the children's tokens planted as their parent's maximum
+    (probability close to 1): long accepted paths, then a bonus drawn from the residual of
+    the full vocabulary (151936 bf16 logits on workload 3)."""
+    w = wl.config(name, forcing="half")
+    racc = check(jf, w.logits, w.logits_dtype, w.draft, w.parent, 1.0, seed=3)
+    assert racc.max() >= 1
+
+
+def test_chain_with_five_planted_acceptances(jf):
+    w = wl.config("c2_qwen3_8b_chain16")
+    racc = check(jf, w.logits, w.logits_dtype, w.draft, w.parent, 1.0, seed=4)
+    assert (racc == 5).all()
+
+
+def test_low_temperature_is_the_greedy_walk(jf):
+    """T -> 0: the stochastic rule accepts exactly the children whose token is the parent's
+    argmax and the bonus is the argmax (distinct sibling tokens)."""
+    w = wl.config("c1_tiny_random16", forcing="half")
+    logits = w.logits.astype(np.float32)
+    B, N = w.parent.shape
+    draft = w.draft.copy()
+    for b in range(B):
+        for p_ in range(N):
+            kids = np.flatnonzero(w.parent[b] == p_)
+            seen = set()
+            for c in kids:
+                while int(draft[b, c]) in seen:
+                    draft[b, c] = (draft[b, c] + 1) % w.V
+                seen.add(int(draft[b, c]))
+    u, bu = wl.sampling_uniforms(B, N, 5)
+    acc, path, bonus = jf.tree_verify_sampled(
+        logits_tensor(logits, "f32"), torch.from_numpy(draft).cuda(),
+        torch.from_numpy(w.parent).cuda(), torch.from_numpy(np.clip(u, 0.01, 0.99)).cuda(),
+        torch.from_numpy(np.clip(bu, 0.01, 0.99)).cuda(), 1e-4)
+    am, gacc, gpath, gbonus = jf.tree_verify(logits_tensor(logits, "f32"), torch.from_numpy(draft).cuda(),
+                                             torch.from_numpy(w.parent).cuda())
+    torch.cuda.synchronize()
+    assert (acc.cpu() == gacc.cpu()).all() and (path.cpu() == gpath.cpu()).all()
+    assert (bonus.cpu() == gbonus.cpu()).all()
+
+
+def test_reports_bad_tokens(jf):
+    lg = torch.randn(1, 4, 50, device="cuda")
+    par = torch.tensor([[-1, 0, 0, 1]], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    u = torch.full((1, 4), 0.5, device="cuda")
+    jf.tree_verify_sampled(lg, torch.tensor([[0, 3, 99, 1]], dtype=torch.int32, device="cuda"), par,
+                           u, torch.full((1,), 0.5, device="cuda"), 1.0, dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == jf.DEVERR_BAD_TOKEN

@@ -16,6 +16,7 @@
 // and walks the best children from the root.  Trees of at most 64 nodes take a one-warp
 // version of the same steps with no block barriers.
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "jf_common.cuh"
@@ -640,4 +641,387 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
   if (ea != cudaSuccess) return JF_ERR_CUDA;
   return jf::launch_walk(part, p.chunks, draft, parent, nullptr, B, N, V, argmax, accept_len, path,
                          bonus, dev_err, s);
+}
+
+// ------------------------------------------------------------------------ stochastic verify
+// jf_tree_verify_sampled: lossless acceptance instead of argmax matching.  The target
+// distribution of node u is p = softmax(logits[u] / T).  Children of u are tested in
+// increasing node id: child c with token x is accepted iff uniform[c] * R < p(x), R the
+// probability mass left after removing the tokens rejected so far at u (a point-mass
+// draft's residual: SpecInfer's multi-step speculative sampling for deterministic
+// candidates); with no acceptance the bonus token is drawn from the residual by inverse
+// CDF with bonus_uniform.  Every emitted token then follows the target distribution.
+//
+// Kernel 1 (HBM-bound, the argmax grid): per (row, chunk) the chunk's largest logit m_c and
+// the Kahan-compensated sum s_c of exp((x - m_c) / T).  Kernel 2 (one CTA per sequence):
+// per visited node, M = max_c m_c and Z = sum_c s_c exp((m_c - M) / T) in fp64, the
+// node's children in id order (a block scan over contiguous node ranges), their logits
+// gathered at once, then one thread takes the acceptance decisions in fp64.  The bonus
+// draw finds the chunk where the residual CDF crosses the threshold from the chunk sums,
+// then scans that one chunk: per-thread Kahan sums, an fp64 block scan, and one thread
+// re-walks its segment.
+namespace jf {
+namespace {
+
+constexpr int kSampleThreads = 256;
+
+struct KahanSum {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+};
+
+__device__ __forceinline__ float block_max_f32(float v, float* s_red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = -INFINITY;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) r = fmaxf(r, s_red[w]);
+  return r;
+}
+
+__device__ __forceinline__ double block_sum_f64(double v, double* s_red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  double r = 0.0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) r += s_red[w];
+  return r;
+}
+
+// Calls f(value) for every element of [s, e) of `base` that this thread owns, with 16-byte
+// loads for the aligned body (the argmax kernel's split into head, body and tail).
+template <typename T, typename F>
+__device__ __forceinline__ void for_chunk(const T* base, long long s, long long e, F f) {
+  constexpr int kVec = 16 / sizeof(T);
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base + s);
+  long long head = ((16 - (addr & 15)) & 15) / sizeof(T);
+  if (head > e - s) head = e - s;
+  const long long body0 = s + head;
+  const long long nvec = (e - body0) / kVec;
+  const long long body1 = body0 + nvec * kVec;
+  if (threadIdx.x < head) f(to_f<T>(base[s + threadIdx.x]));
+  const uint4* vb = reinterpret_cast<const uint4*>(base + body0);
+  for (long long v0 = threadIdx.x; v0 < nvec; v0 += blockDim.x) {
+    const uint4 q = vb[v0];
+    if constexpr (sizeof(T) == 2) {
+      f(bf16_lo(q.x)); f(bf16_hi(q.x)); f(bf16_lo(q.y)); f(bf16_hi(q.y));
+      f(bf16_lo(q.z)); f(bf16_hi(q.z)); f(bf16_lo(q.w)); f(bf16_hi(q.w));
+    } else {
+      f(__uint_as_float(q.x)); f(__uint_as_float(q.y)); f(__uint_as_float(q.z)); f(__uint_as_float(q.w));
+    }
+  }
+  if (threadIdx.x < e - body1) f(to_f<T>(base[body1 + threadIdx.x]));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSampleThreads)
+    sample_stats_kernel(const T* __restrict__ logits, long long V, int chunks, int chunk_len,
+                        float inv_t, float2* __restrict__ stats) {
+  __shared__ float s_redf[kSampleThreads / 32];
+  __shared__ double s_redd[kSampleThreads / 32];
+  grid_dependency_wait();
+  const long long row = blockIdx.x / chunks;
+  const int c = blockIdx.x - static_cast<int>(row * chunks);
+  const long long s = static_cast<long long>(c) * chunk_len;
+  const long long e = min(V, s + chunk_len);
+  const T* base = logits + row * V;
+  float m = -INFINITY;
+  for_chunk<T>(base, s, e, [&](float x) { m = fmaxf(m, x); });
+  m = block_max_f32(m, s_redf);
+  KahanSum acc;
+  for_chunk<T>(base, s, e, [&](float x) { acc.add(expf((x - m) * inv_t)); });
+  const double tot = block_sum_f64(static_cast<double>(acc.s) - static_cast<double>(acc.c), s_redd);
+  if (threadIdx.x == 0) stats[blockIdx.x] = make_float2(m, static_cast<float>(tot));
+  grid_dependents_launch();
+}
+
+// Exclusive block scan of one int per thread; returns the thread's offset, total in *all.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_red, int* all) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) s_red[w] = x;
+  __syncthreads();
+  int base = 0, tot = 0;
+  for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) {
+    if (k < w) base += s_red[k];
+    tot += s_red[k];
+  }
+  *all = tot;
+  return base + x - v;
+}
+
+__device__ __forceinline__ double block_excl_scan_f64(double v, double* s_red, double* all) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  double x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) s_red[w] = x;
+  __syncthreads();
+  double base = 0.0, tot = 0.0;
+  for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) {
+    if (k < w) base += s_red[k];
+    tot += s_red[k];
+  }
+  *all = tot;
+  return base + x - v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSampleThreads)
+    sampled_walk_kernel(const T* __restrict__ logits, const float2* __restrict__ stats, int chunks,
+                        int chunk_len, const int32_t* __restrict__ draft,
+                        const int32_t* __restrict__ parent, const float* __restrict__ uniform,
+                        const float* __restrict__ bonus_uniform, float temperature, int N,
+                        long long V, int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
+                        int32_t* __restrict__ bonus, int32_t* dev_err) {
+  extern __shared__ int32_t smw[];
+  int32_t* s_par = smw;                 // [N] parent (malformed -> -1)
+  int32_t* s_draft = s_par + N;         // [N]
+  int32_t* s_kids = s_draft + N;        // [N] children of the current node, id order
+  int32_t* s_path = s_kids + N;         // [N]
+  float* s_lg = reinterpret_cast<float*>(s_path + N);                    // [N] children's logits
+  int32_t* s_rej = reinterpret_cast<int32_t*>(s_lg + N);                  // [N] rejected tokens
+  double* s_rejp = reinterpret_cast<double*>(                             // [N] their probabilities
+      (reinterpret_cast<uintptr_t>(s_rej + N) + 7) & ~static_cast<uintptr_t>(7));
+  __shared__ double s_redd[kSampleThreads / 32];
+  __shared__ float s_redf[kSampleThreads / 32];
+  __shared__ int s_redi[kSampleThreads / 32];
+  __shared__ int s_next, s_nrej, s_chunk, s_y;
+  __shared__ double s_rejmass, s_base;
+
+  grid_dependency_wait();
+  const int b = blockIdx.x;
+  const size_t rb = static_cast<size_t>(b) * N;
+  const double Td = temperature;
+  const float inv_t = 1.f / temperature;
+  int bad_parent = 0, bad_token = 0;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    int p = parent[rb + i];
+    const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+    if (!ok) { bad_parent = 1; p = -1; }
+    s_par[i] = p;
+    const int d = draft[rb + i];
+    if (i > 0 && (d < 0 || d >= V)) bad_token = 1;
+    s_draft[i] = (d >= 0 && d < V) ? d : -1;
+  }
+  bad_parent = __syncthreads_or(bad_parent);
+  bad_token = __syncthreads_or(bad_token);
+  if (threadIdx.x == 0) {
+    if (bad_parent) report(dev_err, JF_DEVERR_BAD_PARENT);
+    if (bad_token) report(dev_err, JF_DEVERR_BAD_TOKEN);
+    s_path[0] = 0;
+  }
+  // contiguous node range of this thread, for the ordered child lists
+  const int per = (N + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+  const int c_lo = min(N, static_cast<int>(threadIdx.x) * per), c_hi = min(N, c_lo + per);
+  int u = 0, n = 0;
+  double M = 0.0, Z = 1.0;
+  for (;;) {
+    const T* row = logits + (rb + u) * V;
+    const float2* st = stats + (rb + u) * chunks;
+    // M and Z of row u from the chunk statistics (fp64)
+    float mloc = -INFINITY;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) mloc = fmaxf(mloc, st[c].x);
+    M = block_max_f32(mloc, s_redf);
+    double zloc = 0.0;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x)
+      zloc += static_cast<double>(st[c].y) * exp((static_cast<double>(st[c].x) - M) / Td);
+    Z = block_sum_f64(zloc, s_redd);
+    // children of u in id order, and their logits
+    int cnt = 0;
+    for (int c = c_lo; c < c_hi; ++c) cnt += (s_par[c] == u) ? 1 : 0;
+    int nk = 0;
+    int off = block_excl_scan(cnt, s_redi, &nk);
+    for (int c = c_lo; c < c_hi; ++c)
+      if (s_par[c] == u) s_kids[off++] = c;
+    __syncthreads();
+    for (int k = threadIdx.x; k < nk; k += blockDim.x) {
+      const int x = s_draft[s_kids[k]];
+      s_lg[k] = x >= 0 ? to_f<T>(row[x]) : -INFINITY;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double rej = 0.0;
+      int next = -1, nrej = 0;
+      for (int k = 0; k < nk; ++k) {
+        const int c = s_kids[k];
+        const int x = s_draft[c];
+        bool seen = x < 0;
+        for (int r = 0; r < nrej && !seen; ++r) seen = s_rej[r] == x;
+        const double p = seen ? 0.0 : exp((static_cast<double>(s_lg[k]) - M) / Td) / Z;
+        if (static_cast<double>(uniform[rb + c]) * (1.0 - rej) < p) {
+          next = c;
+          break;
+        }
+        if (!seen) {
+          s_rej[nrej] = x;
+          s_rejp[nrej] = p;
+          ++nrej;
+          rej += p;
+        }
+      }
+      s_next = next;
+      s_nrej = nrej;
+      s_rejmass = rej;
+      if (next >= 0) s_path[n + 1] = next;
+    }
+    __syncthreads();
+    if (s_next < 0) break;
+    u = s_next;
+    ++n;
+  }
+  // bonus token: inverse CDF of the residual at u
+  const int nrej = s_nrej;
+  const double target = static_cast<double>(bonus_uniform[b]) * (1.0 - s_rejmass);
+  const T* row = logits + (rb + u) * V;
+  const float2* st = stats + (rb + u) * chunks;
+  if (threadIdx.x == 0) {
+    double cum = 0.0;
+    int cs = chunks - 1;
+    double base = 0.0;
+    for (int c = 0; c < chunks; ++c) {
+      const long long s0 = static_cast<long long>(c) * chunk_len, e0 = min(V, s0 + chunk_len);
+      double w = static_cast<double>(st[c].y) * exp((static_cast<double>(st[c].x) - M) / Td) / Z;
+      for (int r = 0; r < nrej; ++r)
+        if (s_rej[r] >= s0 && s_rej[r] < e0) w -= s_rejp[r];
+      if (cum + w > target || c == chunks - 1) {
+        cs = c;
+        base = cum;
+        break;
+      }
+      cum += w;
+    }
+    s_chunk = cs;
+    s_base = base;
+    s_y = -1;
+  }
+  __syncthreads();
+  const long long cs0 = static_cast<long long>(s_chunk) * chunk_len;
+  const long long ce0 = min(V, cs0 + chunk_len);
+  const long long len = ce0 - cs0;
+  const long long seg = (len + blockDim.x - 1) / blockDim.x;
+  const long long t0 = cs0 + min(len, static_cast<long long>(threadIdx.x) * seg);
+  const long long t1 = min(ce0, t0 + seg);
+  const float Mf = static_cast<float>(M);
+  auto mass = [&](long long x) -> float {      // exp((l - M) / T) of a live token, else 0
+    for (int r = 0; r < nrej; ++r)
+      if (s_rej[r] == x) return 0.f;
+    return expf((to_f<T>(row[x]) - Mf) * inv_t);
+  };
+  KahanSum ks;
+  for (long long x = t0; x < t1; ++x) ks.add(mass(x));
+  const double mine = (static_cast<double>(ks.s) - static_cast<double>(ks.c)) / Z;
+  double all = 0.0;
+  const double before = s_base + block_excl_scan_f64(mine, s_redd, &all);
+  if (t1 > t0 && before <= target && target < before + mine) {
+    double cum = before;
+    long long y = -1, last = -1;
+    for (long long x = t0; x < t1; ++x) {
+      const float e = mass(x);
+      if (e > 0.f) last = x;
+      cum += static_cast<double>(e) / Z;
+      if (cum > target) { y = x; break; }
+    }
+    s_y = static_cast<int>(y >= 0 ? y : last);
+  }
+  __syncthreads();
+  if (s_y < 0) {                               // rounding past the chunk's end: last live token
+    int lastl = -1;
+    for (long long x = t0; x < t1; ++x)
+      if (mass(x) > 0.f) lastl = static_cast<int>(x);
+    // the largest live index over the block
+    int v = lastl;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) s_redi[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int r = -1;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) r = max(r, s_redi[w]);
+      s_y = r >= 0 ? r : static_cast<int>(cs0);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    accept_len[b] = n;
+    bonus[b] = s_y;
+  }
+  for (int k = threadIdx.x; k < N; k += blockDim.x) path[rb + k] = k <= n ? s_path[k] : -1;
+  grid_dependents_launch();
+}
+
+}  // namespace
+}  // namespace jf
+
+extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, const int32_t* draft,
+                                            const int32_t* parent, const float* uniform,
+                                            const float* bonus_uniform, float temperature,
+                                            int32_t B, int32_t N, int32_t V, int32_t* accept_len,
+                                            int32_t* path, int32_t* bonus, void* workspace,
+                                            size_t workspace_bytes, int32_t* dev_err,
+                                            jf_stream_t stream) {
+  if (logits == nullptr || draft == nullptr || parent == nullptr || uniform == nullptr ||
+      bonus_uniform == nullptr || accept_len == nullptr || path == nullptr || bonus == nullptr ||
+      workspace == nullptr)
+    return JF_ERR_INVALID_ARGUMENT;
+  if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
+  if (B < 1 || N < 1 || V < 1 || !(temperature > 0.f) || !std::isfinite(temperature))
+    return JF_ERR_INVALID_ARGUMENT;
+  if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  jf::VerifyPlan p;
+  if (!jf::plan_verify(B, N, V, &p)) return JF_ERR_UNSUPPORTED;
+  const size_t need = static_cast<size_t>(B) * N * p.chunks * sizeof(float2);
+  if (workspace_bytes < need) return JF_ERR_WORKSPACE_TOO_SMALL;
+  if (!jf::aligned_to(workspace, 8)) return JF_ERR_MISALIGNED;
+  if (!jf::aligned_to(logits, dtype == JF_DTYPE_BF16 ? 2 : 4)) return JF_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float2* stats = static_cast<float2*>(workspace);
+  const long long grid = static_cast<long long>(B) * N * p.chunks;
+  if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  const long long Vl = V;
+  const float inv_t = 1.f / temperature;
+  const cudaError_t ea =
+      dtype == JF_DTYPE_BF16
+          ? jf::launch_pdl(jf::sample_stats_kernel<uint16_t>, dim3(static_cast<unsigned>(grid)),
+                           dim3(jf::kSampleThreads), 0, s, static_cast<const uint16_t*>(logits), Vl,
+                           p.chunks, p.chunk_len, inv_t, stats)
+          : jf::launch_pdl(jf::sample_stats_kernel<float>, dim3(static_cast<unsigned>(grid)),
+                           dim3(jf::kSampleThreads), 0, s, static_cast<const float*>(logits), Vl,
+                           p.chunks, p.chunk_len, inv_t, stats);
+  if (ea != cudaSuccess) return JF_ERR_CUDA;
+  const size_t smem = static_cast<size_t>(N) * (6 * sizeof(int32_t) + sizeof(double)) + 16;
+  auto walk = [&](auto kern, const auto* lg) -> cudaError_t {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+      return cudaErrorInvalidValue;
+    return jf::launch_pdl(kern, dim3(B), dim3(jf::kSampleThreads), smem, s, lg,
+                          static_cast<const float2*>(stats), p.chunks, p.chunk_len, draft, parent,
+                          uniform, bonus_uniform, temperature, N, Vl, accept_len, path, bonus, dev_err);
+  };
+  const cudaError_t ew =
+      dtype == JF_DTYPE_BF16
+          ? walk(jf::sampled_walk_kernel<uint16_t>, static_cast<const uint16_t*>(logits))
+          : walk(jf::sampled_walk_kernel<float>, static_cast<const float*>(logits));
+  return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }

@@ -71,6 +71,9 @@ def _load():
     lib.jf_tree_verify_ragged.argtypes = [P, i32, P, P, P, i32, i32, i32, P, P, P, P, P, sz, P, P]
     lib.jf_tree_verify_ragged.restype = ctypes.c_int
     lib.jf_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+    lib.jf_tree_verify_sampled.argtypes = [P, i32, P, P, P, P, f32, i32, i32, i32, P, P, P, P, sz,
+                                           P, P]
+    lib.jf_tree_verify_sampled.restype = ctypes.c_int
     lib.jf_debug_set_wait_limit_ns.restype = ctypes.c_int
     return lib
 
@@ -236,6 +239,35 @@ def jf_tree_verify_ragged(logits, draft, parent, tree_len, accept_len, path, bon
                  dev_err, stream)
 
 
+def jf_tree_verify_sampled(logits, draft, parent, uniform, bonus_uniform, temperature,
+                           accept_len, path, bonus, workspace, dev_err=None, stream=None) -> None:
+    """Lossless (stochastic) verification; uniform float32 [B][N] and bonus_uniform float32
+    [B] are the random numbers in [0, 1) (see include/jf.h).  The workspace is sized by
+    jf_tree_verify_workspace_size."""
+    B, N, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = JF_DTYPE_BF16
+    elif logits.dtype == torch.float32:
+        dt = JF_DTYPE_F32
+    else:
+        raise TypeError("logits must be bfloat16 or float32")
+    _need(logits, "logits", logits.dtype)
+    _need(draft, "draft", torch.int32, (B, N))
+    _need(parent, "parent", torch.int32, (B, N))
+    _need(uniform, "uniform", torch.float32, (B, N))
+    _need(bonus_uniform, "bonus_uniform", torch.float32, (B,))
+    _need(accept_len, "accept_len", torch.int32, (B,))
+    _need(path, "path", torch.int32, (B, N))
+    _need(bonus, "bonus", torch.int32, (B,))
+    _need(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_tree_verify_sampled", _lib.jf_tree_verify_sampled(
+        _ptr(logits), dt, _ptr(draft), _ptr(parent), _ptr(uniform), _ptr(bonus_uniform),
+        float(temperature), B, N, V, _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(workspace),
+        workspace.numel(), _ptr(dev_err), _stream(stream)))
+
+
 def _verify_call(logits, draft, parent, tree_len, accept_len, path, bonus, argmax, workspace,
                  dev_err, stream) -> None:
     B, N, V = logits.shape
@@ -394,6 +426,20 @@ def tree_verify(logits, draft, parent, dev_err=None, stream=None, tree_len=None)
         jf_tree_verify_ragged(logits, draft, parent, tree_len, accept_len, path, bonus, argmax, ws,
                               dev_err, stream)
     return argmax, accept_len, path, bonus
+
+
+def tree_verify_sampled(logits, draft, parent, uniform, bonus_uniform, temperature=1.0,
+                        dev_err=None, stream=None):
+    """Allocating wrapper of jf_tree_verify_sampled: (accept_len, path, bonus)."""
+    B, N, V = logits.shape
+    dev = logits.device
+    accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    bonus = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = _workspace(jf_tree_verify_workspace_size(B, N, V), dev)
+    jf_tree_verify_sampled(logits, draft, parent, uniform, bonus_uniform, temperature, accept_len,
+                           path, bonus, ws, dev_err, stream)
+    return accept_len, path, bonus
 
 
 def compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,

@@ -348,3 +348,12 @@ def draft_logits(B: int, Dmax: int, V: int, sigma: float = 3.0, dtype: str = "bf
     x = (rng.standard_normal((B, Dmax, V), dtype=np.float32) * np.float32(sigma)).astype(np.float32)
     return to_bf16_bits(x) if dtype == "bf16" else x
 
+
+
+def sampling_uniforms(B: int, N: int, seed: int = 0):
+    """Seeded random numbers of stochastic verification: (uniform float32 [B][N],
+    bonus_uniform float32 [B]), all in [0, 1)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x5A3F]))
+    u = rng.random((B, N), dtype=np.float32)
+    bu = rng.random(B, dtype=np.float32)
+    return u, bu
