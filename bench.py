@@ -15,7 +15,8 @@ them on the stream the kernels run on.  ``value`` is the mean attention time ove
 steps; the step time and the other calls go to ``breakdown_us``.  The same run then
 times the attention call alone for at least half a second (so the clock sampler sees
 sustained load), the attention calls of the budget-16 and budget-256 Qwen3-8B workloads,
-the draft-tree build, the ragged attention call and the KV compaction.  ``e2e`` times the
+the lossless (sampled) verification, the draft-tree build, the ragged attention call and
+the KV compaction.  ``e2e`` times the
 attention call through the plain API with pinned host buffers: the copies of its inputs
 in and of its outputs back are inside the timed region.  Under torchrun every rank runs
 its own replica (the path shards by sequence with no exchange), and the slowest rank's
@@ -382,6 +383,24 @@ def run_gpu(args, w, rank, world, peaks):
         e2e = {"value": max_over_ranks(statistics.mean(e2e_ms) * 1e3, world), "unit": "µs/call",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
         del host, dt
+    # ---- lossless (stochastic) verification of the same trees (seeded random numbers,
+    # temperature 1); not part of the step, which verifies greedily.
+    su, sbu = wl.sampling_uniforms(B, N, w.seed)
+    t_su, t_sbu = torch.from_numpy(su).to(dev), torch.from_numpy(sbu).to(dev)
+    s_acc = torch.empty_like(acc)
+    s_path = torch.empty_like(path)
+    s_bonus = torch.empty_like(bonus)
+
+    def call_sampled():
+        jf.jf_tree_verify_sampled(t["logits"], t["draft"], t["parent"], t_su, t_sbu, 1.0, s_acc,
+                                  s_path, s_bonus, ws_v, err)
+
+    call_sampled()
+    g_samp = capture(call_sampled)
+    for k in range(args.warmup):
+        timed(g_samp, k)
+    samp_ms = ms([timed(g_samp, k) for k in range(args.steps)])
+
     # ---- before verification: best-first draft-tree construction from per-depth draft
     # logits (16 depths, 8 candidates per depth, the workload's budget); not part of the step.
     dl = wl.draft_logits(B, 16, V, seed=w.seed)
@@ -440,7 +459,8 @@ def run_gpu(args, w, rank, world, peaks):
         raise RuntimeError(f"device error bits {err.item():#x} after the benchmark's calls")
     return dict(step_ms=step_ms, mask_ms=mask_ms, attn_ms=attn_ms, ver_ms=ver_ms, sus_ms=sus_ms,
                 clocks=clk, e2e=e2e, launches=launches_per_step * args.steps, ws=ws_a_bytes,
-                compact_ms=compact_ms, accepted=acc.cpu().tolist(), tree_ms=tree_ms,
+                compact_ms=compact_ms, accepted=acc.cpu().tolist(), tree_ms=tree_ms, samp_ms=samp_ms,
+                samp_accepted=s_acc.cpu().tolist(),
                 tree_bytes=tree_bytes, rag_ms=rag_ms, rag_len=rag_len.tolist(), side=side_lines)
 
 
@@ -545,6 +565,10 @@ def main():
                          "verify": statistics.mean(r["ver_ms"]) * 1e3,
                          "verify_hbm_gbs": verify_algorithmic_bytes(w) /
                          (statistics.mean(r["ver_ms"]) * 1e-3) / 1e9,
+                         "verify_sampled": statistics.mean(r["samp_ms"]) * 1e3,
+                         "verify_sampled_hbm_gbs": verify_algorithmic_bytes(w) /
+                         (statistics.mean(r["samp_ms"]) * 1e-3) / 1e9,
+                         "verify_sampled_accepted_nodes": r["samp_accepted"],
                          "other_workloads_attention": r["side"],
                          "draft_tree_build": statistics.mean(r["tree_ms"]) * 1e3,
                          "draft_tree_logits_hbm_gbs": r["tree_bytes"] /
