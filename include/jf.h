@@ -91,9 +91,9 @@ jf_status jf_build_tree_mask(const int32_t* parent, const int32_t* prefix_len, i
                              int32_t* dev_err, jf_stream_t stream);
 
 /*
- * Bytes of device workspace jf_tree_attention needs for these sizes on the CURRENT
- * device (split-KV partial results).  0 means no workspace is needed.  Returns
- * (size_t)-1 if the sizes are unsupported or the device cannot be queried.
+ * Bytes of device workspace jf_tree_attention and jf_tree_attention_ragged need for these
+ * sizes on the CURRENT device (split-KV partial results).  0 means no workspace is needed.
+ * Returns (size_t)-1 if the sizes are unsupported or the device cannot be queried.
  */
 size_t jf_tree_attention_workspace_size(int32_t B, int32_t N, int32_t Hq, int32_t Hkv,
                                         int32_t D, int32_t max_pages, int32_t page_size);
@@ -259,7 +259,9 @@ jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, const int32_
  * one more argument, tree_len int32 [B] (device): sequence b's tree has the nodes
  * 0 .. n_b - 1, n_b = tree_len[b], 1 <= n_b <= N; arrays keep their [B][N] shapes and
  * entries of nodes i >= n_b are padding.  With tree_len[b] == N for every b each call
- * computes exactly what its fixed-size counterpart computes.  A tree_len entry outside
+ * computes what its fixed-size counterpart computes (the attention call up to
+ * floating-point summation order, since a ragged call never takes the stream-K dispatch,
+ * whose ranges cannot skip padding row groups).  A tree_len entry outside
  * [1, N] sets JF_DEVERR_BAD_TREE_LEN and is clamped into that range.
  *   jf_build_tree_mask_ragged: parent[b][i] is read for i < n_b only; rows i >= n_b get
  *     all-zero mask words and depth = pos = -1.
@@ -267,12 +269,14 @@ jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, const int32_
  *     P_b .. P_b + n_b - 1; block-table entries past ceil((P_b + n_b) / page_size) are
  *     never read and K/V slots past P_b + n_b may hold anything (the padding nodes need no
  *     K/V at all).  Rows i < n_b are as in jf_tree_attention; rows i >= n_b of out and lse
- *     carry no meaning (they attend to what their mask row allows, the prefix with the
- *     mask of jf_build_tree_mask_ragged).
+ *     carry no meaning (they may be left unwritten or hold anything).  Groups of 128-256
+ *     query rows that hold only padding nodes are not computed, so a batch of small trees
+ *     costs about what its trees need.
  *   jf_tree_verify_ragged: nodes i >= n_b are never accepted and their parent and draft
  *     entries are not read; argmax is still written for every row, so logits rows
  *     i >= n_b must be readable (their values do not matter).  path[b] lists nodes < n_b.
- * Workspace sizes are those of the fixed-size calls with the same N.
+ * Workspace sizes: jf_tree_attention_workspace_size and jf_tree_verify_workspace_size
+ * with the same N.
  */
 jf_status jf_build_tree_mask_ragged(const int32_t* parent, const int32_t* prefix_len,
                                     const int32_t* tree_len, int32_t B, int32_t N,

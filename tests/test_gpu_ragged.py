@@ -94,7 +94,8 @@ def check_rows(w, tree_len, out, lse, rows_per_seq, seed=0):
         assert not bad.any(), (f"sequence {b} (n={n}): {bad.sum()} elements out of tolerance, "
                                f"max abs err {err.max():.3e}")
         assert np.abs(lse[b, rh, ri] - ref_l).max() <= LSE_ATOL
-    assert np.isfinite(out).all()        # padding rows carry no meaning but stay finite
+    for b, n in enumerate(tree_len):     # padding rows carry no meaning (may be unwritten)
+        assert np.isfinite(out[b, :n]).all()
 
 
 def make(B, N, Hq, Hkv, D, prefix, seed, permute=True):
@@ -131,8 +132,16 @@ def test_ragged_attention_matches_slices(jf, case):
     check_rows(w, tree_len, out, lse, rows_per_seq=48 if B > 8 else 160, seed=case)
 
 
-def test_ragged_full_length_is_bit_identical(jf):
-    w = make(8, 256, 32, 4, 128, [600, 1500, 977, 2000, 64, 1234, 15, 800], seed=3)
+@pytest.mark.parametrize("shape", ["per_unit", "stream_k_sized"])
+def test_ragged_full_length_matches_fixed_size(jf, shape):
+    """Every tree at full size: the ragged call computes what the fixed-size call computes.
+    Bit for bit when both take the same dispatch; the fixed-size call of the 8 x 256-node
+    shape takes stream-K (ragged calls never do: stream-K ranges cannot skip padding row
+    groups), so there the two agree within the attention tolerance."""
+    if shape == "per_unit":
+        w = make(3, 64, 8, 2, 128, [0, 300, 1000], seed=3)
+    else:
+        w = make(8, 256, 32, 4, 128, [600, 1500, 977, 2000, 64, 1234, 15, 800], seed=3)
     t = wl.device_tensors(w, with_logits=False)
     mask, depth, pos = jf.build_tree_mask(t["parent"], t["prefix_len"])
     ref = jf.tree_attention(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
@@ -143,8 +152,42 @@ def test_ragged_full_length_is_bit_identical(jf):
                             t["prefix_len"], mask2, scale=w.scale, with_lse=True, tree_len=tl)
     torch.cuda.synchronize()
     assert torch.equal(mask, mask2) and torch.equal(depth, depth2) and torch.equal(pos, pos2)
-    assert torch.equal(ref[0].view(torch.int16), got[0].view(torch.int16))
-    assert torch.equal(ref[1], got[1])
+    if shape == "per_unit":
+        assert torch.equal(ref[0].view(torch.int16), got[0].view(torch.int16))
+        assert torch.equal(ref[1], got[1])
+    else:
+        a, b = ref[0].float(), got[0].float()
+        assert ((a - b).abs() <= ATOL + RTOL * a.abs()).all()
+        assert (ref[1] - got[1]).abs().max().item() <= LSE_ATOL
+
+
+def test_ragged_small_trees_skip_padding_groups(jf):
+    """8 sequences of budget 256 at G = 8 (eight 256-row groups each) with trees of 1..63
+    nodes: only the first group of each sequence holds real nodes.  Its rows must match the
+    oracle; the call must leave the other groups' rows alone (they carry no meaning), which
+    the poisoned output shows."""
+    tree_len = [1, 5, 31, 32, 33, 63, 17, 2]
+    w = poison_padding(make(8, 256, 32, 4, 128, [300, 1500, 64, 2000, 700, 15, 900, 5], seed=11),
+                       tree_len)
+    t = wl.device_tensors(w, with_logits=False)
+    tl = torch.tensor(tree_len, dtype=torch.int32, device="cuda")
+    mask, _, _ = jf.build_tree_mask(t["parent"], t["prefix_len"], tree_len=tl)
+    out = torch.full_like(t["q"], float("nan"))
+    lse = torch.full((w.B, w.Hq, w.N), float("nan"), device="cuda")
+    nws = jf.jf_tree_attention_workspace_size(w.B, w.N, w.Hq, w.Hkv, w.D, w.max_pages, w.page)
+    ws = torch.empty(max(16, nws), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    jf.jf_tree_attention_ragged(t["q"], t["k_cache"], t["v_cache"], t["block_table"],
+                                t["prefix_len"], tl, mask, w.scale, out, lse, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    o = out.float().cpu().numpy()
+    check_rows(w, tree_len, o, lse.cpu().numpy(), rows_per_seq=64)
+    G = w.Hq // w.Hkv
+    per_group = 256 // G                 # nodes per 256-row group
+    for b, n in enumerate(tree_len):     # rows of the padding-only groups stay untouched
+        first_skipped = (n + per_group - 1) // per_group * per_group
+        assert np.isnan(o[b, first_skipped:]).all()
 
 
 def test_ragged_mask_matches_slices(jf):

@@ -568,6 +568,17 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const int k1 = min(ntiles, k0 + p.chunk_tiles);
   const int T = max(0, k1 - k0);
 
+  // Ragged calls: a row-tile group whose rows all belong to padding nodes (node >= n_b)
+  // has nothing to compute (those rows carry no meaning).  The splits of a unit share the
+  // group, so the CTAs of a merging cluster leave together.  The Q load is drained first.
+  if (p.tree_len != nullptr && (mp * NT * kRowTile) / p.G >= nt) {
+    if (threadIdx.x == 0) {
+      int zero = 0;
+      mbar_wait(&q_full, 0, &zero);
+    }
+    return;
+  }
+
   if (T == 0) {
     // An empty split still drains its Q load before the shared memory is reused or freed.
     if (threadIdx.x == 0) {
@@ -1853,7 +1864,10 @@ bool shape_supported(int B, int N, int Hq, int Hkv, int D, int max_pages, int pa
   return true;
 }
 
-bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms, AttnPlan* pl) {
+// allow_streamk = false for ragged calls: stream-K ranges are walked by every row-tile
+// group of a (sequence, kv-head) pair together, so padding groups could not skip their work.
+bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms, AttnPlan* pl,
+                    bool allow_streamk = true) {
   const int G = Hq / Hkv;
   const long long M = static_cast<long long>(N) * G;
   const int mtiles = static_cast<int>((M + kRowTile - 1) / kRowTile);
@@ -1910,7 +1924,7 @@ bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms
   const bool ragged_waves = units < waves1 * sms * 9 / 10;
   const long long max_tiles_all =
       static_cast<long long>(B) * Hkv * (static_cast<long long>(max_pages) * kPage / kKeyTile + 1);
-  if (pl->NT == 2 && pl->n_groups >= 2 && units >= sms && ragged_waves && B <= kLptMaxB &&
+  if (allow_streamk && pl->NT == 2 && pl->n_groups >= 2 && units >= sms && ragged_waves && B <= kLptMaxB &&
       pl->n_groups <= sms && max_tiles_all < (1ll << 30)) {
     pl->streamk = true;
     pl->nvirt = sms / pl->n_groups;
@@ -1985,9 +1999,10 @@ extern "C" size_t jf_tree_attention_workspace_size(int32_t B, int32_t N, int32_t
   if (!jf::shape_supported(B, N, Hq, Hkv, D, max_pages, page_size)) return static_cast<size_t>(-1);
   const int sms = jf::current_sm_count();
   if (sms <= 0) return static_cast<size_t>(-1);
-  jf::AttnPlan pl;
+  jf::AttnPlan pl, pr;
   jf::plan_attention(B, N, Hq, Hkv, D, max_pages, sms, &pl);
-  return pl.ws_bytes;
+  jf::plan_attention(B, N, Hq, Hkv, D, max_pages, sms, &pr, false);   // the ragged call's plan
+  return std::max(pl.ws_bytes, pr.ws_bytes);
 }
 
 namespace {
@@ -2014,7 +2029,7 @@ jf_status tree_attention_call(const void* q, const void* k_cache, const void* v_
   const int sms = current_sm_count();
   if (sms <= 0) return JF_ERR_CUDA;
   AttnPlan pl;
-  plan_attention(B, N, Hq, Hkv, D, max_pages, sms, &pl);
+  plan_attention(B, N, Hq, Hkv, D, max_pages, sms, &pl, tree_len == nullptr);
   if (pl.ws_bytes > 0) {
     if (workspace == nullptr || workspace_bytes < pl.ws_bytes) return JF_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned_to(workspace, 16)) return JF_ERR_MISALIGNED;
