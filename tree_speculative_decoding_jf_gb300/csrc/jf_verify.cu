@@ -511,13 +511,21 @@ jf_status launch_walk(const uint64_t* part, int chunks, const int32_t* draft,
   return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
 
+// Chunks of the stochastic verification: fixed 8192-logit chunks, so the bonus draw scans
+// one chunk of 32 logits per thread (the argmax plan may give a whole row to one CTA).
+constexpr int kSampleChunk = 8192;
+
+inline int sampled_chunks(int V) { return (V + kSampleChunk - 1) / kSampleChunk; }
+
 }  // namespace
 }  // namespace jf
 
 extern "C" size_t jf_tree_verify_workspace_size(int32_t B, int32_t N, int32_t V) {
   jf::VerifyPlan p;
   if (!jf::plan_verify(B, N, V, &p)) return static_cast<size_t>(-1);
-  return static_cast<size_t>(B) * N * p.chunks * sizeof(uint64_t);
+  const size_t rows = static_cast<size_t>(B) * N;
+  return std::max(rows * p.chunks * sizeof(uint64_t),                       // argmax keys
+                  rows * jf::sampled_chunks(V) * sizeof(float2));          // sampling stats
 }
 
 namespace {
@@ -665,6 +673,12 @@ namespace {
 
 constexpr int kSampleThreads = 256;
 
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 struct KahanSum {
   float s = 0.f, c = 0.f;
   __device__ __forceinline__ void add(float x) {
@@ -722,25 +736,99 @@ __device__ __forceinline__ void for_chunk(const T* base, long long s, long long 
   if (threadIdx.x < e - body1) f(to_f<T>(base[body1 + threadIdx.x]));
 }
 
+// Adds the exponentials of one 16-byte vector of logits to a thread's running (m, sum):
+// k = log2(e) / T; the sum is kept relative to 2^(m k) and rescaled when m rises (once per
+// vector at most).  The vector's own terms are summed pairwise in fp32 before a
+// Kahan-compensated add, so the thread's sum stays within a few ulp.
+template <int NV>
+__device__ __forceinline__ void stats_add(const float (&x)[NV], float k, float& m, KahanSum& acc) {
+  float vm = x[0];
+#pragma unroll
+  for (int e = 1; e < NV; ++e) vm = fmaxf(vm, x[e]);
+  if (vm > m) {
+    const float f = m == -INFINITY ? 0.f : fast_exp2((m - vm) * k);
+    acc.s *= f;
+    acc.c *= f;
+    m = vm;
+  }
+  float part[NV];
+#pragma unroll
+  for (int e = 0; e < NV; ++e) part[e] = fast_exp2((x[e] - m) * k);   // x - m: exact near m
+#pragma unroll
+  for (int w = NV / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) part[e] += part[e + w];
+  acc.add(part[0]);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kSampleThreads)
     sample_stats_kernel(const T* __restrict__ logits, long long V, int chunks, int chunk_len,
                         float inv_t, float2* __restrict__ stats) {
-  __shared__ float s_redf[kSampleThreads / 32];
-  __shared__ double s_redd[kSampleThreads / 32];
+  constexpr int kVec = 16 / sizeof(T);
+  constexpr int kInFlight = 4;
+  __shared__ float s_m[kSampleThreads / 32];
+  __shared__ double s_s[kSampleThreads / 32];
   grid_dependency_wait();
   const long long row = blockIdx.x / chunks;
   const int c = blockIdx.x - static_cast<int>(row * chunks);
   const long long s = static_cast<long long>(c) * chunk_len;
   const long long e = min(V, s + chunk_len);
   const T* base = logits + row * V;
+  const float k = inv_t * 1.4426950408889634f;       // exp(y / T) = 2^(y * k)
   float m = -INFINITY;
-  for_chunk<T>(base, s, e, [&](float x) { m = fmaxf(m, x); });
-  m = block_max_f32(m, s_redf);
   KahanSum acc;
-  for_chunk<T>(base, s, e, [&](float x) { acc.add(expf((x - m) * inv_t)); });
-  const double tot = block_sum_f64(static_cast<double>(acc.s) - static_cast<double>(acc.c), s_redd);
-  if (threadIdx.x == 0) stats[blockIdx.x] = make_float2(m, static_cast<float>(tot));
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base + s);
+  long long head = ((16 - (addr & 15)) & 15) / sizeof(T);
+  if (head > e - s) head = e - s;
+  const long long body0 = s + head;
+  const long long nvec = (e - body0) / kVec;
+  const long long body1 = body0 + nvec * kVec;
+  if (threadIdx.x < head) {
+    const float x[1] = {to_f<T>(base[s + threadIdx.x])};
+    stats_add<1>(x, k, m, acc);
+  }
+  const uint4* vb = reinterpret_cast<const uint4*>(base + body0);
+  for (long long v0 = threadIdx.x; v0 < nvec; v0 += kSampleThreads * kInFlight) {
+    uint4 q[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const long long vi = v0 + static_cast<long long>(u) * kSampleThreads;
+      if (vi < nvec) q[u] = __ldcs(vb + vi);
+    }
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const long long vi = v0 + static_cast<long long>(u) * kSampleThreads;
+      if (vi < nvec) {
+        float x[kVec];
+        if constexpr (sizeof(T) == 2) {
+          x[0] = bf16_lo(q[u].x); x[1] = bf16_hi(q[u].x); x[2] = bf16_lo(q[u].y); x[3] = bf16_hi(q[u].y);
+          x[4] = bf16_lo(q[u].z); x[5] = bf16_hi(q[u].z); x[6] = bf16_lo(q[u].w); x[7] = bf16_hi(q[u].w);
+        } else {
+          x[0] = __uint_as_float(q[u].x); x[1] = __uint_as_float(q[u].y);
+          x[2] = __uint_as_float(q[u].z); x[3] = __uint_as_float(q[u].w);
+        }
+        stats_add<kVec>(x, k, m, acc);
+      }
+    }
+  }
+  if (threadIdx.x < e - body1) {
+    const float x[1] = {to_f<T>(base[body1 + threadIdx.x])};
+    stats_add<1>(x, k, m, acc);
+  }
+  // combine the threads' (m, sum) pairs: M = max m, S = sum_t sum_t * 2^((m_t - M) k); the
+  // rescale and the warp sums in fp32 (GB300's fp64 rate is low), the eight warp sums in fp64
+  const float M = block_max_f32(m, s_m);
+  float mine = (m == -INFINITY) ? 0.f : (acc.s - acc.c) * fast_exp2((m - M) * k);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if ((threadIdx.x & 31) == 0) s_s[threadIdx.x >> 5] = static_cast<double>(mine);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < kSampleThreads / 32; ++w) tot += s_s[w];
+    stats[blockIdx.x] = make_float2(M, static_cast<float>(tot));
+  }
   grid_dependents_launch();
 }
 
@@ -915,41 +1003,47 @@ __global__ void __launch_bounds__(kSampleThreads)
     s_y = -1;
   }
   __syncthreads();
+  // The chunk's logits, 32 per thread in token order, all loads in flight together.
+  constexpr int kSeg = kSampleChunk / kSampleThreads;
   const long long cs0 = static_cast<long long>(s_chunk) * chunk_len;
   const long long ce0 = min(V, cs0 + chunk_len);
-  const long long len = ce0 - cs0;
-  const long long seg = (len + blockDim.x - 1) / blockDim.x;
-  const long long t0 = cs0 + min(len, static_cast<long long>(threadIdx.x) * seg);
-  const long long t1 = min(ce0, t0 + seg);
-  const float Mf = static_cast<float>(M);
-  auto mass = [&](long long x) -> float {      // exp((l - M) / T) of a live token, else 0
-    for (int r = 0; r < nrej; ++r)
-      if (s_rej[r] == x) return 0.f;
-    return expf((to_f<T>(row[x]) - Mf) * inv_t);
-  };
+  const long long t0 = cs0 + static_cast<long long>(threadIdx.x) * kSeg;
+  float ev[kSeg];
+  {
+    float lv[kSeg];
+#pragma unroll
+    for (int e = 0; e < kSeg; ++e) lv[e] = (t0 + e < ce0) ? to_f<T>(row[t0 + e]) : 0.f;
+    const float Mf = static_cast<float>(M);
+#pragma unroll
+    for (int e = 0; e < kSeg; ++e) {        // exp((l - M) / T) of live tokens, else 0
+      bool live = t0 + e < ce0;
+      for (int r = 0; r < nrej && live; ++r) live = s_rej[r] != t0 + e;
+      ev[e] = live ? expf((lv[e] - Mf) * inv_t) : 0.f;
+    }
+  }
   KahanSum ks;
-  for (long long x = t0; x < t1; ++x) ks.add(mass(x));
+#pragma unroll
+  for (int e = 0; e < kSeg; ++e) ks.add(ev[e]);
   const double mine = (static_cast<double>(ks.s) - static_cast<double>(ks.c)) / Z;
   double all = 0.0;
   const double before = s_base + block_excl_scan_f64(mine, s_redd, &all);
-  if (t1 > t0 && before <= target && target < before + mine) {
+  if (mine > 0.0 && before <= target && target < before + mine) {
     double cum = before;
-    long long y = -1, last = -1;
-    for (long long x = t0; x < t1; ++x) {
-      const float e = mass(x);
-      if (e > 0.f) last = x;
-      cum += static_cast<double>(e) / Z;
-      if (cum > target) { y = x; break; }
+    int y = -1, last = -1;
+#pragma unroll
+    for (int e = 0; e < kSeg; ++e) {
+      if (ev[e] > 0.f) last = e;
+      cum += static_cast<double>(ev[e]) / Z;
+      if (y < 0 && cum > target) y = e;
     }
-    s_y = static_cast<int>(y >= 0 ? y : last);
+    s_y = static_cast<int>(t0) + (y >= 0 ? y : last);
   }
   __syncthreads();
   if (s_y < 0) {                               // rounding past the chunk's end: last live token
-    int lastl = -1;
-    for (long long x = t0; x < t1; ++x)
-      if (mass(x) > 0.f) lastl = static_cast<int>(x);
-    // the largest live index over the block
-    int v = lastl;
+    int v = -1;
+#pragma unroll
+    for (int e = 0; e < kSeg; ++e)
+      if (ev[e] > 0.f) v = static_cast<int>(t0) + e;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
     __syncthreads();
@@ -989,7 +1083,8 @@ extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, c
     return JF_ERR_INVALID_ARGUMENT;
   if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
   jf::VerifyPlan p;
-  if (!jf::plan_verify(B, N, V, &p)) return JF_ERR_UNSUPPORTED;
+  p.chunk_len = jf::kSampleChunk;
+  p.chunks = jf::sampled_chunks(V);
   const size_t need = static_cast<size_t>(B) * N * p.chunks * sizeof(float2);
   if (workspace_bytes < need) return JF_ERR_WORKSPACE_TOO_SMALL;
   if (!jf::aligned_to(workspace, 8)) return JF_ERR_MISALIGNED;
