@@ -53,7 +53,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (attention kernel + combine) from ncu captures of the current kernels (None until a
 # capture of the current kernel exists for that workload); the capture commands are in
 # the profile summaries.
-NCU_TRAFFIC_BYTES: dict = {}
+NCU_TRAFFIC_BYTES = {
+    "c5_qwen3_30b_b8_tree256_32k": 571180800 + 31351808 + 38086144 + 512,
+    "c3_qwen3_8b_tree256": 20040704 + 0,
+    "c4_qwen3_8b_b32_tree64_paged": 569097984 + 9734144,
+    "c2_qwen3_8b_chain16": 8670464 + 2404096,
+}
 
 
 # ----------------------------------------------------------------------------- work model
@@ -308,13 +313,17 @@ def run_gpu(args, w, rank, world, peaks):
     ver_ms = [e[2].elapsed_time(e[3]) for e in step_ev]
     # Sustained: the attention call alone for at least SUSTAINED_S seconds, still inside
     # the clock sampler's window.
-    reps = max(args.steps, int(SUSTAINED_S / max(statistics.mean(attn_ms) * 1e-3, 1e-6)) + 1)
+    reps = args.steps if args.step_only else max(
+        args.steps, int(SUSTAINED_S / max(statistics.mean(attn_ms) * 1e-3, 1e-6)) + 1)
     sus_ms = ms([timed(g_attn, k) for k in range(reps)])
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if err.item() != 0:
         raise RuntimeError(f"device error bits {err.item():#x} during the benchmark")
 
+    if args.step_only:
+        return dict(step_ms=step_ms, mask_ms=mask_ms, attn_ms=attn_ms, ver_ms=ver_ms, sus_ms=sus_ms,
+                    clocks=clk, e2e=None, launches=launches_per_step * args.steps, ws=ws_a_bytes)
     # ---- the attention calls of the budget-16 and budget-256 Qwen3-8B workloads
     side_lines = {}
     for name in SIDE_CONFIGS:
@@ -494,6 +503,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time only the step (no sustained loop, other workloads, e2e or CPU "
+                         "baseline): short runs for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -545,11 +557,20 @@ def main():
     if rank != 0:
         return
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and not args.step_only and world == 1:
         s, sample, threads = oracle_attention_time(w, budget_s=args.cpu_budget)
         cpu = {"value": s * 1e6, "unit": "µs/call", "cores": threads, "kind": "oracle",
                "sample": sample}
     sus_us = statistics.mean(r["sus_ms"]) * 1e3
+    if args.step_only:
+        print(json.dumps({"metric": METRIC, "value": attn_us, "unit": "µs/call", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_us / 1e3,
+                          "higher_is_better": False, "config": config_dict(w), "roofline": roof,
+                          "breakdown_us": {"step": step_us, "mask": statistics.mean(r["mask_ms"]) * 1e3,
+                                           "verify": statistics.mean(r["ver_ms"]) * 1e3,
+                                           "attention_sustained": sus_us},
+                          "clocks": r["clocks"], "note": "step-only run (profiling)"}), flush=True)
+        return
     line = {
         "metric": METRIC, "value": attn_us, "unit": "µs/call", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_us / 1e3,
