@@ -753,19 +753,21 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
     bool ok = wait_warp(&q_full, 0, abort, wlim) && wait_warp(&k_full[0], 0, abort, wlim);
-    if (ok && lane == 0) {
+    if (ok) {
+      // The whole warp runs this loop (warp-uniform counters and descriptors); the MMA and
+      // commit wrappers issue from one elected lane.
       tc_fence_after();
       for (int t = 0; t < NT; ++t) {
         issue_s(t, 0);
         mma_commit(&s_full[t]);
       }
       mma_commit(&step_done[0]);
-      // One thread drives every row tile.  Row tile t's next step is PV of key tile
-      // jn[t] followed by S of key tile jn[t] + 1.  It may go once p_full[t] completes: the
+      // One warp drives every row tile.  Row tile t's next step is PV of key tile jn[t]
+      // followed by S of key tile jn[t] + 1.  It may go once p_full[t] completes: the
       // tile's softmax has arrived and so has its voucher warp, which arrives only after V
       // tile jn[t] and K tile jn[t] + 1 have landed, so a step costs the issuer a single
-      // barrier probe.  The thread probes the tiles in turn and issues whichever
-      // step is ready, so one tile's softmax never holds back the other tile's MMAs.
+      // barrier probe.  The warp probes the tiles in turn and issues whichever step is
+      // ready, so one tile's softmax never holds back the other tile's MMAs.
       // After the last row tile's step j one commit completes step record j + 1.
       // When P is stored as hi + lo (prefix shorter than kSplitPrefix), steps from j_tree on
       // cover key tiles that hold tree keys: the polling loop stops before them and an
@@ -784,7 +786,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         for (int t = 0; t < NT; ++t) {
           const int j = jn[t];
           if (j >= j_tree) continue;
-          if (!mbar_try_wait(&p_full[t], static_cast<uint32_t>(j) & 1u)) continue;
+          // lane 0's probe decides for the warp
+          if (__shfl_sync(0xffffffffu, mbar_try_wait(&p_full[t], static_cast<uint32_t>(j) & 1u) ? 1 : 0, 0) == 0)
+            continue;
           bool last = true;                  // the other row tiles are past key tile j
 #pragma unroll
           for (int u = 0; u < NT; ++u)
@@ -804,7 +808,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           idle = 0;
         } else {
           if (idle == 0) idle_since = global_timer_ns();
-          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > wlim)) {
+          if ((++idle & 255u) == 0u &&
+              __shfl_sync(0xffffffffu, (*abort || global_timer_ns() - idle_since > wlim) ? 1 : 0, 0) != 0) {
             ok = false;
             break;
           }
@@ -812,7 +817,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       }
       for (int j = j_tree; j < T && ok; ++j) {
         for (int t = 0; t < NT && ok; ++t) {
-          if (!mbar_wait(&p_full[t], static_cast<uint32_t>(j) & 1u, abort, wlim)) {
+          if (!wait_warp(&p_full[t], static_cast<uint32_t>(j) & 1u, abort, wlim)) {
             ok = false;
             break;
           }
@@ -826,15 +831,13 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         }
       }
     }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok) set_abort(abort, p.dev_err);
-    if (lane == 0) {
-      if (ok) mma_commit(&o_full);
-      mma_commit(&fin);   // all MMAs done before TMEM is released
+    if (!ok && lane == 0) set_abort(abort, p.dev_err);
+    if (ok) mma_commit(&o_full);
+    mma_commit(&fin);   // all MMAs done before TMEM is released
+    {
       int zero = 0;
-      mbar_wait(&fin, 0, &zero);
+      wait_warp(&fin, 0, &zero, kWaitLimitNs);
     }
-    __syncwarp();
   } else if (warp >= 2 && warp < 2 + NT) {
     // ================================================================ data vouchers
     // Warp 2 + t adds the last arrival to p_full[t] for key tile j once V tile j, K tile
@@ -1365,7 +1368,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
     bool ok = wait_warp(&q_full, 0, abort, wlim) && wait_warp(&k_full[0], 0, abort, wlim);
-    if (ok && lane == 0) {
+    if (ok) {
+      // The whole warp runs this loop; the MMA and commit wrappers issue from one elected
+      // lane (see tree_attention_kernel).
       tc_fence_after();
       for (int t = 0; t < NT; ++t) {
         issue_s(t, 0);
@@ -1385,13 +1390,16 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         for (int t = 0; t < NT; ++t) {
           const int j = jn[t];
           if (j >= Wc) continue;
-          if (!mbar_try_wait(&p_full[t], static_cast<uint32_t>(j) & 1u)) continue;
+          if (__shfl_sync(0xffffffffu, mbar_try_wait(&p_full[t], static_cast<uint32_t>(j) & 1u) ? 1 : 0, 0) == 0)
+            continue;
           bool last = true;
 #pragma unroll
           for (int u = 0; u < NT; ++u)
             if (u != t && jn[u] <= j) last = false;
           tc_fence_after();
-          issue_pv(t, j % SV, j > 0, *reinterpret_cast<volatile int*>(&s_lo[t]) != 0);
+          // s_lo[t] was written before the softmax's arrival on p_full[t]: lane 0 reads it
+          const bool lo = __shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&s_lo[t]), 0) != 0;
+          issue_pv(t, j % SV, j > 0, lo);
           if (j + 1 < Wc) {
             issue_s(t, (j + 1) % SK);
             mma_commit(&s_full[t]);
@@ -1405,22 +1413,21 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
           idle = 0;
         } else {
           if (idle == 0) idle_since = global_timer_ns();
-          if ((++idle & 255u) == 0u && (*abort || global_timer_ns() - idle_since > wlim)) {
+          if ((++idle & 255u) == 0u &&
+              __shfl_sync(0xffffffffu, (*abort || global_timer_ns() - idle_since > wlim) ? 1 : 0, 0) != 0) {
             ok = false;
             break;
           }
         }
       }
     }
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok) set_abort(abort, p.dev_err);
-    if (lane == 0) {
-      if (ok) mma_commit(&o_full);   // the range's last PV
-      mma_commit(&fin);   // all MMAs done before TMEM is released
+    if (!ok && lane == 0) set_abort(abort, p.dev_err);
+    if (ok) mma_commit(&o_full);   // the range's last PV
+    mma_commit(&fin);   // all MMAs done before TMEM is released
+    {
       int zero = 0;
-      mbar_wait(&fin, 0, &zero);
+      wait_warp(&fin, 0, &zero, kWaitLimitNs);
     }
-    __syncwarp();
   } else if (warp >= 2 && warp < 2 + NT) {
     // ================================================================ data vouchers
     // As in tree_attention_kernel, plus: at a segment's last tile the V tail of that
