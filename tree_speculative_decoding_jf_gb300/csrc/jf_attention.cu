@@ -431,9 +431,7 @@ __device__ __noinline__ void merge_cluster(uint8_t* sm, const MergeArgs p, int b
 // O += P_lo V from the second bf16 part of P (columns 64..127 of a row tile's S region).
 // Out of line: the MMA issuer's steady-state loop carries none of this code.
 __device__ __noinline__ void issue_pv_lo(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t idO) {
-#pragma unroll
-  for (int kk = 0; kk < kKeyTile / 16; ++kk)
-    mma_ts(d_tmem, a_tmem + 64 + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO, 1u);
+  mma_ts_tile(d_tmem, a_tmem + 64, db, idO, true);
 }
 
 // Longest sequences first: with one CTA per unit and ragged prefixes, CTAs are handed to
@@ -734,11 +732,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const uint64_t da = dq + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
       const uint64_t db = dk + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
       const uint32_t d_tmem = tmem + C::kTmemS + t * 128;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = static_cast<uint64_t>(((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4);
-        mma_ss(d_tmem, da + off, db + off, idS, kk > 0 ? 1u : 0u);
-      }
+      mma_ss_tile<D / 16>(d_tmem, da, db, idS);
     };
     // O_t (+)= P_t V; with `lo`, also O_t += P_lo V from the second bf16 part of P (columns
     // 64..127 of the S region), issued before the next S MMA overwrites those columns.
@@ -746,10 +740,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const uint64_t db = dv + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
       const uint32_t d_tmem = tmem + C::kTmemO + t * 128;
       const uint32_t a_tmem = tmem + C::kTmemS + t * 128;
-#pragma unroll
-      for (int kk = 0; kk < kKeyTile / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
-               (acc || kk > 0) ? 1u : 0u);
+      mma_ts_tile(d_tmem, a_tmem, db, idO, acc);
       if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
     bool ok = wait_warp(&q_full, 0, abort, wlim) && wait_warp(&k_full[0], 0, abort, wlim);
@@ -1349,11 +1340,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const uint64_t da = dq + static_cast<uint64_t>((t * C::kTileBytes) >> 4);
       const uint64_t db = dk + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
       const uint32_t d_tmem = tmem + C::kTmemS + t * 128;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = static_cast<uint64_t>(((kk / 4) * C::kHalfBytes + (kk % 4) * 32) >> 4);
-        mma_ss(d_tmem, da + off, db + off, idS, kk > 0 ? 1u : 0u);
-      }
+      mma_ss_tile<D / 16>(d_tmem, da, db, idS);
     };
     // O_t (+)= P_t V; with `lo`, also O_t += P_lo V from the second bf16 part of P (columns
     // 64..127 of the S region), issued before the next S MMA overwrites those columns.
@@ -1361,10 +1348,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       const uint64_t db = dv + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
       const uint32_t d_tmem = tmem + C::kTmemO + t * 128;
       const uint32_t a_tmem = tmem + C::kTmemS + t * 128;
-#pragma unroll
-      for (int kk = 0; kk < kKeyTile / 16; ++kk)
-        mma_ts(d_tmem, a_tmem + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO,
-               (acc || kk > 0) ? 1u : 0u);
+      mma_ts_tile(d_tmem, a_tmem, db, idO, acc);
       if (lo) issue_pv_lo(d_tmem, a_tmem, db, idO);
     };
     bool ok = wait_warp(&q_full, 0, abort, wlim) && wait_warp(&k_full[0], 0, abort, wlim);

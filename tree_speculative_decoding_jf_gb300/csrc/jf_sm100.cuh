@@ -218,34 +218,10 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // MMA issue from a whole warp.  Every lane of the warp runs the issuing code (so loop
 // counters and descriptors stay warp-uniform) and elect.sync picks the one lane that
-// executes the tcgen05 instruction: always the same lane while the warp is converged, so
+// executes the tcgen05 instructions: always the same lane while the warp is converged, so
 // the commits below track that lane's MMAs.  Issuing from lane 0 inside a divergent branch
 // instead measured ~110-120 cycles per 128x128x16 MMA next to busy softmax warps on the
 // same scheduler, against ~75-80 in this form (64 when the scheduler is otherwise idle).
-//
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 in, fp32 accumulate).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-      "elect.sync r|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16 (whole warp, one elected lane issues).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\t"
-      "elect.sync r|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 
 // The mbarrier gets one arrival when every tcgen05 op the elected lane issued so far is
 // done (whole warp calls).
@@ -257,6 +233,64 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+
+// The K-step MMAs of one 128 x N tile (kind::f16: bf16 in, fp32 accumulate) from a whole
+// warp in one block: one elect.sync, constant accumulate predicates and 32-bit adds on the
+// descriptors' start-address word (the word above it stays fixed; addresses stay below
+// 256 KB, so the 14-bit field never carries into the next one).
+// SS form: D[tmem] = sum_k A_k * B_k^T over KSTEPS steps of 16 (8 for a 128-wide K, 4 for
+// 64), A_k / B_k at start-address offsets (16-byte units) from adesc / bdesc.
+#define JF_MMA_SS_STEP(OFF, P) \
+  "add.u32 al, %1, " #OFF ";\n\tadd.u32 bl, %3, " #OFF ";\n\t" \
+  "mov.b64 ad, {al, %2};\n\tmov.b64 bd, {bl, %4};\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, " #P ";\n\t"
+template <int KSTEPS>
+__device__ __forceinline__ void mma_ss_tile(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  static_assert(KSTEPS == 8 || KSTEPS == 4, "D = 128 or 64");
+  const uint32_t alo = static_cast<uint32_t>(adesc), ahi = static_cast<uint32_t>(adesc >> 32);
+  const uint32_t blo = static_cast<uint32_t>(bdesc), bhi = static_cast<uint32_t>(bdesc >> 32);
+  if constexpr (KSTEPS == 8) {
+    // K steps of 16 bf16 (32 bytes) inside a 128-byte swizzle row, then the second 64-column
+    // half 16 KB further on (1024 units of 16 bytes).
+    asm volatile(
+        "{\n\t.reg .pred e, pz, pa;\n\t.reg .b32 r, al, bl;\n\t.reg .b64 ad, bd;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\t"
+        JF_MMA_SS_STEP(0, pz) JF_MMA_SS_STEP(2, pa) JF_MMA_SS_STEP(4, pa) JF_MMA_SS_STEP(6, pa)
+        JF_MMA_SS_STEP(1024, pa) JF_MMA_SS_STEP(1026, pa) JF_MMA_SS_STEP(1028, pa) JF_MMA_SS_STEP(1030, pa)
+        "}" ::"r"(d_tmem), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, pz, pa;\n\t.reg .b32 r, al, bl;\n\t.reg .b64 ad, bd;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\t"
+        "setp.ne.b32 pz, 0, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\t"
+        JF_MMA_SS_STEP(0, pz) JF_MMA_SS_STEP(2, pa) JF_MMA_SS_STEP(4, pa) JF_MMA_SS_STEP(6, pa)
+        "}" ::"r"(d_tmem), "r"(alo), "r"(ahi), "r"(blo), "r"(bhi), "r"(idesc)
+        : "memory");
+  }
+}
+#undef JF_MMA_SS_STEP
+
+// TS form over 128 keys: D[tmem] (+)= sum_k A[tmem cols a + 8k] * B_k, B_k 16 rows of 128
+// bytes (128 units of 16 bytes) apart; the first MMA accumulates onto D only if acc0.
+#define JF_MMA_TS_STEP(ACOL, BOFF, P) \
+  "add.u32 at, %1, " #ACOL ";\n\tadd.u32 bl, %2, " #BOFF ";\n\t" \
+  "mov.b64 bd, {bl, %3};\n\t" \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %4, " #P ";\n\t"
+__device__ __forceinline__ void mma_ts_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            bool acc0) {
+  const uint32_t blo = static_cast<uint32_t>(bdesc), bhi = static_cast<uint32_t>(bdesc >> 32);
+  asm volatile(
+      "{\n\t.reg .pred e, p0, pa;\n\t.reg .b32 r, at, bl;\n\t.reg .b64 bd;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pa, 0, 0;\n\t"
+      JF_MMA_TS_STEP(0, 0, p0) JF_MMA_TS_STEP(8, 128, pa) JF_MMA_TS_STEP(16, 256, pa) JF_MMA_TS_STEP(24, 384, pa)
+      JF_MMA_TS_STEP(32, 512, pa) JF_MMA_TS_STEP(40, 640, pa) JF_MMA_TS_STEP(48, 768, pa) JF_MMA_TS_STEP(56, 896, pa)
+      "}" ::"r"(d_tmem), "r"(a_tmem), "r"(blo), "r"(bhi), "r"(idesc), "r"(acc0 ? 1u : 0u)
+      : "memory");
+}
+#undef JF_MMA_TS_STEP
 
 // Shared-memory matrix descriptor, 128-byte swizzle.  Addresses and offsets in bytes.
 //   K-major operand: rows of 128 B (64 bf16 along K), 8-row groups SBO bytes apart; LBO
