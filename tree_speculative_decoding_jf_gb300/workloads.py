@@ -357,3 +357,27 @@ def sampling_uniforms(B: int, N: int, seed: int = 0):
     u = rng.random((B, N), dtype=np.float32)
     bu = rng.random(B, dtype=np.float32)
     return u, bu
+
+
+# ----------------------------------------------------------------------------- sharding
+
+def shard_sequences(B: int, rank: int, world: int) -> np.ndarray:
+    """Sequences of one batch that rank `rank` of `world` owns when the batch is split
+    across GPUs: b = rank, rank + world, ...  Sequences are independent through the whole
+    path (mask, attention, verify), so the split needs no exchange."""
+    if not (0 <= rank < world):
+        raise ValueError(f"rank {rank} outside a world of {world}")
+    return np.arange(rank, B, world, dtype=np.int64)
+
+
+def sub_workload(w: Workload, seqs) -> Workload:
+    """The workload of sequences `seqs` of `w`: every per-sequence array is taken in that
+    order; the paged K/V pool is shared as is (the block-table rows keep their page ids)."""
+    seqs = np.asarray(seqs, dtype=np.int64)
+    if seqs.size == 0:
+        raise ValueError("a shard needs at least one sequence")
+    return dataclasses.replace(
+        w, name=f"{w.name}[{','.join(str(int(b)) for b in seqs)}]", B=int(seqs.size),
+        prefix_len=w.prefix_len[seqs].copy(), parent=w.parent[seqs].copy(), q=w.q[seqs].copy(),
+        block_table=w.block_table[seqs].copy(), logits=w.logits[seqs].copy(),
+        draft=w.draft[seqs].copy())
