@@ -277,6 +277,43 @@ def test_attention_configs(jf, name, nrows):
     assert_attention_close(w, out, lse, rows)
 
 
+def first_stream_k_cut_pair(w, sms):
+    """(b, kv-head) of the first pair that a stream-K range boundary cuts inside, for the
+    range partition the attention call uses on `sms` SMs: the key tiles of all pairs laid
+    end to end head-major (pair (b, g) at g*S + pre[b], S = tiles of one head over all
+    sequences) and cut into nvirt = sms // n_groups ranges of q or q + 1 tiles."""
+    G = w.Hq // w.Hkv
+    n_groups = -(-(-(-w.N * G // 128)) // 2)
+    tiles = [-(-(int(w.prefix_len[b]) + w.N) // 128) for b in range(w.B)]
+    pre = np.concatenate([[0], np.cumsum(tiles)])
+    S = int(pre[-1])
+    nvirt = sms // n_groups
+    q, rem = divmod(w.Hkv * S, nvirt)
+    for v in range(1, nvirt):
+        x = v * q + min(v, rem)
+        g, off = divmod(x, S)
+        b = int(np.searchsorted(pre, off, side="right") - 1)
+        if off > pre[b]:
+            return b, g
+    return None
+
+
+def test_attention_c5_every_row_of_a_stream_k_cut_pair(jf):
+    """Rows of a (sequence, kv-head) pair split between two stream-K ranges are merged by
+    the boundary combine: check every row of the first such pair against the oracle."""
+    w = cfg("c5_qwen3_30b_b8_tree256_32k")
+    cut = first_stream_k_cut_pair(w, torch.cuda.get_device_properties(0).multi_processor_count)
+    if cut is None:
+        pytest.skip("every range boundary falls between pairs on this SM count")
+    b, g = cut
+    G = w.Hq // w.Hkv
+    i, h = np.meshgrid(np.arange(w.N), np.arange(g * G, (g + 1) * G), indexing="ij")
+    rows = (np.full(i.size, b), h.ravel(), i.ravel())
+    out, lse, err = gpu_attention(jf, w)
+    assert err == 0
+    assert_attention_close(w, out, lse, rows)
+
+
 SHAPES = [  # B, N, Hq, Hkv, D, P, tree
     (1, 1, 4, 1, 64, 0, "chain"),
     (1, 1, 8, 2, 128, 1, "chain"),
