@@ -761,73 +761,75 @@ __device__ __forceinline__ void stats_add(const float (&x)[NV], float k, float& 
   acc.add(part[0]);
 }
 
+// One warp per (row, chunk): lane-strided 16-byte vectors, kInFlight per lane in flight, each
+// vector folded into the lane's running (m, Kahan sum) by stats_add; the warp then combines
+// its lanes: M = max m, S = sum_lanes sum * 2^((m - M) k), in fp32 (GB300's fp64 rate is
+// low; the lanes' sums are already compensated).  No block-wide barrier: the CTA's warps
+// (up to kSampleThreads / 32; fewer when there are few chunks, so the CTAs still spread
+// over the SMs) work on consecutive chunks independently.
 template <typename T>
 __global__ void __launch_bounds__(kSampleThreads)
-    sample_stats_kernel(const T* __restrict__ logits, long long V, int chunks, int chunk_len,
-                        float inv_t, float2* __restrict__ stats) {
+    sample_stats_kernel(const T* __restrict__ logits, long long V, long long total_chunks, int chunks,
+                        int chunk_len, float inv_t, float2* __restrict__ stats) {
   constexpr int kVec = 16 / sizeof(T);
-  constexpr int kInFlight = 4;
-  __shared__ float s_m[kSampleThreads / 32];
-  __shared__ double s_s[kSampleThreads / 32];
+  constexpr int kInFlight = 8;
   grid_dependency_wait();
-  const long long row = blockIdx.x / chunks;
-  const int c = blockIdx.x - static_cast<int>(row * chunks);
-  const long long s = static_cast<long long>(c) * chunk_len;
-  const long long e = min(V, s + chunk_len);
-  const T* base = logits + row * V;
-  const float k = inv_t * 1.4426950408889634f;       // exp(y / T) = 2^(y * k)
-  float m = -INFINITY;
-  KahanSum acc;
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(base + s);
-  long long head = ((16 - (addr & 15)) & 15) / sizeof(T);
-  if (head > e - s) head = e - s;
-  const long long body0 = s + head;
-  const long long nvec = (e - body0) / kVec;
-  const long long body1 = body0 + nvec * kVec;
-  if (threadIdx.x < head) {
-    const float x[1] = {to_f<T>(base[s + threadIdx.x])};
-    stats_add<1>(x, k, m, acc);
-  }
-  const uint4* vb = reinterpret_cast<const uint4*>(base + body0);
-  for (long long v0 = threadIdx.x; v0 < nvec; v0 += kSampleThreads * kInFlight) {
-    uint4 q[kInFlight];
-#pragma unroll
-    for (int u = 0; u < kInFlight; ++u) {
-      const long long vi = v0 + static_cast<long long>(u) * kSampleThreads;
-      if (vi < nvec) q[u] = __ldcs(vb + vi);
+  const int lane = threadIdx.x & 31;
+  const long long gc = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (gc < total_chunks) {
+    const long long row = gc / chunks;
+    const int c = static_cast<int>(gc - row * chunks);
+    const long long s = static_cast<long long>(c) * chunk_len;
+    const long long e = min(V, s + chunk_len);
+    const T* base = logits + row * V;
+    const float k = inv_t * 1.4426950408889634f;       // exp(y / T) = 2^(y * k)
+    float m = -INFINITY;
+    KahanSum acc;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(base + s);
+    long long head = ((16 - (addr & 15)) & 15) / sizeof(T);
+    if (head > e - s) head = e - s;
+    const long long body0 = s + head;
+    const int nvec = static_cast<int>((e - body0) / kVec);
+    const long long body1 = body0 + static_cast<long long>(nvec) * kVec;
+    if (lane < head) {
+      const float x[1] = {to_f<T>(base[s + lane])};
+      stats_add<1>(x, k, m, acc);
     }
+    const uint4* vb = reinterpret_cast<const uint4*>(base + body0);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kInFlight) {
+      uint4 q[kInFlight];
 #pragma unroll
-    for (int u = 0; u < kInFlight; ++u) {
-      const long long vi = v0 + static_cast<long long>(u) * kSampleThreads;
-      if (vi < nvec) {
-        float x[kVec];
-        if constexpr (sizeof(T) == 2) {
-          x[0] = bf16_lo(q[u].x); x[1] = bf16_hi(q[u].x); x[2] = bf16_lo(q[u].y); x[3] = bf16_hi(q[u].y);
-          x[4] = bf16_lo(q[u].z); x[5] = bf16_hi(q[u].z); x[6] = bf16_lo(q[u].w); x[7] = bf16_hi(q[u].w);
-        } else {
-          x[0] = __uint_as_float(q[u].x); x[1] = __uint_as_float(q[u].y);
-          x[2] = __uint_as_float(q[u].z); x[3] = __uint_as_float(q[u].w);
+      for (int u = 0; u < kInFlight; ++u) {
+        const int vi = v0 + u * 32;
+        if (vi < nvec) q[u] = __ldcs(vb + vi);
+      }
+#pragma unroll
+      for (int u = 0; u < kInFlight; ++u) {
+        const int vi = v0 + u * 32;
+        if (vi < nvec) {
+          float x[kVec];
+          if constexpr (sizeof(T) == 2) {
+            x[0] = bf16_lo(q[u].x); x[1] = bf16_hi(q[u].x); x[2] = bf16_lo(q[u].y); x[3] = bf16_hi(q[u].y);
+            x[4] = bf16_lo(q[u].z); x[5] = bf16_hi(q[u].z); x[6] = bf16_lo(q[u].w); x[7] = bf16_hi(q[u].w);
+          } else {
+            x[0] = __uint_as_float(q[u].x); x[1] = __uint_as_float(q[u].y);
+            x[2] = __uint_as_float(q[u].z); x[3] = __uint_as_float(q[u].w);
+          }
+          stats_add<kVec>(x, k, m, acc);
         }
-        stats_add<kVec>(x, k, m, acc);
       }
     }
-  }
-  if (threadIdx.x < e - body1) {
-    const float x[1] = {to_f<T>(base[body1 + threadIdx.x])};
-    stats_add<1>(x, k, m, acc);
-  }
-  // combine the threads' (m, sum) pairs: M = max m, S = sum_t sum_t * 2^((m_t - M) k); the
-  // rescale and the warp sums in fp32 (GB300's fp64 rate is low), the eight warp sums in fp64
-  const float M = block_max_f32(m, s_m);
-  float mine = (m == -INFINITY) ? 0.f : (acc.s - acc.c) * fast_exp2((m - M) * k);
+    if (lane < e - body1) {
+      const float x[1] = {to_f<T>(base[body1 + lane])};
+      stats_add<1>(x, k, m, acc);
+    }
+    float M = m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-  if ((threadIdx.x & 31) == 0) s_s[threadIdx.x >> 5] = static_cast<double>(mine);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double tot = 0.0;
-    for (int w = 0; w < kSampleThreads / 32; ++w) tot += s_s[w];
-    stats[blockIdx.x] = make_float2(M, static_cast<float>(tot));
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float mine = (m == -INFINITY) ? 0.f : (acc.s - acc.c) * fast_exp2((m - M) * k);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    if (lane == 0) stats[gc] = make_float2(M, mine);
   }
   grid_dependents_launch();
 }
@@ -890,6 +892,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   int32_t* s_rej = reinterpret_cast<int32_t*>(s_lg + N);                  // [N] rejected tokens
   double* s_rejp = reinterpret_cast<double*>(                             // [N] their probabilities
       (reinterpret_cast<uintptr_t>(s_rej + N) + 7) & ~static_cast<uintptr_t>(7));
+  double* s_pk = s_rejp + N;            // [N] target probabilities of the children's tokens
   __shared__ double s_redd[kSampleThreads / 32];
   __shared__ float s_redf[kSampleThreads / 32];
   __shared__ int s_redi[kSampleThreads / 32];
@@ -922,7 +925,8 @@ __global__ void __launch_bounds__(kSampleThreads)
   const int per = (N + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
   const int c_lo = min(N, static_cast<int>(threadIdx.x) * per), c_hi = min(N, c_lo + per);
   int u = 0, n = 0;
-  double M = 0.0, Z = 1.0;
+  double M = 0.0, Z = 1.0, invZ = 1.0;
+  const double invTd = 1.0 / Td;
   for (;;) {
     const T* row = logits + (rb + u) * V;
     const float2* st = stats + (rb + u) * chunks;
@@ -930,10 +934,14 @@ __global__ void __launch_bounds__(kSampleThreads)
     float mloc = -INFINITY;
     for (int c = threadIdx.x; c < chunks; c += blockDim.x) mloc = fmaxf(mloc, st[c].x);
     M = block_max_f32(mloc, s_redf);
+    // fp64 sums of fp32 exponentials of fp64 arguments: exp's ~1e-7 relative error is far
+    // below the 1e-5 margin the decisions are held to, and fp64 exp / division are slow on
+    // this GPU (one division per node: the probabilities multiply by 1 / Z).
     double zloc = 0.0;
     for (int c = threadIdx.x; c < chunks; c += blockDim.x)
-      zloc += static_cast<double>(st[c].y) * exp((static_cast<double>(st[c].x) - M) / Td);
+      zloc += static_cast<double>(st[c].y) * expf(static_cast<float>((static_cast<double>(st[c].x) - M) * invTd));
     Z = block_sum_f64(zloc, s_redd);
+    invZ = 1.0 / Z;
     // children of u in id order, and their logits
     int cnt = 0;
     for (int c = c_lo; c < c_hi; ++c) cnt += (s_par[c] == u) ? 1 : 0;
@@ -942,9 +950,14 @@ __global__ void __launch_bounds__(kSampleThreads)
     for (int c = c_lo; c < c_hi; ++c)
       if (s_par[c] == u) s_kids[off++] = c;
     __syncthreads();
+    // the children's target probabilities p(x) = exp((l_x - M) / T) / Z, one thread each
+    // (fp64 is slow on this GPU: the ordered decisions below only read them)
     for (int k = threadIdx.x; k < nk; k += blockDim.x) {
       const int x = s_draft[s_kids[k]];
-      s_lg[k] = x >= 0 ? to_f<T>(row[x]) : -INFINITY;
+      const float lg = x >= 0 ? to_f<T>(row[x]) : -INFINITY;
+      s_lg[k] = lg;
+      s_pk[k] = x >= 0 ? static_cast<double>(expf(static_cast<float>((static_cast<double>(lg) - M) * invTd))) * invZ
+                       : 0.0;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -955,7 +968,7 @@ __global__ void __launch_bounds__(kSampleThreads)
         const int x = s_draft[c];
         bool seen = x < 0;
         for (int r = 0; r < nrej && !seen; ++r) seen = s_rej[r] == x;
-        const double p = seen ? 0.0 : exp((static_cast<double>(s_lg[k]) - M) / Td) / Z;
+        const double p = seen ? 0.0 : s_pk[k];
         if (static_cast<double>(uniform[rb + c]) * (1.0 - rej) < p) {
           next = c;
           break;
@@ -982,27 +995,52 @@ __global__ void __launch_bounds__(kSampleThreads)
   const double target = static_cast<double>(bonus_uniform[b]) * (1.0 - s_rejmass);
   const T* row = logits + (rb + u) * V;
   const float2* st = stats + (rb + u) * chunks;
-  if (threadIdx.x == 0) {
-    double cum = 0.0;
-    int cs = chunks - 1;
-    double base = 0.0;
-    for (int c = 0; c < chunks; ++c) {
+  // The chunk holding the threshold: residual chunk masses (the chunk's mass minus its
+  // rejected tokens' probabilities), each thread over a contiguous range of chunks, an fp64
+  // block scan over the ranges, then the thread whose range crosses the threshold walks it.
+  {
+    const int cpt = (chunks + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    const int q0 = min(chunks, static_cast<int>(threadIdx.x) * cpt), q1 = min(chunks, q0 + cpt);
+    auto chunk_mass = [&](int c) -> double {
       const long long s0 = static_cast<long long>(c) * chunk_len, e0 = min(V, s0 + chunk_len);
-      double w = static_cast<double>(st[c].y) * exp((static_cast<double>(st[c].x) - M) / Td) / Z;
+      double w = static_cast<double>(st[c].y) *
+                 expf(static_cast<float>((static_cast<double>(st[c].x) - M) * invTd)) * invZ;
       for (int r = 0; r < nrej; ++r)
         if (s_rej[r] >= s0 && s_rej[r] < e0) w -= s_rejp[r];
-      if (cum + w > target || c == chunks - 1) {
-        cs = c;
-        base = cum;
-        break;
+      return w;
+    };
+    double mine_w = 0.0;
+    for (int c = q0; c < q1; ++c) mine_w += chunk_mass(c);
+    if (threadIdx.x == 0) s_chunk = 0x7fffffff;
+    double all_w = 0.0;
+    const double before_w = block_excl_scan_f64(mine_w, s_redd, &all_w);
+    // the first chunk c with (mass of the chunks before c) + w_c > target; masses can be a
+    // rounding error below zero, so every range looks for its own first crossing
+    int my_c = -1;
+    double my_base = 0.0;
+    {
+      double cum = before_w;
+      for (int c = q0; c < q1; ++c) {
+        const double w = chunk_mass(c);
+        if (cum + w > target) { my_c = c; my_base = cum; break; }
+        cum += w;
       }
-      cum += w;
     }
-    s_chunk = cs;
-    s_base = base;
-    s_y = -1;
+    if (my_c >= 0) atomicMin(&s_chunk, my_c);
+    __syncthreads();
+    const bool none = s_chunk == 0x7fffffff;
+    if (!none && my_c == s_chunk) s_base = my_base;
+    __syncthreads();
+    if (none && q0 <= chunks - 1 && chunks - 1 < q1) {
+      // rounding past the last chunk: the last one, after the mass of all the others
+      double cum = before_w;
+      for (int c = q0; c < chunks - 1; ++c) cum += chunk_mass(c);
+      s_chunk = chunks - 1;
+      s_base = cum;
+    }
+    if (threadIdx.x == 0) s_y = -1;
+    __syncthreads();
   }
-  __syncthreads();
   // The chunk's logits, 32 per thread in token order, all loads in flight together.
   constexpr int kSeg = kSampleChunk / kSampleThreads;
   const long long cs0 = static_cast<long long>(s_chunk) * chunk_len;
@@ -1024,7 +1062,7 @@ __global__ void __launch_bounds__(kSampleThreads)
   KahanSum ks;
 #pragma unroll
   for (int e = 0; e < kSeg; ++e) ks.add(ev[e]);
-  const double mine = (static_cast<double>(ks.s) - static_cast<double>(ks.c)) / Z;
+  const double mine = (static_cast<double>(ks.s) - static_cast<double>(ks.c)) * invZ;
   double all = 0.0;
   const double before = s_base + block_excl_scan_f64(mine, s_redd, &all);
   if (mine > 0.0 && before <= target && target < before + mine) {
@@ -1033,7 +1071,7 @@ __global__ void __launch_bounds__(kSampleThreads)
 #pragma unroll
     for (int e = 0; e < kSeg; ++e) {
       if (ev[e] > 0.f) last = e;
-      cum += static_cast<double>(ev[e]) / Z;
+      cum += static_cast<double>(ev[e]) * invZ;
       if (y < 0 && cum > target) y = e;
     }
     s_y = static_cast<int>(t0) + (y >= 0 ? y : last);
@@ -1091,20 +1129,24 @@ extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, c
   if (!jf::aligned_to(logits, dtype == JF_DTYPE_BF16 ? 2 : 4)) return JF_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float2* stats = static_cast<float2*>(workspace);
-  const long long grid = static_cast<long long>(B) * N * p.chunks;
+  const long long total = static_cast<long long>(B) * N * p.chunks;     // one warp each
+  const int sms = jf::current_sm_count() > 0 ? jf::current_sm_count() : 148;
+  int warps = jf::kSampleThreads / 32;
+  while (warps > 1 && total < static_cast<long long>(warps) * 4 * sms) warps >>= 1;
+  const long long grid = (total + warps - 1) / warps;
   if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
   const long long Vl = V;
   const float inv_t = 1.f / temperature;
   const cudaError_t ea =
       dtype == JF_DTYPE_BF16
           ? jf::launch_pdl(jf::sample_stats_kernel<uint16_t>, dim3(static_cast<unsigned>(grid)),
-                           dim3(jf::kSampleThreads), 0, s, static_cast<const uint16_t*>(logits), Vl,
-                           p.chunks, p.chunk_len, inv_t, stats)
+                           dim3(32 * warps), 0, s, static_cast<const uint16_t*>(logits), Vl,
+                           total, p.chunks, p.chunk_len, inv_t, stats)
           : jf::launch_pdl(jf::sample_stats_kernel<float>, dim3(static_cast<unsigned>(grid)),
-                           dim3(jf::kSampleThreads), 0, s, static_cast<const float*>(logits), Vl,
-                           p.chunks, p.chunk_len, inv_t, stats);
+                           dim3(32 * warps), 0, s, static_cast<const float*>(logits), Vl,
+                           total, p.chunks, p.chunk_len, inv_t, stats);
   if (ea != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * (6 * sizeof(int32_t) + sizeof(double)) + 16;
+  const size_t smem = static_cast<size_t>(N) * (6 * sizeof(int32_t) + 2 * sizeof(double)) + 16;
   auto walk = [&](auto kern, const auto* lg) -> cudaError_t {
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
