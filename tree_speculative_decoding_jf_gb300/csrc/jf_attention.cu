@@ -10,33 +10,42 @@
 // node share one mask row and the contraction has a real M dimension.  Rows come in
 // 128-row tiles; one CTA owns NT tiles (NT = 2 when there are at least two) and a range
 // of 128-key tiles ("split"), so every K/V tile it loads feeds NT tensor-core tiles.
-// Splits and CTA count are chosen on the host from the SM count; partial results of a
-// split go to a workspace and a second kernel merges them by log-sum-exp.
+// Splits and CTA count are chosen on the host from the SM count.  The partial results of
+// a unit's splits merge by log-sum-exp either inside a thread-block cluster through
+// distributed shared memory or, through a workspace, in a combine kernel launched as a
+// programmatic dependent.  With more units than SMs and several row-tile groups per
+// kv-head, a stream-K variant runs one CTA per SM over equal ranges of all key tiles.
 //
 // Roles inside a CTA (128 * (1 + NT) threads):
 //   warp 0      TMA producer: page ids travel through registers four tiles ahead (bounds-
-//               checked at use); Q is loaded once; per key tile K then V go into a
-//               STAGES-deep ring as one 128-row box per 64-column half when the tile's eight
-//               pages are consecutive in the pool, else one box per (page, half) issued by
-//               16 lanes at once.  Pages past the sequence end load as zeros.
-//   warp 1      allocates TMEM and issues tcgen05.mma from one lane:
+//               checked at use); Q is loaded once; per key tile K then V go into a ring
+//               (2 K + 3 V stages for D = 128) as one 128-row box per 64-column half when the
+//               tile's eight pages are consecutive in the pool, else one box per (page,
+//               half) issued by 16 lanes at once.  Pages past the sequence end load as
+//               zeros, and V rows past the sequence end in the last tile are zeroed once it
+//               has landed (garbage in unused page slots must not meet a zero probability
+//               as NaN).  A stage is reloaded once a step record (below) says the MMAs
+//               that read it have completed.
+//   warp 1      allocates TMEM and issues the MMAs; the whole warp runs the issue loop and
+//               one elected lane executes the tcgen05 instructions, a row tile's 8 K-step
+//               MMAs from one inline-PTX block:
 //                 S_t = Q_t K^T  (128 x 128, fp32 in TMEM),  O_t += P_t V  (P from TMEM).
-//               A V stage is released as soon as the tile's last PV MMA is issued, a K
-//               stage as soon as the next tile's S MMAs are.  It zeroes V rows past the
-//               sequence end in the last tile (garbage in unused page slots must not meet
-//               a zero probability as NaN).
+//               Row tile t's step j (PV of key tile j, then S of key tile j + 1) goes once
+//               its softmax and its data voucher have arrived; after the last row tile's
+//               step j one commit completes step record j + 1.
+//   warps 2..   data vouchers, one per row tile: the last arrival on p_full[t] once the V
+//               and K tiles that the step reads have landed.
 //   warps 4..   one warpgroup per row tile t: TMEM lane = row, so each thread owns one
-//               full score row.  Ancestor bitmasks of the tile's nodes are staged in
-//               shared memory; on tiles reaching positions >= P_b they become one 32-bit
-//               visibility word per 32 keys.  Online softmax in the log2 domain (row max
-//               and row sum over independent partial accumulators); the running max is
-//               only raised when a tile's max exceeds it by more than 8 (factor 256),
-//               which keeps P <= 256 in bf16 and makes the O rescale (TMEM
-//               load/scale/store) rare.  P (bf16) is written back into the S columns and
-//               consumed by the PV MMA from TMEM.
-// The control warpgroup hands registers to the softmax warpgroups (setmaxnreg).  Split
-// partials go to a workspace laid out [b][kv-head][split][row][D] (row-contiguous per CTA)
-// and a combine kernel, launched as a programmatic dependent, merges them.
+//               full score row.  On key tiles reaching positions >= P_b the node's
+//               ancestor-mask words are read into registers before the tile's S is waited
+//               for and turned into one 32-bit visibility word per 32 keys.  Online softmax
+//               in the log2 domain (row max and row sum over independent partial
+//               accumulators); the running max is only raised when a tile's max exceeds it
+//               by more than 8 (factor 256), which keeps P <= 256 in bf16 and makes the O
+//               rescale (TMEM load/scale/store) rare.  P (bf16; hi + lo parts on tree tiles
+//               of short prefixes) is written back into the S columns and consumed by the
+//               PV MMA from TMEM.
+// The control warpgroup hands registers to the softmax warpgroups (setmaxnreg).
 // All waits are bounded (see jf_sm100.cuh); on a timeout the CTA records
 // JF_DEVERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
