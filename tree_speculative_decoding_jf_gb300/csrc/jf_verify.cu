@@ -660,14 +660,14 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
 // candidates); with no acceptance the bonus token is drawn from the residual by inverse
 // CDF with bonus_uniform.  Every emitted token then follows the target distribution.
 //
-// Kernel 1 (HBM-bound, the argmax grid): per (row, chunk) the chunk's largest logit m_c and
-// the Kahan-compensated sum s_c of exp((x - m_c) / T).  Kernel 2 (one CTA per sequence):
-// per visited node, M = max_c m_c and Z = sum_c s_c exp((m_c - M) / T) in fp64, the
-// node's children in id order (a block scan over contiguous node ranges), their logits
-// gathered at once, then one thread takes the acceptance decisions in fp64.  The bonus
-// draw finds the chunk where the residual CDF crosses the threshold from the chunk sums,
-// then scans that one chunk: per-thread Kahan sums, an fp64 block scan, and one thread
-// re-walks its segment.
+// Kernel 1 (HBM-bound, one warp per (row, 8192-logit chunk)): the chunk's largest logit
+// m_c and the Kahan-compensated sum s_c of exp((x - m_c) / T).  Kernel 2 (one CTA per
+// sequence): per visited node, M = max_c m_c and Z = sum_c s_c exp((m_c - M) / T) (fp64
+// sums), the node's children in id order (a block scan over contiguous node ranges), their
+// target probabilities computed in parallel, then one thread takes the ordered acceptance
+// decisions from them in fp64.  The bonus draw finds the first chunk where the residual CDF
+// crosses the threshold (per-thread chunk masses and an fp64 block scan), then scans that
+// one chunk: per-thread Kahan sums, an fp64 block scan, and one thread re-walks its segment.
 namespace jf {
 namespace {
 
