@@ -1,0 +1,75 @@
+"""Seeded random attention shapes against the fp64 oracle, through the C ABI.
+
+The planner picks among several dispatches (one CTA per unit, key splits merged in a
+cluster or by the combine kernel, longest-first order, stream-K ranges) from B, N, G, Hkv,
+D and the prefix lengths; fixed test shapes reach each of them once.  These cases draw the
+shapes at random (fixed seeds) so that the dispatch boundaries, odd row counts, mixed
+prefix lengths (including empty ones) and deep or flat trees meet in combinations nobody
+picked by hand.  Every row is compared when there are few, else a sample that includes
+each sequence's root, last and deepest node."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_speculative_decoding_jf_gb300 import workloads as wl
+from test_gpu_parity import assert_attention_close, gpu_attention, jf, sample_rows  # noqa: F401 (fixture)
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 48
+
+
+def draw(case):
+    rng = np.random.default_rng(9000 + case)
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    B = int(rng.choice([1, 2, 3, 5, 8, 13, 24, 40]))
+    N = int(rng.choice([1, 7, 16, 33, 64, 100, 200, 256]))
+    while B * N * G * Hkv > 120000:                      # keep the oracle's share small
+        B = max(1, B // 2)
+        N = max(1, N // 2)
+    prefix = rng.integers(0, 3000, B).astype(np.int32)
+    prefix[rng.random(B) < 0.15] = 0                     # some sequences without prefix
+    prefix[rng.random(B) < 0.15] = rng.integers(1, 4)    # and some of 1..3 keys
+    kind = rng.choice(["window", "chain", "star", "deep"])
+    parents = []
+    for _ in range(B):
+        if kind == "chain":
+            par = np.arange(-1, N - 1)
+        elif kind == "star":
+            par = np.array([-1] + [0] * (N - 1))
+        else:
+            width = 2 if kind == "deep" else int(rng.integers(2, 9))
+            par = np.array([-1] + [rng.integers(max(0, i - width), i) for i in range(1, N)])
+        parents.append(par.astype(np.int32))
+    parent = np.stack(parents)
+    w = wl.make_workload(f"fuzz{case}", B, N, G * Hkv, Hkv, D, 64, prefix, tree="chain",
+                         parent=parent, permute_pages=bool(rng.random() < 0.7), seed=case,
+                         with_logits=False)
+    return w
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_attention_random_shapes(jf, case):
+    w = draw(case)
+    out, lse, err = gpu_attention(jf, w)
+    assert err == 0
+    assert np.isfinite(out).all()
+    nrows = w.B * w.N * w.Hq
+    rows = oracle.all_rows(w) if nrows <= 6144 else sample_rows(w, 1536, seed=case)
+    assert_attention_close(w, out, lse, rows)
+
+
+def test_fuzz_shapes_cover_the_dispatches():
+    """The draw reaches stream-K-sized calls (units >= 152 with two or more row-tile groups
+    per kv-head), single-unit calls and both head dims (checked on the shapes alone)."""
+    shapes = [draw(c) for c in range(N_CASES)]
+    def units(w):
+        mt = -(-w.N * (w.Hq // w.Hkv) // 128)
+        groups = -(-mt // 2) if mt >= 2 else mt
+        return w.B * w.Hkv * groups, groups
+    assert any(units(w)[0] >= 152 and units(w)[1] >= 2 for w in shapes)
+    assert any(units(w)[0] == 1 for w in shapes) or any(units(w)[0] < 8 for w in shapes)
+    assert {w.D for w in shapes} == {64, 128}
