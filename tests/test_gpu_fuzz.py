@@ -73,3 +73,27 @@ def test_fuzz_shapes_cover_the_dispatches():
     assert any(units(w)[0] >= 152 and units(w)[1] >= 2 for w in shapes)
     assert any(units(w)[0] == 1 for w in shapes) or any(units(w)[0] < 8 for w in shapes)
     assert {w.D for w in shapes} == {64, 128}
+
+
+# ----------------------------------------------------------------------------- ragged
+
+N_RAGGED = 16
+
+
+@pytest.mark.parametrize("case", range(N_RAGGED))
+def test_ragged_attention_random_shapes(jf, case):
+    """Random shapes again, now with a random tree size per sequence (some one-node, some
+    full) and hostile padding (out-of-range parents, NaN K/V in the padding slots, -1 block
+    table past the needed pages); rows of the first n_b nodes against the oracle run on
+    each sequence's slice."""
+    from test_gpu_ragged import check_rows, poison_padding, ragged_attention
+    w = draw(100 + case)
+    rng = np.random.default_rng(7000 + case)
+    tree_len = [int(x) for x in rng.integers(1, w.N + 1, w.B)]
+    tree_len[0] = w.N
+    if w.B > 1:
+        tree_len[-1] = 1
+    w = poison_padding(w, tree_len)
+    out, lse, err = ragged_attention(jf, w, tree_len)
+    assert err == 0
+    check_rows(w, tree_len, out, lse, rows_per_seq=24 if w.B > 8 else 96, seed=case)
