@@ -97,3 +97,33 @@ def test_ragged_attention_random_shapes(jf, case):
     out, lse, err = ragged_attention(jf, w, tree_len)
     assert err == 0
     check_rows(w, tree_len, out, lse, rows_per_seq=24 if w.B > 8 else 96, seed=case)
+
+
+# ----------------------------------------------------------------------------- verify
+
+N_VERIFY = 24
+
+
+@pytest.mark.parametrize("case", range(N_VERIFY))
+def test_verify_random_shapes(jf, case):
+    """Greedy verification on random trees, vocabularies (odd sizes: unaligned rows and
+    chunk tails), both logit types, with about half of the nodes forced to be accepted
+    (their draft token is the parent's planted maximum): argmax, accepted length, path and
+    bonus bit-exact against the oracle."""
+    from test_gpu_parity import assert_verify_matches
+    rng = np.random.default_rng(5000 + case)
+    V = int(rng.choice([7, 33, 1000, 4097, 32001, 151936]))
+    N = int(rng.choice([1, 2, 16, 64, 100, 256, 700]))
+    B = int(rng.choice([1, 2, 5, 16]))
+    while B * N * V > 60_000_000:
+        if B > 1:
+            B //= 2
+        else:
+            N = max(1, N // 2)
+    width = int(rng.integers(1, 10))
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - width), i) for i in range(1, N)],
+                                np.int32) for _ in range(B)])
+    w = wl.make_workload(f"vfuzz{case}", B, N, 1, 1, 64, V, 8, tree="chain", parent=parent,
+                         logits_dtype=str(rng.choice(["bf16", "f32"])), forcing="half",
+                         seed=300 + case)
+    assert_verify_matches(jf, w)
