@@ -127,3 +127,32 @@ def test_verify_random_shapes(jf, case):
                          logits_dtype=str(rng.choice(["bf16", "f32"])), forcing="half",
                          seed=300 + case)
     assert_verify_matches(jf, w)
+
+
+# ----------------------------------------------------------------------------- draft tree
+
+N_DRAFT = 12
+
+
+@pytest.mark.parametrize("case", range(N_DRAFT))
+def test_draft_tree_random_shapes(jf, case):
+    """Best-first draft trees on random shapes (batch, depths, vocabulary, K, budget, dtype,
+    logit spread), checked against the oracle as in test_gpu_draft_tree: candidates exact,
+    the tree equal to the oracle's up to swaps of near-tied nodes."""
+    from test_gpu_draft_tree import check
+    rng = np.random.default_rng(4000 + case)
+    K = int(rng.integers(1, 9))
+    Dmax = int(rng.integers(1, 17))
+    lattice, level = 1, 1
+    for _ in range(Dmax):
+        level *= K
+        lattice += level
+    N = int(min(lattice, rng.choice([2, 9, 33, 64, 129, 256]), 4096 // (K + 1)))
+    B = int(rng.choice([1, 2, 3, 8, 21]))
+    V = int(rng.choice([K + 3, 500, 4099, 32000, 151936]))
+    while B * Dmax * V > 40_000_000 and B > 1:
+        B //= 2
+    dtype = str(rng.choice(["bf16", "f32"]))
+    sigma = float(rng.choice([0.5, 3.0, 8.0]))
+    x = wl.draft_logits(B, Dmax, V, sigma=sigma, dtype=dtype, seed=600 + case)
+    check(jf, x, dtype, K, N)
