@@ -16,11 +16,11 @@
 // nodes of the candidate lattice in that order (a parent always precedes its children:
 // its score is not lower and its depth is smaller).  The kernel finds them level by
 // level: the level-d candidates are the children of the chosen level-(d-1) nodes (once
-// N nodes are chosen, only those that beat the last of them), and the chosen set is the
-// best N of (chosen so far + candidates), kept sorted with a bitonic sort in shared
-// memory.  A node is identified by its rank path packed into a
-// 64-bit code (4 bits per level, first level in the top bits), so its parent's code is
-// its own with the last digit cleared.
+// N nodes are chosen, only those that beat the last of them), and the chosen set, kept
+// sorted in shared memory, becomes the first N keys of (chosen so far + candidates): each
+// key's place is the number of keys below it.  A node is identified by its rank path
+// packed into a 64-bit code (4 bits per level, first level in the top bits), so its
+// parent's code is its own with the last digit cleared.
 #include <algorithm>
 #include <cmath>
 
@@ -37,7 +37,8 @@ constexpr int kTreeThreads = 1024;
 constexpr int kMaxK = 8;
 constexpr int kMaxDepth = 16;
 constexpr int kMaxTreeN = 256;
-constexpr int kSortCap = 4096;            // >= N + N * K, a power of two
+constexpr int kCandMax = kMaxTreeN * kMaxK;   // candidates of one level, at most
+constexpr int kCountMaxC = 128;          // up to this many candidates are placed by counting
 constexpr int kRowParts = 8;             // most CTAs (one cluster) per logit row
 constexpr int kCandCap = 1024;           // filtered candidates a CTA keeps in shared memory
 
@@ -117,6 +118,66 @@ __device__ __forceinline__ void take(float v, int i, bool valid, PassState& st) 
   }
 }
 
+// bf16 logits two to a 32-bit word (the lower-indexed one in the low half).  The maximum
+// of packed pairs is exact, so the passes fold whole vectors with it.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t bf16x8_max(const uint4& q) {
+  return bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
+}
+
+// Passes 1 and 2 over 16-byte vectors of bf16 logits.  Pass 1 keeps the slice maximum as
+// a packed pair.  Pass 2 sums exp(x - M) as 2^(x log2 e - M log2 e) over the eight logits
+// and looks at them one by one only when the vector's maximum reaches tau.
+template <int PASS>
+__device__ __forceinline__ void bf16_vec_pass(const uint4* xv, int vb, int nvec, PassState& st) {
+  constexpr int kUnroll = 4;
+  constexpr float kLog2e = 1.4426950408889634f;
+  uint32_t pm = 0xFF80FF80u;                    // (-inf, -inf)
+  const float neg_ml = -st.M * kLog2e;
+  float s0 = 0.f, s1 = 0.f;
+  for (int v0 = vb + static_cast<int>(threadIdx.x); v0 < nvec; v0 += blockDim.x * kUnroll) {
+    uint4 buf[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = v0 + u * blockDim.x;
+      buf[u] = v < nvec ? __ldg(xv + v) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int v = v0 + u * blockDim.x;
+      if (PASS == 1) {
+        pm = bf16x2_max(pm, bf16x8_max(buf[u]));
+      } else if (v < nvec) {
+        const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          s0 += fast_exp2(fmaf(bf16_lo(w[k]), kLog2e, neg_ml));
+          s1 += fast_exp2(fmaf(bf16_hi(w[k]), kLog2e, neg_ml));
+        }
+        const uint32_t m2 = bf16x8_max(buf[u]);
+        if (fmaxf(bf16_lo(m2), bf16_hi(m2)) >= st.tau) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float val = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+            if (val >= st.tau) {
+              const int pos = atomicAdd(st.ncand, 1);
+              if (pos < kCandCap) st.cand[pos] = Cand{val, v * 8 + e};
+            }
+          }
+        }
+      }
+    }
+  }
+  if (PASS == 1) st.m = fmaxf(st.m, fmaxf(bf16_lo(pm), bf16_hi(pm)));
+  else st.sum += s0 + s1;
+}
+
 template <typename T, int PASS>
 __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts, PassState& st) {
   constexpr int kPer = 16 / sizeof(T);          // logits per vector
@@ -128,6 +189,9 @@ __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts,
     const int per = (nvec_all + parts - 1) / parts;
     const int vb = min(nvec_all, part * per);
     const int nvec = min(nvec_all, vb + per);
+    if constexpr (sizeof(T) == 2 && PASS != 3) {
+      bf16_vec_pass<PASS>(xv, vb, nvec, st);
+    } else {
     // the warp loops while its first lane still has vectors, so all lanes step together
     for (int w0 = vb + lane0; w0 < nvec; w0 += blockDim.x * kUnroll) {
       const int v0 = w0 + (threadIdx.x & 31);
@@ -152,6 +216,7 @@ __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts,
           take<PASS>(val, v * kPer + e, valid, st);
         }
       }
+    }
     }
     if (part == parts - 1)
       for (int b0 = nvec_all * kPer + lane0; b0 < V; b0 += blockDim.x) {
@@ -215,8 +280,11 @@ __device__ float block_kth_largest(float x, int k, float* scratch) {
 // ranks the whole slice per warp instead (exact either way).  The cluster's first CTA
 // merges the slices through distributed shared memory: M = max m_c,
 // S = sum s_c * exp(m_c - M), lse = M + log S, and the K best of the slices' lists.
-template <typename T>
-__global__ void __launch_bounds__(kTopThreads)
+// kMinBlocks: CTAs an SM must hold (3 caps registers at 40 and keeps a one-wave grid
+// resident at once; 2 leaves the passes unconstrained and, on grids of several waves,
+// keeps fewer rows in flight, so the second pass finds its slice in L2).
+template <typename T, int kMinBlocks>
+__global__ void __launch_bounds__(kTopThreads, kMinBlocks)
     draft_candidates_kernel(const T* __restrict__ logits, int V, int K, int parts,
                             int32_t* __restrict__ cand_token, float* __restrict__ cand_logp) {
   constexpr int kWarps = kTopThreads / 32;
@@ -451,6 +519,18 @@ __device__ __forceinline__ void bitonic_sort_e(uint64_t* hi, uint64_t* lo, uint6
   __syncthreads();
 }
 
+// Number of the first n keys of a sorted array that are below (h, l).
+__device__ __forceinline__ int lower_bound_key(const uint64_t* hi, const uint64_t* lo, int n, uint64_t h,
+                                               uint64_t l) {
+  int a = 0, c = n;
+  while (a < c) {
+    const int m = (a + c) >> 1;
+    if (key_less(hi[m], lo[m], h, l)) a = m + 1;
+    else c = m;
+  }
+  return a;
+}
+
 __device__ void bitonic_sort(uint64_t* hi, uint64_t* lo, uint64_t* bhi, uint64_t* blo, int n) {
   if (n <= kTreeThreads) bitonic_sort_e<1>(hi, lo, bhi, blo, n);
   else if (n <= 2 * kTreeThreads) bitonic_sort_e<2>(hi, lo, bhi, blo, n);
@@ -462,93 +542,129 @@ __global__ void __launch_bounds__(kTreeThreads)
                            const int32_t* __restrict__ root_token, int Dmax, int K, int N,
                            int32_t* __restrict__ parent, int32_t* __restrict__ draft,
                            int32_t* __restrict__ depth_out, float* __restrict__ score_out) {
-  extern __shared__ uint64_t s_keys[];     // [kSortCap] hi, [kSortCap] lo, then the sort's scratch
-  uint64_t* s_hi = s_keys;
-  uint64_t* s_lo = s_keys + kSortCap;
-  uint64_t* s_bhi = s_keys + 2 * kSortCap;
-  uint64_t* s_blo = s_keys + 3 * kSortCap;
+  // The chosen set G (at most N keys, in key order) and its successor, double-buffered;
+  // this level's candidates C (at most N * K keys) and the sort's scratch.
+  extern __shared__ uint64_t s_keys[];
+  uint64_t* g_hi = s_keys;
+  uint64_t* g_lo = g_hi + kMaxTreeN;
+  uint64_t* x_hi = g_lo + kMaxTreeN;
+  uint64_t* x_lo = x_hi + kMaxTreeN;
+  uint64_t* c_hi = x_lo + kMaxTreeN;
+  uint64_t* c_lo = c_hi + kCandMax;
+  uint64_t* c_bhi = c_lo + kCandMax;
+  uint64_t* c_blo = c_bhi + kCandMax;
   __shared__ float s_lp[kMaxDepth * kMaxK];
   __shared__ int s_tok[kMaxDepth * kMaxK];
-  __shared__ int s_cnt[kMaxTreeN];
-  __shared__ int s_scan[2][kMaxTreeN];
-  __shared__ int s_nG;
+  __shared__ int s_warp[kMaxTreeN / 32];
   grid_dependency_wait();
   const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < Dmax * K; e += blockDim.x) {
     s_lp[e] = cand_logp[static_cast<size_t>(b) * Dmax * K + e];
     s_tok[e] = cand_token[static_cast<size_t>(b) * Dmax * K + e];
   }
-  // the chosen set G lives in slots [0, nG), sorted; start with the root
-  if (threadIdx.x == 0) {
-    s_hi[0] = static_cast<uint64_t>(desc_bits(0.f)) << 32;
-    s_lo[0] = 0ull;
-    s_nG = 1;
+  if (threadIdx.x == 0) {                          // G starts as the root
+    g_hi[0] = static_cast<uint64_t>(desc_bits(0.f)) << 32;
+    g_lo[0] = 0ull;
   }
+  int nG = 1;
   __syncthreads();
   for (int d = 1; d <= Dmax; ++d) {
-    const int nG = s_nG;
     const int shift = 4 * (kMaxDepth - d);
     // Level-d candidates: children of the chosen level-(d-1) nodes.  Once G holds N nodes
     // a child only matters if it beats G's last; a parent's children fall in score with
-    // their rank, so those form a prefix of its K children.
+    // their rank, so those form a prefix of its K children.  Slot f's count is found by
+    // thread f, the counts are scanned per warp and across the (at most 8) warps, and
+    // each parent writes its children into C in slot order.
     const bool full = nG == N;
-    const uint64_t thr_hi = full ? s_hi[N - 1] : ~0ull, thr_lo = full ? s_lo[N - 1] : ~0ull;
-    for (int f = threadIdx.x; f < kMaxTreeN; f += blockDim.x) {
-      int cnt = 0;
-      if (f < nG && (s_hi[f] & 0xFFFFFFFFull) == static_cast<uint64_t>(d - 1)) {
-        const float ps = from_desc_bits(static_cast<uint32_t>(s_hi[f] >> 32));
-        for (int r = 0; r < K; ++r) {
-          const float cs = __fadd_rn(ps, s_lp[(d - 1) * K + r]);
-          const uint64_t ch = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
-          const uint64_t cl = s_lo[f] | (static_cast<uint64_t>(r) << shift);
-          if (!key_less(ch, cl, thr_hi, thr_lo)) break;
-          ++cnt;
-        }
+    const uint64_t thr_hi = full ? g_hi[N - 1] : ~0ull, thr_lo = full ? g_lo[N - 1] : ~0ull;
+    const int f = threadIdx.x;
+    int cnt = 0;
+    float ps = 0.f;
+    if (f < nG && (g_hi[f] & 0xFFFFFFFFull) == static_cast<uint64_t>(d - 1)) {
+      ps = from_desc_bits(static_cast<uint32_t>(g_hi[f] >> 32));
+      for (int r = 0; r < K; ++r) {
+        const float cs = __fadd_rn(ps, s_lp[(d - 1) * K + r]);
+        const uint64_t ch = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
+        const uint64_t cl = g_lo[f] | (static_cast<uint64_t>(r) << shift);
+        if (!key_less(ch, cl, thr_hi, thr_lo)) break;
+        ++cnt;
       }
-      s_cnt[f] = cnt;
-      s_scan[0][f] = cnt;
+    }
+    int incl = cnt;
+    if (f < kMaxTreeN) {
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) s_warp[warp] = incl;
     }
     __syncthreads();
-    int src = 0;                                     // inclusive scan of the counts
-    for (int off = 1; off < kMaxTreeN; off <<= 1) {
-      for (int f = threadIdx.x; f < kMaxTreeN; f += blockDim.x)
-        s_scan[1 - src][f] = s_scan[src][f] + (f >= off ? s_scan[src][f - off] : 0);
-      src = 1 - src;
-      __syncthreads();
+    int nC = 0, base = 0;
+#pragma unroll
+    for (int w = 0; w < kMaxTreeN / 32; ++w) {
+      base += w < warp ? s_warp[w] : 0;
+      nC += s_warp[w];
     }
-    const int nC = s_scan[src][kMaxTreeN - 1];
     if (nC == 0) break;
-    for (int f = threadIdx.x; f < nG; f += blockDim.x) {
-      const int cnt = s_cnt[f];
-      if (cnt == 0) continue;
-      const int base = nG + s_scan[src][f] - cnt;
-      const float ps = from_desc_bits(static_cast<uint32_t>(s_hi[f] >> 32));
-      const uint64_t pc = s_lo[f];
+    if (cnt > 0) {
+      const int o = base + incl - cnt;
+      const uint64_t pc = g_lo[f];
       for (int r = 0; r < cnt; ++r) {
         const float cs = __fadd_rn(ps, s_lp[(d - 1) * K + r]);
-        s_hi[base + r] = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
-        s_lo[base + r] = pc | (static_cast<uint64_t>(r) << shift);
+        c_hi[o + r] = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
+        c_lo[o + r] = pc | (static_cast<uint64_t>(r) << shift);
       }
     }
-    int n = 1;
-    while (n < nG + nC) n <<= 1;
-    for (int e = nG + nC + threadIdx.x; e < n; e += blockDim.x) {
-      s_hi[e] = ~0ull;
-      s_lo[e] = ~0ull;
-    }
     __syncthreads();
-    bitonic_sort(s_hi, s_lo, s_bhi, s_blo, n);
-    // keep the best N; stop once no level-d node made it (deeper ones cannot either)
+    // The next G is the first N keys of G + C.  Keys are distinct (rank paths are), so a
+    // key's place is the number of keys below it: its index in sorted G plus those of C
+    // below it, or the other way round.  Few candidates are counted directly; many are
+    // sorted first and placed by binary search.
+    const int total = nG + nC, keep = min(N, total);
     int kept_d = 0;
-    for (int e = threadIdx.x; e < min(N, nG + nC); e += blockDim.x)
-      kept_d |= static_cast<int>((s_hi[e] & 0xFFFFFFFFull) == static_cast<uint64_t>(d));
+    if (nC <= kCountMaxC) {
+      for (int e = threadIdx.x; e < total; e += blockDim.x) {
+        const bool in_g = e < nG;
+        const uint64_t h = in_g ? g_hi[e] : c_hi[e - nG], l = in_g ? g_lo[e] : c_lo[e - nG];
+        int pos = in_g ? e : lower_bound_key(g_hi, g_lo, nG, h, l);
+        for (int j = 0; j < nC; ++j) pos += key_less(c_hi[j], c_lo[j], h, l) ? 1 : 0;
+        if (pos < keep) {
+          x_hi[pos] = h;
+          x_lo[pos] = l;
+          kept_d |= in_g ? 0 : 1;
+        }
+      }
+    } else {
+      int n = 1;
+      while (n < nC) n <<= 1;
+      for (int e = nC + threadIdx.x; e < n; e += blockDim.x) {   // pad to a power of two
+        c_hi[e] = ~0ull;
+        c_lo[e] = ~0ull;
+      }
+      __syncthreads();
+      bitonic_sort(c_hi, c_lo, c_bhi, c_blo, n);
+      for (int e = threadIdx.x; e < total; e += blockDim.x) {
+        const bool in_g = e < nG;
+        const uint64_t h = in_g ? g_hi[e] : c_hi[e - nG], l = in_g ? g_lo[e] : c_lo[e - nG];
+        const int pos = in_g ? e + lower_bound_key(c_hi, c_lo, nC, h, l)
+                             : (e - nG) + lower_bound_key(g_hi, g_lo, nG, h, l);
+        if (pos < keep) {
+          x_hi[pos] = h;
+          x_lo[pos] = l;
+          kept_d |= in_g ? 0 : 1;
+        }
+      }
+    }
     kept_d = __syncthreads_or(kept_d);
-    if (threadIdx.x == 0) s_nG = min(N, nG + nC);
-    __syncthreads();
+    uint64_t* t = g_hi; g_hi = x_hi; x_hi = t;
+    t = g_lo; g_lo = x_lo; x_lo = t;
+    nG = keep;
+    // stop once no level-d node made it (deeper ones cannot either)
     if (!kept_d) break;
   }
   // G in key order is the tree in pop order: node id = slot
-  const int nG = s_nG;
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     const size_t o = static_cast<size_t>(b) * N + i;
     if (i >= nG) {                          // lattice smaller than N (rejected on the host)
@@ -556,8 +672,8 @@ __global__ void __launch_bounds__(kTreeThreads)
       if (score_out != nullptr) score_out[o] = -INFINITY;
       continue;
     }
-    const int d = static_cast<int>(s_hi[i] & 0xFFFFFFFFull);
-    const uint64_t code = s_lo[i];
+    const int d = static_cast<int>(g_hi[i] & 0xFFFFFFFFull);
+    const uint64_t code = g_lo[i];
     int par = -1, tok = root_token != nullptr ? root_token[b] : -1;
     if (d > 0) {
       const int shift = 4 * (kMaxDepth - d);
@@ -565,12 +681,12 @@ __global__ void __launch_bounds__(kTreeThreads)
       tok = s_tok[(d - 1) * K + r];
       const uint64_t pcode = code & ~(0xFull << shift);
       for (int u = 0; u < i; ++u)
-        if (s_lo[u] == pcode && static_cast<int>(s_hi[u] & 0xFFFFFFFFull) == d - 1) { par = u; break; }
+        if (g_lo[u] == pcode && static_cast<int>(g_hi[u] & 0xFFFFFFFFull) == d - 1) { par = u; break; }
     }
     parent[o] = par;
     draft[o] = tok;
     depth_out[o] = d;
-    if (score_out != nullptr) score_out[o] = from_desc_bits(static_cast<uint32_t>(s_hi[i] >> 32));
+    if (score_out != nullptr) score_out[o] = from_desc_bits(static_cast<uint32_t>(g_hi[i] >> 32));
   }
   grid_dependents_launch();
 }
@@ -589,7 +705,6 @@ extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype
   if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
   if (B < 1 || Dmax < 1 || K < 1 || N < 1 || V < 1) return JF_ERR_INVALID_ARGUMENT;
   if (K > jf::kMaxK || Dmax > jf::kMaxDepth || N > jf::kMaxTreeN || V < K) return JF_ERR_UNSUPPORTED;
-  if (N + N * K > jf::kSortCap) return JF_ERR_UNSUPPORTED;
   // the lattice must hold N nodes: 1 + K + K^2 + ... + K^Dmax >= N
   long long lattice = 1, level = 1;
   for (int d = 1; d <= Dmax && lattice < N; ++d) {
@@ -619,16 +734,21 @@ extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype
   attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  cudaError_t e =
-      dtype == JF_DTYPE_BF16
-          ? cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<uint16_t>,
-                               static_cast<const uint16_t*>(draft_logits), V, K, parts, cand_token,
-                               cand_logp)
-          : cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<float>,
-                               static_cast<const float*>(draft_logits), V, K, parts, cand_token,
-                               cand_logp);
+  // A grid that fits in one wave at three CTAs per SM runs the register-capped kernel.
+  const bool one_wave = rows * parts <= 3LL * sms;
+  const uint16_t* lb = static_cast<const uint16_t*>(draft_logits);
+  const float* lf = static_cast<const float*>(draft_logits);
+  cudaError_t e;
+  if (dtype == JF_DTYPE_BF16)
+    e = one_wave ? cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<uint16_t, 3>, lb, V, K, parts,
+                                      cand_token, cand_logp)
+                 : cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<uint16_t, 2>, lb, V, K, parts,
+                                      cand_token, cand_logp);
+  else
+    e = cudaLaunchKernelEx(&lc, jf::draft_candidates_kernel<float, 1>, lf, V, K, parts, cand_token,
+                           cand_logp);
   if (e != cudaSuccess) return JF_ERR_CUDA;
-  constexpr size_t kTreeSmem = 4 * jf::kSortCap * sizeof(uint64_t);
+  constexpr size_t kTreeSmem = (4 * jf::kMaxTreeN + 4 * jf::kCandMax) * sizeof(uint64_t);
   {
     // Once per device; host threads calling concurrently serialise on the mutex.
     static std::mutex mu;
