@@ -314,7 +314,7 @@ jf_status jf_tree_verify_ragged(const void* logits, int32_t dtype, const int32_t
  *      root_token[b] or -1 for the root when root_token is NULL), depth and score (may be
  *      NULL), all [B][N].
  * Arguments: draft_logits bf16 or fp32 [B][Dmax][V] (dtype JF_DTYPE_*), device pointers.
- * Limits: 1 <= K <= 8, 1 <= Dmax <= 16, 1 <= N <= 256, N * (K + 1) <= 4096, V >= K, and
+ * Limits: 1 <= K <= 8, 1 <= Dmax <= 16, 1 <= N <= 256, V >= K, and
  *   the candidate lattice must hold N nodes (1 + K + ... + K^Dmax >= N); otherwise
  *   JF_ERR_UNSUPPORTED.  Logits must be finite.
  */
