@@ -100,7 +100,8 @@ struct PassState {
 // adds exp(x - M) into sum and appends every logit >= tau to the shared candidate buffer.
 // PASS 3 (only when the buffer overflowed) offers every logit to the warp's K-best list.
 // The row is read as 16-byte vectors, kUnroll per thread in flight, when it starts on a
-// 16-byte boundary; otherwise element by element.
+// 16-byte boundary (bf16 passes 1 and 2 then work on packed pairs, see bf16_vec_pass);
+// otherwise element by element.
 template <int PASS>
 __device__ __forceinline__ void take(float v, int i, bool valid, PassState& st) {
   if constexpr (PASS == 1) {
@@ -192,31 +193,31 @@ __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts,
     if constexpr (sizeof(T) == 2 && PASS != 3) {
       bf16_vec_pass<PASS>(xv, vb, nvec, st);
     } else {
-    // the warp loops while its first lane still has vectors, so all lanes step together
-    for (int w0 = vb + lane0; w0 < nvec; w0 += blockDim.x * kUnroll) {
-      const int v0 = w0 + (threadIdx.x & 31);
-      uint4 buf[kUnroll];
+      // the warp loops while its first lane still has vectors, so all lanes step together
+      for (int w0 = vb + lane0; w0 < nvec; w0 += blockDim.x * kUnroll) {
+        const int v0 = w0 + (threadIdx.x & 31);
+        uint4 buf[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * blockDim.x;
-        buf[u] = v < nvec ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
-      }
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + u * blockDim.x;
+          buf[u] = v < nvec ? __ldg(xv + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v = v0 + u * blockDim.x;
-        const bool valid = v < nvec;
-        const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + u * blockDim.x;
+          const bool valid = v < nvec;
+          const uint32_t w[4] = {buf[u].x, buf[u].y, buf[u].z, buf[u].w};
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-          float val;
-          if constexpr (sizeof(T) == 2)
-            val = __uint_as_float(((w[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu) << 16);
-          else
-            val = __uint_as_float(w[e]);
-          take<PASS>(val, v * kPer + e, valid, st);
+          for (int e = 0; e < kPer; ++e) {
+            float val;
+            if constexpr (sizeof(T) == 2)
+              val = __uint_as_float(((w[e >> 1] >> ((e & 1) * 16)) & 0xFFFFu) << 16);
+            else
+              val = __uint_as_float(w[e]);
+            take<PASS>(val, v * kPer + e, valid, st);
+          }
         }
       }
-    }
     }
     if (part == parts - 1)
       for (int b0 = nvec_all * kPer + lane0; b0 < V; b0 += blockDim.x) {
