@@ -237,9 +237,10 @@ __device__ __forceinline__ void row_pass(const T* x, int V, int part, int parts,
 }
 
 // The k-th largest (k <= kMaxK) of one value per thread of the CTA, by repeated
-// extraction: each warp takes its k largest, then warp 0 takes the k largest of those.
-// Every thread of the CTA calls it; `scratch` holds kWarps * kMaxK floats.
-__device__ float block_kth_largest(float x, int k, float* scratch) {
+// extraction: each warp takes its k largest, then warp 0 takes the k largest of those;
+// the first of them is the CTA's maximum, returned in *mx.  Every thread of the CTA calls
+// it; `scratch` holds kWarps * kMaxK floats.
+__device__ float block_kth_largest(float x, int k, float* scratch, float* mx) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   for (int r = 0; r < k; ++r) {
@@ -251,7 +252,7 @@ __device__ float block_kth_largest(float x, int k, float* scratch) {
     if (lane == 0) scratch[warp * kMaxK + r] = b;
   }
   __syncthreads();
-  float kth = -INFINITY;
+  float kth = -INFINITY, top = -INFINITY;
   if (warp == 0) {
     int head = 0;                                  // lane q < nwarps walks warp q's list
     for (int r = 0; r < k; ++r) {
@@ -261,12 +262,17 @@ __device__ float block_kth_largest(float x, int k, float* scratch) {
       for (int o = 16; o > 0; o >>= 1) b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
       const unsigned who = __ballot_sync(0xffffffffu, lane < nwarps && head < k && h == b);
       if (lane == __ffs(who) - 1) ++head;
+      if (r == 0) top = b;
       kth = b;
     }
-    if (lane == 0) scratch[0] = kth;
+    if (lane == 0) {
+      scratch[0] = kth;
+      scratch[1] = top;
+    }
   }
   __syncthreads();
   kth = scratch[0];
+  *mx = scratch[1];
   __syncthreads();
   return kth;
 }
@@ -311,16 +317,9 @@ __global__ void __launch_bounds__(kTopThreads, kMinBlocks)
   if (threadIdx.x == 0) s_ncand = 0;
   row_pass<T, 1>(x, V, part, parts, st);                      // slice maximum
   // threshold: the K-th largest thread maximum (-inf when the slice has fewer logits)
-  st.tau = block_kth_largest(st.m, K, s_red);
-  s_red[threadIdx.x] = st.m;
-  __syncthreads();
-  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) s_red[threadIdx.x] = fmaxf(s_red[threadIdx.x], s_red[threadIdx.x + w]);
-    __syncthreads();
-  }
-  const float M = s_red[0];
+  float M;
+  st.tau = block_kth_largest(st.m, K, s_red, &M);
   st.M = M;
-  __syncthreads();
   if (M != -INFINITY) row_pass<T, 2>(x, V, part, parts, st);
   __syncthreads();
   const int ncand = s_ncand;
@@ -337,12 +336,11 @@ __global__ void __launch_bounds__(kTopThreads, kMinBlocks)
     row_pass<T, 3>(x, V, part, parts, st);                    // every logit, per warp
   }
   if (lane < kMaxK) s_top[warp][lane] = st.wl;
-  s_red[threadIdx.x] = st.sum;
+  float wsum = st.sum;                             // the slice's sum: per warp, then warp 0
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane == 0) s_red[warp] = wsum;
   __syncthreads();
-  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
-    __syncthreads();
-  }
   // merge the warps' lists: warp 0 takes the K best heads, one per round
   if (warp == 0) {
     int head = 0;                                  // lane q < kWarps walks list q
@@ -363,8 +361,10 @@ __global__ void __launch_bounds__(kTopThreads, kMinBlocks)
     __syncwarp();
     if (lane < kMaxK) s_top[0][lane] = out;        // this slice's K best, in order
     if (lane == 0) {
+      float sum = 0.f;
+      for (int w = 0; w < kWarps; ++w) sum += s_red[w];
       s_slice[0] = M;
-      s_slice[1] = s_red[0];
+      s_slice[1] = sum;
     }
   }
   cluster_sync();                                // every slice's result is in place
