@@ -17,7 +17,8 @@
 // its score is not lower and its depth is smaller).  The kernel finds them level by
 // level: the level-d candidates are the children of the chosen level-(d-1) nodes (once
 // N nodes are chosen, only those that beat the last of them), and the chosen set, kept
-// sorted in shared memory, becomes the first N keys of (chosen so far + candidates): each
+// sorted in shared memory, becomes the first N keys of (chosen so far + candidates): the
+// candidates, sorted runs per parent, are merged pairwise into one sorted run, and each
 // key's place is the number of keys below it.  A node is identified by its rank path
 // packed into a 64-bit code (4 bits per level, first level in the top bits), so its
 // parent's code is its own with the last digit cleared.
@@ -38,7 +39,7 @@ constexpr int kMaxK = 8;
 constexpr int kMaxDepth = 16;
 constexpr int kMaxTreeN = 256;
 constexpr int kCandMax = kMaxTreeN * kMaxK;   // candidates of one level, at most
-constexpr int kCountMaxC = 128;          // up to this many candidates are placed by counting
+constexpr int kCountMaxC = 64;           // up to this many candidates are ranked by counting
 constexpr int kRowParts = 8;             // most CTAs (one cluster) per logit row
 constexpr int kCandCap = 1024;           // filtered candidates a CTA keeps in shared memory
 
@@ -431,95 +432,6 @@ __device__ __forceinline__ bool key_less(uint64_t ah, uint64_t al, uint64_t bh, 
   return ah < bh || (ah == bh && al < bl);
 }
 
-// One compare-exchange of bitonic sorting network stage (k, j) seen from element i: keep
-// the smaller key when i is the pair's lower index in an ascending block (or the upper
-// index in a descending one), else the larger.
-__device__ __forceinline__ void cx_keep(uint64_t& h, uint64_t& l, uint64_t ph, uint64_t pl, int i,
-                                        int k, int j) {
-  const bool keep_min = ((i & k) == 0) == ((i & j) == 0);
-  const bool p_less = key_less(ph, pl, h, l);
-  if (keep_min ? p_less : !p_less && !(ph == h && pl == l)) {
-    h = ph;
-    l = pl;
-  }
-}
-
-// Stage (k, J) for partners inside one thread (J < E): compile-time register indices.
-template <int E, int J>
-__device__ __forceinline__ void reg_stage(uint64_t (&h)[E], uint64_t (&l)[E], int t, int k) {
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    if ((e ^ J) > e) {
-      const int pe = e ^ J;
-      const bool up = ((t * E + e) & k) == 0;
-      const bool sw = up ? key_less(h[pe], l[pe], h[e], l[e]) : key_less(h[e], l[e], h[pe], l[pe]);
-      if (sw) {
-        const uint64_t th = h[e], tl = l[e];
-        h[e] = h[pe]; l[e] = l[pe];
-        h[pe] = th; l[pe] = tl;
-      }
-    }
-  }
-}
-
-// Bitonic sort of n = E * 1024 keys (or n <= 1024 with E = 1) held E per thread,
-// element i = thread * E + e.  Stages whose partner is in the same thread swap registers,
-// those in the same warp use shuffles, and only partners in other warps go through shared
-// memory (double-buffered, one barrier per stage); so a sort of 4096 keys takes 15
-// barriers instead of 78.  Input and output in hi/lo; bhi/blo is scratch of n keys.
-// Every thread of the block calls it.
-template <int E>
-__device__ __forceinline__ void bitonic_sort_e(uint64_t* hi, uint64_t* lo, uint64_t* bhi,
-                                               uint64_t* blo, int n) {
-  const int t = threadIdx.x;
-  uint64_t h[E], l[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int i = t * E + e;
-    h[e] = i < n ? hi[i] : ~0ull;
-    l[e] = i < n ? lo[i] : ~0ull;
-  }
-  int buf = 0;
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j < E) {                                   // partner in this thread
-        if (j == 1) reg_stage<E, 1>(h, l, t, k);
-        else if constexpr (E > 2) reg_stage<E, 2>(h, l, t, k);
-      } else if (j < 32 * E) {                       // partner in this warp
-        const int lm = j / E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const uint64_t ph = __shfl_xor_sync(0xffffffffu, h[e], lm);
-          const uint64_t pl = __shfl_xor_sync(0xffffffffu, l[e], lm);
-          cx_keep(h[e], l[e], ph, pl, t * E + e, k, j);
-        }
-      } else {                                       // partner in another warp
-        uint64_t* sh = buf ? bhi : hi;
-        uint64_t* sl = buf ? blo : lo;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int i = t * E + e;
-          if (i < n) { sh[i] = h[e]; sl[i] = l[e]; }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const int i = t * E + e;
-          if (i < n) cx_keep(h[e], l[e], sh[i ^ j], sl[i ^ j], i, k, j);
-        }
-        buf ^= 1;
-      }
-    }
-  }
-  __syncthreads();                                   // every shared-memory read is done
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    const int i = t * E + e;
-    if (i < n) { hi[i] = h[e]; lo[i] = l[e]; }
-  }
-  __syncthreads();
-}
-
 // Number of the first n keys of a sorted array that are below (h, l).
 __device__ __forceinline__ int lower_bound_key(const uint64_t* hi, const uint64_t* lo, int n, uint64_t h,
                                                uint64_t l) {
@@ -532,19 +444,26 @@ __device__ __forceinline__ int lower_bound_key(const uint64_t* hi, const uint64_
   return a;
 }
 
-__device__ void bitonic_sort(uint64_t* hi, uint64_t* lo, uint64_t* bhi, uint64_t* blo, int n) {
-  if (n <= kTreeThreads) bitonic_sort_e<1>(hi, lo, bhi, blo, n);
-  else if (n <= 2 * kTreeThreads) bitonic_sort_e<2>(hi, lo, bhi, blo, n);
-  else bitonic_sort_e<4>(hi, lo, bhi, blo, n);
+// Number of the first n keys of a sorted array that are at or below (h, l).
+__device__ __forceinline__ int upper_bound_key(const uint64_t* hi, const uint64_t* lo, int n, uint64_t h,
+                                               uint64_t l) {
+  int a = 0, c = n;
+  while (a < c) {
+    const int m = (a + c) >> 1;
+    if (!key_less(h, l, hi[m], lo[m])) a = m + 1;
+    else c = m;
+  }
+  return a;
 }
 
-__global__ void __launch_bounds__(kTreeThreads)
+
+__global__ void __launch_bounds__(kTreeThreads, 1)
     best_first_tree_kernel(const int32_t* __restrict__ cand_token, const float* __restrict__ cand_logp,
                            const int32_t* __restrict__ root_token, int Dmax, int K, int N,
                            int32_t* __restrict__ parent, int32_t* __restrict__ draft,
                            int32_t* __restrict__ depth_out, float* __restrict__ score_out) {
   // The chosen set G (at most N keys, in key order) and its successor, double-buffered;
-  // this level's candidates C (at most N * K keys) and the sort's scratch.
+  // this level's candidates C (at most N * kMaxK slots) and the merge's scratch.
   extern __shared__ uint64_t s_keys[];
   uint64_t* g_hi = s_keys;
   uint64_t* g_lo = g_hi + kMaxTreeN;
@@ -575,8 +494,7 @@ __global__ void __launch_bounds__(kTreeThreads)
     // Level-d candidates: children of the chosen level-(d-1) nodes.  Once G holds N nodes
     // a child only matters if it beats G's last; a parent's children fall in score with
     // their rank, so those form a prefix of its K children.  Slot f's count is found by
-    // thread f, the counts are scanned per warp and across the (at most 8) warps, and
-    // each parent writes its children into C in slot order.
+    // thread f and scanned per warp and across the (at most 8) warps.
     const bool full = nG == N;
     const uint64_t thr_hi = full ? g_hi[N - 1] : ~0ull, thr_lo = full ? g_lo[N - 1] : ~0ull;
     const int f = threadIdx.x;
@@ -592,7 +510,11 @@ __global__ void __launch_bounds__(kTreeThreads)
         ++cnt;
       }
     }
-    int incl = cnt;
+    // One scan gives both C's size (the counts) and each parent's index among the slots
+    // that have children (the flags, in the upper half).  A parent's children fall in key
+    // order with their rank, so each parent writes a sorted run of kMaxK slots, the ranks
+    // past its count padded with the largest key.
+    int incl = cnt | ((cnt > 0 ? 1 : 0) << 16);
     if (f < kMaxTreeN) {
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -602,60 +524,80 @@ __global__ void __launch_bounds__(kTreeThreads)
       if (lane == 31) s_warp[warp] = incl;
     }
     __syncthreads();
-    int nC = 0, base = 0;
+    int tot = 0, base = 0;
 #pragma unroll
     for (int w = 0; w < kMaxTreeN / 32; ++w) {
       base += w < warp ? s_warp[w] : 0;
-      nC += s_warp[w];
+      tot += s_warp[w];
     }
+    const int nC = tot & 0xFFFF, npar = tot >> 16;
     if (nC == 0) break;
+    const bool few = nC <= kCountMaxC;               // few candidates: C stays unsorted
+    int runs = 1;
+    while (runs < npar) runs <<= 1;
+    const int nS = few ? nC : runs * kMaxK;          // candidate slots
     if (cnt > 0) {
-      const int o = base + incl - cnt;
+      const int o = few ? ((base + incl) & 0xFFFF) - cnt : (((base + incl) >> 16) - 1) * kMaxK;
       const uint64_t pc = g_lo[f];
-      for (int r = 0; r < cnt; ++r) {
-        const float cs = __fadd_rn(ps, s_lp[(d - 1) * K + r]);
-        c_hi[o + r] = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
-        c_lo[o + r] = pc | (static_cast<uint64_t>(r) << shift);
+      for (int r = 0; r < (few ? cnt : kMaxK); ++r) {
+        uint64_t h = ~0ull, l = ~0ull;
+        if (r < cnt) {
+          const float cs = __fadd_rn(ps, s_lp[(d - 1) * K + r]);
+          h = (static_cast<uint64_t>(desc_bits(cs)) << 32) | static_cast<uint64_t>(d);
+          l = pc | (static_cast<uint64_t>(r) << shift);
+        }
+        c_hi[o + r] = h;
+        c_lo[o + r] = l;
       }
+    }
+    for (int e = (few ? nS : npar * kMaxK) + threadIdx.x; e < nS; e += blockDim.x) {   // empty runs
+      c_hi[e] = ~0ull;
+      c_lo[e] = ~0ull;
     }
     __syncthreads();
-    // The next G is the first N keys of G + C.  Keys are distinct (rank paths are), so a
-    // key's place is the number of keys below it: its index in sorted G plus those of C
-    // below it, or the other way round.  Few candidates are counted directly; many are
-    // sorted first and placed by binary search.
-    const int total = nG + nC, keep = min(N, total);
-    int kept_d = 0;
-    if (nC <= kCountMaxC) {
-      for (int e = threadIdx.x; e < total; e += blockDim.x) {
-        const bool in_g = e < nG;
-        const uint64_t h = in_g ? g_hi[e] : c_hi[e - nG], l = in_g ? g_lo[e] : c_lo[e - nG];
-        int pos = in_g ? e : lower_bound_key(g_hi, g_lo, nG, h, l);
-        for (int j = 0; j < nC; ++j) pos += key_less(c_hi[j], c_lo[j], h, l) ? 1 : 0;
-        if (pos < keep) {
-          x_hi[pos] = h;
-          x_lo[pos] = l;
-          kept_d |= in_g ? 0 : 1;
-        }
-      }
-    } else {
-      int n = 1;
-      while (n < nC) n <<= 1;
-      for (int e = nC + threadIdx.x; e < n; e += blockDim.x) {   // pad to a power of two
-        c_hi[e] = ~0ull;
-        c_lo[e] = ~0ull;
+    // Merge the runs pairwise until C is one sorted run: a key's place in the merged pair is
+    // its index in its own run plus the keys of the other run below it (at or below it, for
+    // the second run: the padding keys are equal and keep their order).  Real keys come
+    // first; they are distinct.
+    int src = 0;                                     // the merge's current buffer
+    for (int L = kMaxK; !few && L < nS; L <<= 1, src ^= 1) {
+      const uint64_t* sh = src ? c_bhi : c_hi;
+      const uint64_t* sl = src ? c_blo : c_lo;
+      uint64_t* dh = src ? c_hi : c_bhi;
+      uint64_t* dl = src ? c_lo : c_blo;
+      for (int i = threadIdx.x; i < nS; i += blockDim.x) {
+        const int p0 = i & ~(2 * L - 1);
+        const bool in_a = (i & L) == 0;
+        const uint64_t h = sh[i], l = sl[i];
+        const int at = in_a ? (i - p0) + lower_bound_key(sh + p0 + L, sl + p0 + L, L, h, l)
+                            : (i - p0 - L) + upper_bound_key(sh + p0, sl + p0, L, h, l);
+        dh[p0 + at] = h;
+        dl[p0 + at] = l;
       }
       __syncthreads();
-      bitonic_sort(c_hi, c_lo, c_bhi, c_blo, n);
-      for (int e = threadIdx.x; e < total; e += blockDim.x) {
-        const bool in_g = e < nG;
-        const uint64_t h = in_g ? g_hi[e] : c_hi[e - nG], l = in_g ? g_lo[e] : c_lo[e - nG];
-        const int pos = in_g ? e + lower_bound_key(c_hi, c_lo, nC, h, l)
-                             : (e - nG) + lower_bound_key(g_hi, g_lo, nG, h, l);
-        if (pos < keep) {
-          x_hi[pos] = h;
-          x_lo[pos] = l;
-          kept_d |= in_g ? 0 : 1;
-        }
+    }
+    const uint64_t* sh = src ? c_bhi : c_hi;         // C, sorted unless few
+    const uint64_t* sl = src ? c_blo : c_lo;
+    // The next G is the first N keys of G + C: a key's place is the number of keys below
+    // it, its index in its own sorted set plus the other set's keys below it (counted
+    // one by one when C is small and unsorted).
+    const int total = nG + nC, keep = min(N, total);
+    int kept_d = 0;
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+      const bool in_g = e < nG;
+      const uint64_t h = in_g ? g_hi[e] : sh[e - nG], l = in_g ? g_lo[e] : sl[e - nG];
+      int pos;
+      if (few) {                                     // unsorted C: count its keys below
+        pos = in_g ? e : lower_bound_key(g_hi, g_lo, nG, h, l);
+        for (int j = 0; j < nC; ++j) pos += key_less(sh[j], sl[j], h, l) ? 1 : 0;
+      } else {
+        pos = in_g ? e + lower_bound_key(sh, sl, nC, h, l)
+                   : (e - nG) + lower_bound_key(g_hi, g_lo, nG, h, l);
+      }
+      if (pos < keep) {
+        x_hi[pos] = h;
+        x_lo[pos] = l;
+        kept_d |= in_g ? 0 : 1;
       }
     }
     kept_d = __syncthreads_or(kept_d);
