@@ -158,11 +158,31 @@ def test_equal_logits_and_scores_tie_break(jf):
     check(jf, x, "f32", 6, 150)
 
 
-@pytest.mark.parametrize("B,N", [(20, 64), (8, 256)])
+@pytest.mark.parametrize("V", [704, 700])
+def test_equal_bf16_logits_tie_break(jf, V):
+    """The same integer logits as bf16: rows of 704 logits start on 16-byte boundaries and
+    take the packed passes (whole vectors tie at the threshold), rows of 700 do not."""
+    rng = np.random.default_rng(18)
+    x = rng.integers(-2, 3, size=(3, 6, V)).astype(np.float32)
+    check(jf, wl.to_bf16_bits(x), "bf16", 6, 150)
+
+
+@pytest.mark.parametrize("B,Dmax,V,K,N,dtype", [(2, 6, 3000, 5, 200, "bf16"), (1, 10, 2000, 3, 256, "f32"),
+                                                (3, 16, 8192, 7, 256, "bf16")])
+def test_levels_with_many_candidates(jf, B, Dmax, V, K, N, dtype):
+    """Levels with more than 64 candidates from parent counts that are not powers of two
+    (25 parents of 5 children, 27 of 3, 49 of 7): their children are merged as sorted runs
+    before the chosen set is updated."""
+    check(jf, wl.draft_logits(B, Dmax, V, sigma=1.0, dtype=dtype, seed=30 + K), dtype, K, N, min_pinned=0.8)
+
+
+@pytest.mark.parametrize("B,N", [(20, 64), (8, 256), (32, 64)])
 def test_many_rows_bf16(jf, B, N):
-    """16 depths for 20 (8) sequences: 320 (128) logit rows, so rows run one CTA each
-    (three CTAs per row) instead of eight-CTA clusters."""
-    check(jf, wl.draft_logits(B, 16, 151936, seed=9 + B), "bf16", 8, N, min_pinned=0.8)
+    """16 depths for 20 (8, 32) sequences: 320 (128, 512) logit rows, so rows run one CTA
+    each (three CTAs per row) instead of eight-CTA clusters; 512 rows are more than one
+    wave at three CTAs per SM and take the two-per-SM instantiation."""
+    V = 151936 if B < 32 else 8192
+    check(jf, wl.draft_logits(B, 16, V, seed=9 + B), "bf16", 8, N, min_pinned=0.8)
 
 
 @pytest.mark.parametrize("B,Dmax,V", [(2, 4, 20000), (20, 16, 3000)])

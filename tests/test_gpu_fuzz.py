@@ -131,7 +131,7 @@ def test_verify_random_shapes(jf, case):
 
 # ----------------------------------------------------------------------------- draft tree
 
-N_DRAFT = 12
+N_DRAFT = 24
 
 
 @pytest.mark.parametrize("case", range(N_DRAFT))
