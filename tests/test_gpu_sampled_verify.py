@@ -98,6 +98,26 @@ def test_small_vocab_mixed_decisions(jf, T):
     assert racc.max() >= 2
 
 
+@pytest.mark.parametrize("V,dtype", [(1001, "bf16"), (8195, "f32"), (20000, "bf16"), (16384, "f32")])
+def test_vocab_shapes_mixed_decisions(jf, V, dtype):
+    """Vocabularies of one to three 8192-token chunks, with a ragged last chunk and with
+    rows that do not start on a 16-byte boundary (1001 bf16, 8195 fp32): children drawn
+    from their parent's target distribution, so acceptances, rejections and residual bonus
+    draws across the chunks all occur."""
+    rng = np.random.default_rng(V)
+    B, N, T = 6, 24, 1.0
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - 4), i) for i in range(1, N)])
+                       for _ in range(B)]).astype(np.int32)
+    x = (rng.standard_normal((B, N, V)) * 2.0).astype(np.float32)
+    logits = wl.to_bf16_bits(x) if dtype == "bf16" else x
+    rows = osv._rows_f64(logits, dtype)
+    draft = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for c in range(1, N):
+            draft[b, c] = rng.choice(V, p=osv.target_probs(rows[b, parent[b, c]], T))
+    check(jf, logits, dtype, draft, parent, T, seed=V)
+
+
 @pytest.mark.parametrize("name", ["c1_tiny_random16", "c3_qwen3_8b_tree256"])
 def test_workloads_forced_drafts(jf, name):
     """Workload logits with half the children's tokens planted as their parent's maximum

@@ -689,28 +689,6 @@ struct KahanSum {
   }
 };
 
-__device__ __forceinline__ float block_max_f32(float v, float* s_red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = -INFINITY;
-  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) r = fmaxf(r, s_red[w]);
-  return r;
-}
-
-__device__ __forceinline__ double block_sum_f64(double v, double* s_red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  double r = 0.0;
-  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) r += s_red[w];
-  return r;
-}
-
 // Calls f(value) for every element of [s, e) of `base` that this thread owns, with 16-byte
 // loads for the aligned body (the argmax kernel's split into head, body and tail).
 template <typename T, typename F>
@@ -883,24 +861,26 @@ __global__ void __launch_bounds__(kSampleThreads)
                         const float* __restrict__ bonus_uniform, float temperature, int N,
                         long long V, int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                         int32_t* __restrict__ bonus, int32_t* dev_err) {
-  extern __shared__ int32_t smw[];
-  int32_t* s_par = smw;                 // [N] parent (malformed -> -1)
+  extern __shared__ __align__(16) int32_t smw[];
+  T* s_cv = reinterpret_cast<T*>(smw);  // [kSampleChunk] the bonus chunk's logits
+  int32_t* s_par = smw + kSampleChunk * sizeof(T) / sizeof(int32_t);   // [N] parent (malformed -> -1)
   int32_t* s_draft = s_par + N;         // [N]
   int32_t* s_kids = s_draft + N;        // [N] children of the current node, id order
   int32_t* s_path = s_kids + N;         // [N]
   float* s_lg = reinterpret_cast<float*>(s_path + N);                    // [N] children's logits
-  int32_t* s_rej = reinterpret_cast<int32_t*>(s_lg + N);                  // [N] rejected tokens
+  float* s_uni = s_lg + N;              // [N] the children's uniforms
+  int32_t* s_rej = reinterpret_cast<int32_t*>(s_uni + N);                 // [N] rejected tokens
   double* s_rejp = reinterpret_cast<double*>(                             // [N] their probabilities
       (reinterpret_cast<uintptr_t>(s_rej + N) + 7) & ~static_cast<uintptr_t>(7));
   double* s_pk = s_rejp + N;            // [N] target probabilities of the children's tokens
   __shared__ double s_redd[kSampleThreads / 32];
-  __shared__ float s_redf[kSampleThreads / 32];
   __shared__ int s_redi[kSampleThreads / 32];
   __shared__ int s_next, s_nrej, s_chunk, s_y;
-  __shared__ double s_rejmass, s_base;
+  __shared__ double s_rejmass, s_base, s_M, s_Z;
 
   grid_dependency_wait();
   const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t rb = static_cast<size_t>(b) * N;
   const double Td = temperature;
   const float inv_t = 1.f / temperature;
@@ -930,23 +910,34 @@ __global__ void __launch_bounds__(kSampleThreads)
   for (;;) {
     const T* row = logits + (rb + u) * V;
     const float2* st = stats + (rb + u) * chunks;
-    // M and Z of row u from the chunk statistics (fp64)
-    float mloc = -INFINITY;
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x) mloc = fmaxf(mloc, st[c].x);
-    M = block_max_f32(mloc, s_redf);
-    // fp64 sums of fp32 exponentials of fp64 arguments: exp's ~1e-7 relative error is far
+    // M and Z of row u from the chunk statistics (fp64), in warp 0 (a row has few chunks):
+    // fp64 sums of fp32 exponentials of fp64 arguments; exp's ~1e-7 relative error is far
     // below the 1e-5 margin the decisions are held to, and fp64 exp / division are slow on
     // this GPU (one division per node: the probabilities multiply by 1 / Z).
-    double zloc = 0.0;
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x)
-      zloc += static_cast<double>(st[c].y) * expf(static_cast<float>((static_cast<double>(st[c].x) - M) * invTd));
-    Z = block_sum_f64(zloc, s_redd);
-    invZ = 1.0 / Z;
-    // children of u in id order, and their logits
+    if (warp == 0) {
+      float mloc = -INFINITY;
+      for (int c = lane; c < chunks; c += 32) mloc = fmaxf(mloc, st[c].x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+      double zloc = 0.0;
+      for (int c = lane; c < chunks; c += 32)
+        zloc += static_cast<double>(st[c].y) *
+                expf(static_cast<float>((static_cast<double>(st[c].x) - mloc) * invTd));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) zloc += __shfl_xor_sync(0xffffffffu, zloc, o);
+      if (lane == 0) {
+        s_M = mloc;
+        s_Z = zloc;
+      }
+    }
+    // children of u in id order, and their logits (the scan's barriers publish M and Z)
     int cnt = 0;
     for (int c = c_lo; c < c_hi; ++c) cnt += (s_par[c] == u) ? 1 : 0;
     int nk = 0;
     int off = block_excl_scan(cnt, s_redi, &nk);
+    M = s_M;
+    Z = s_Z;
+    invZ = 1.0 / Z;
     for (int c = c_lo; c < c_hi; ++c)
       if (s_par[c] == u) s_kids[off++] = c;
     __syncthreads();
@@ -956,6 +947,7 @@ __global__ void __launch_bounds__(kSampleThreads)
       const int x = s_draft[s_kids[k]];
       const float lg = x >= 0 ? to_f<T>(row[x]) : -INFINITY;
       s_lg[k] = lg;
+      s_uni[k] = uniform[rb + s_kids[k]];
       s_pk[k] = x >= 0 ? static_cast<double>(expf(static_cast<float>((static_cast<double>(lg) - M) * invTd))) * invZ
                        : 0.0;
     }
@@ -969,7 +961,7 @@ __global__ void __launch_bounds__(kSampleThreads)
         bool seen = x < 0;
         for (int r = 0; r < nrej && !seen; ++r) seen = s_rej[r] == x;
         const double p = seen ? 0.0 : s_pk[k];
-        if (static_cast<double>(uniform[rb + c]) * (1.0 - rej) < p) {
+        if (static_cast<double>(s_uni[k]) * (1.0 - rej) < p) {
           next = c;
           break;
         }
@@ -995,12 +987,12 @@ __global__ void __launch_bounds__(kSampleThreads)
   const double target = static_cast<double>(bonus_uniform[b]) * (1.0 - s_rejmass);
   const T* row = logits + (rb + u) * V;
   const float2* st = stats + (rb + u) * chunks;
-  // The chunk holding the threshold: residual chunk masses (the chunk's mass minus its
-  // rejected tokens' probabilities), each thread over a contiguous range of chunks, an fp64
-  // block scan over the ranges, then the thread whose range crosses the threshold walks it.
-  {
-    const int cpt = (chunks + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
-    const int q0 = min(chunks, static_cast<int>(threadIdx.x) * cpt), q1 = min(chunks, q0 + cpt);
+  // The chunk holding the threshold, in warp 0: residual chunk masses (the chunk's mass
+  // minus its rejected tokens' probabilities) 32 chunks at a time, an fp64 warp scan, and
+  // the first chunk c with (mass of the chunks before c) + w_c > target.  Masses can be a
+  // rounding error below zero; with no crossing at all (rounding past the end) the last
+  // chunk is taken, after the mass of all the others.
+  if (warp == 0) {
     auto chunk_mass = [&](int c) -> double {
       const long long s0 = static_cast<long long>(c) * chunk_len, e0 = min(V, s0 + chunk_len);
       double w = static_cast<double>(st[c].y) *
@@ -1009,54 +1001,70 @@ __global__ void __launch_bounds__(kSampleThreads)
         if (s_rej[r] >= s0 && s_rej[r] < e0) w -= s_rejp[r];
       return w;
     };
-    double mine_w = 0.0;
-    for (int c = q0; c < q1; ++c) mine_w += chunk_mass(c);
-    if (threadIdx.x == 0) s_chunk = 0x7fffffff;
-    double all_w = 0.0;
-    const double before_w = block_excl_scan_f64(mine_w, s_redd, &all_w);
-    // the first chunk c with (mass of the chunks before c) + w_c > target; masses can be a
-    // rounding error below zero, so every range looks for its own first crossing
-    int my_c = -1;
-    double my_base = 0.0;
-    {
-      double cum = before_w;
-      for (int c = q0; c < q1; ++c) {
-        const double w = chunk_mass(c);
-        if (cum + w > target) { my_c = c; my_base = cum; break; }
-        cum += w;
+    double carry = 0.0, fbase = 0.0;
+    int found = -1;
+    for (int c0 = 0; c0 < chunks; c0 += 32) {
+      const int c = c0 + lane;
+      const double w = c < chunks ? chunk_mass(c) : 0.0;
+      double incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
+      const unsigned cross = __ballot_sync(0xffffffffu, c < chunks && carry + incl > target);
+      if (cross != 0u) {
+        const int L = __ffs(cross) - 1;
+        found = c0 + L;
+        fbase = carry + __shfl_sync(0xffffffffu, incl - w, L);
+        break;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (my_c >= 0) atomicMin(&s_chunk, my_c);
-    __syncthreads();
-    const bool none = s_chunk == 0x7fffffff;
-    if (!none && my_c == s_chunk) s_base = my_base;
-    __syncthreads();
-    if (none && q0 <= chunks - 1 && chunks - 1 < q1) {
-      // rounding past the last chunk: the last one, after the mass of all the others
-      double cum = before_w;
-      for (int c = q0; c < chunks - 1; ++c) cum += chunk_mass(c);
-      s_chunk = chunks - 1;
-      s_base = cum;
+    if (found < 0) {
+      found = chunks - 1;
+      fbase = carry - chunk_mass(chunks - 1);
     }
-    if (threadIdx.x == 0) s_y = -1;
-    __syncthreads();
+    if (lane == 0) {
+      s_chunk = found;
+      s_base = fbase;
+      s_y = -1;
+    }
   }
-  // The chunk's logits, 32 per thread in token order, all loads in flight together.
+  __syncthreads();
+  // The chunk's logits are staged in shared memory by coalesced loads (16-byte vectors
+  // when the chunk starts on a 16-byte boundary); then each thread takes 32 in token order.
   constexpr int kSeg = kSampleChunk / kSampleThreads;
   const long long cs0 = static_cast<long long>(s_chunk) * chunk_len;
   const long long ce0 = min(V, cs0 + chunk_len);
+  const int clen = static_cast<int>(ce0 - cs0);
+  {
+    constexpr int kVec = 16 / sizeof(T);
+    const T* src = row + cs0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0u) {
+      const int nv = clen / kVec;
+      for (int v = threadIdx.x; v < nv; v += blockDim.x)
+        reinterpret_cast<uint4*>(s_cv)[v] = __ldcs(reinterpret_cast<const uint4*>(src) + v);
+      for (int e = nv * kVec + threadIdx.x; e < clen; e += blockDim.x) s_cv[e] = src[e];
+    } else {
+      for (int e = threadIdx.x; e < clen; e += blockDim.x) s_cv[e] = src[e];
+    }
+  }
+  __syncthreads();
   const long long t0 = cs0 + static_cast<long long>(threadIdx.x) * kSeg;
   float ev[kSeg];
   {
-    float lv[kSeg];
-#pragma unroll
-    for (int e = 0; e < kSeg; ++e) lv[e] = (t0 + e < ce0) ? to_f<T>(row[t0 + e]) : 0.f;
+    uint32_t rejm = 0u;                     // this thread's rejected tokens, one bit each
+    for (int r = 0; r < nrej; ++r) {
+      const long long d = static_cast<long long>(s_rej[r]) - t0;
+      if (d >= 0 && d < kSeg) rejm |= 1u << d;
+    }
     const float Mf = static_cast<float>(M);
+    const int e0 = static_cast<int>(threadIdx.x) * kSeg;
 #pragma unroll
     for (int e = 0; e < kSeg; ++e) {        // exp((l - M) / T) of live tokens, else 0
-      bool live = t0 + e < ce0;
-      for (int r = 0; r < nrej && live; ++r) live = s_rej[r] != t0 + e;
-      ev[e] = live ? expf((lv[e] - Mf) * inv_t) : 0.f;
+      const bool live = e0 + e < clen && !((rejm >> e) & 1u);
+      ev[e] = live ? expf((to_f<T>(s_cv[e0 + e]) - Mf) * inv_t) : 0.f;
     }
   }
   KahanSum ks;
@@ -1146,8 +1154,10 @@ extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, c
                            dim3(32 * warps), 0, s, static_cast<const float*>(logits), Vl,
                            total, p.chunks, p.chunk_len, inv_t, stats);
   if (ea != cudaSuccess) return JF_ERR_CUDA;
-  const size_t smem = static_cast<size_t>(N) * (6 * sizeof(int32_t) + 2 * sizeof(double)) + 16;
   auto walk = [&](auto kern, const auto* lg) -> cudaError_t {
+    // the bonus chunk's logits, then 7 int/float and 2 double arrays of N (+ alignment)
+    const size_t smem = jf::kSampleChunk * sizeof(*lg) +
+                        static_cast<size_t>(N) * (7 * sizeof(int32_t) + 2 * sizeof(double)) + 16;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess)
