@@ -672,6 +672,7 @@ namespace jf {
 namespace {
 
 constexpr int kSampleThreads = 256;
+constexpr int kPreStats = 64;             // trees up to this size get every row's statistics first
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -854,7 +855,7 @@ __device__ __forceinline__ double block_excl_scan_f64(double v, double* s_red, d
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kSampleThreads)
+__global__ void __launch_bounds__(kSampleThreads, 1)
     sampled_walk_kernel(const T* __restrict__ logits, const float2* __restrict__ stats, int chunks,
                         int chunk_len, const int32_t* __restrict__ draft,
                         const int32_t* __restrict__ parent, const float* __restrict__ uniform,
@@ -867,16 +868,19 @@ __global__ void __launch_bounds__(kSampleThreads)
   int32_t* s_draft = s_par + N;         // [N]
   int32_t* s_kids = s_draft + N;        // [N] children of the current node, id order
   int32_t* s_path = s_kids + N;         // [N]
-  float* s_lg = reinterpret_cast<float*>(s_path + N);                    // [N] children's logits
-  float* s_uni = s_lg + N;              // [N] the children's uniforms
-  int32_t* s_rej = reinterpret_cast<int32_t*>(s_uni + N);                 // [N] rejected tokens
+  float* s_uni = reinterpret_cast<float*>(s_path + N);                   // [N] the children's uniforms
+  float* s_tlg = s_uni + N;             // [N] node c's token's logit in its parent's row
+  int32_t* s_rej = reinterpret_cast<int32_t*>(s_tlg + N);                 // [N] rejected tokens
   double* s_rejp = reinterpret_cast<double*>(                             // [N] their probabilities
       (reinterpret_cast<uintptr_t>(s_rej + N) + 7) & ~static_cast<uintptr_t>(7));
   double* s_pk = s_rejp + N;            // [N] target probabilities of the children's tokens
+  __shared__ float s_aM[kPreStats];     // small trees: every row's maximum and normaliser
+  __shared__ double s_aZ[kPreStats];
   __shared__ double s_redd[kSampleThreads / 32];
   __shared__ int s_redi[kSampleThreads / 32];
   __shared__ int s_next, s_nrej, s_chunk, s_y;
-  __shared__ double s_rejmass, s_base, s_M, s_Z;
+  __shared__ double s_rejmass, s_base, s_uZ;
+  __shared__ float s_uM;
 
   grid_dependency_wait();
   const int b = blockIdx.x;
@@ -895,6 +899,12 @@ __global__ void __launch_bounds__(kSampleThreads)
     s_draft[i] = (d >= 0 && d < V) ? d : -1;
   }
   bad_parent = __syncthreads_or(bad_parent);
+  // every node's token logit in its parent's row, all requested at once (a walk step then
+  // reads its children's from shared memory)
+  for (int c = threadIdx.x; c < N; c += blockDim.x) {
+    const int p = s_par[c], x = s_draft[c];
+    s_tlg[c] = (p >= 0 && x >= 0) ? to_f<T>(logits[(rb + p) * V + x]) : -INFINITY;
+  }
   bad_token = __syncthreads_or(bad_token);
   if (threadIdx.x == 0) {
     if (bad_parent) report(dev_err, JF_DEVERR_BAD_PARENT);
@@ -907,37 +917,51 @@ __global__ void __launch_bounds__(kSampleThreads)
   int u = 0, n = 0;
   double M = 0.0, Z = 1.0, invZ = 1.0;
   const double invTd = 1.0 / Td;
-  for (;;) {
-    const T* row = logits + (rb + u) * V;
-    const float2* st = stats + (rb + u) * chunks;
-    // M and Z of row u from the chunk statistics (fp64), in warp 0 (a row has few chunks):
-    // fp64 sums of fp32 exponentials of fp64 arguments; exp's ~1e-7 relative error is far
-    // below the 1e-5 margin the decisions are held to, and fp64 exp / division are slow on
-    // this GPU (one division per node: the probabilities multiply by 1 / Z).
-    if (warp == 0) {
-      float mloc = -INFINITY;
-      for (int c = lane; c < chunks; c += 32) mloc = fmaxf(mloc, st[c].x);
+  // M and Z of a row from its chunk statistics (fp64), by one warp (a row has a few dozen
+  // chunks): fp64 sums of fp32 exponentials of fp64 arguments; exp's ~1e-7 relative error is
+  // far below the 1e-5 margin the decisions are held to, and fp64 exp / division are slow
+  // on this GPU (one division per node: the probabilities multiply by 1 / Z).
+  auto row_stats = [&](int node, float* m_out, double* z_out) {
+    const float2* st = stats + (rb + node) * chunks;
+    float mloc = -INFINITY;
+    for (int c = lane; c < chunks; c += 32) mloc = fmaxf(mloc, st[c].x);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-      double zloc = 0.0;
-      for (int c = lane; c < chunks; c += 32)
-        zloc += static_cast<double>(st[c].y) *
-                expf(static_cast<float>((static_cast<double>(st[c].x) - mloc) * invTd));
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    double zloc = 0.0;
+    for (int c = lane; c < chunks; c += 32)
+      zloc += static_cast<double>(st[c].y) *
+              expf(static_cast<float>((static_cast<double>(st[c].x) - mloc) * invTd));
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) zloc += __shfl_xor_sync(0xffffffffu, zloc, o);
-      if (lane == 0) {
-        s_M = mloc;
-        s_Z = zloc;
-      }
+    for (int o = 16; o > 0; o >>= 1) zloc += __shfl_xor_sync(0xffffffffu, zloc, o);
+    if (lane == 0) {
+      *m_out = mloc;
+      *z_out = zloc;
     }
-    // children of u in id order, and their logits (the scan's barriers publish M and Z)
+  };
+  // Small trees: every row's M and Z up front, one warp per row, so a walk step waits on
+  // no memory; larger ones find row u's when the walk reaches it.
+  const bool all_stats = N <= kPreStats;
+  if (all_stats)
+    for (int k = warp; k < N; k += static_cast<int>(blockDim.x >> 5)) row_stats(k, &s_aM[k], &s_aZ[k]);
+  __syncthreads();
+  for (;;) {
+    if (all_stats) {
+      if (threadIdx.x == 0) {
+        s_uM = s_aM[u];
+        s_uZ = s_aZ[u];
+      }
+    } else if (warp == 0) {
+      row_stats(u, &s_uM, &s_uZ);
+    }
+    // children of u in id order (the scan's barriers publish M and Z)
     int cnt = 0;
     for (int c = c_lo; c < c_hi; ++c) cnt += (s_par[c] == u) ? 1 : 0;
     int nk = 0;
     int off = block_excl_scan(cnt, s_redi, &nk);
-    M = s_M;
-    Z = s_Z;
+    M = s_uM;
+    Z = s_uZ;
     invZ = 1.0 / Z;
+    __syncthreads();                               // every thread has read M and Z
     for (int c = c_lo; c < c_hi; ++c)
       if (s_par[c] == u) s_kids[off++] = c;
     __syncthreads();
@@ -945,8 +969,7 @@ __global__ void __launch_bounds__(kSampleThreads)
     // (fp64 is slow on this GPU: the ordered decisions below only read them)
     for (int k = threadIdx.x; k < nk; k += blockDim.x) {
       const int x = s_draft[s_kids[k]];
-      const float lg = x >= 0 ? to_f<T>(row[x]) : -INFINITY;
-      s_lg[k] = lg;
+      const float lg = s_tlg[s_kids[k]];
       s_uni[k] = uniform[rb + s_kids[k]];
       s_pk[k] = x >= 0 ? static_cast<double>(expf(static_cast<float>((static_cast<double>(lg) - M) * invTd))) * invZ
                        : 0.0;
@@ -1059,12 +1082,15 @@ __global__ void __launch_bounds__(kSampleThreads)
       const long long d = static_cast<long long>(s_rej[r]) - t0;
       if (d >= 0 && d < kSeg) rejm |= 1u << d;
     }
+    // exp((l - M) / T) of live tokens as 2^((l - M) log2(e) / T), else 0 (ex2.approx: ~2e-7
+    // relative, inside the 1e-6 the bonus draw is held to)
     const float Mf = static_cast<float>(M);
+    const float k2 = inv_t * 1.4426950408889634f;
     const int e0 = static_cast<int>(threadIdx.x) * kSeg;
 #pragma unroll
-    for (int e = 0; e < kSeg; ++e) {        // exp((l - M) / T) of live tokens, else 0
+    for (int e = 0; e < kSeg; ++e) {
       const bool live = e0 + e < clen && !((rejm >> e) & 1u);
-      ev[e] = live ? expf((to_f<T>(s_cv[e0 + e]) - Mf) * inv_t) : 0.f;
+      ev[e] = live ? fast_exp2((to_f<T>(s_cv[e0 + e]) - Mf) * k2) : 0.f;
     }
   }
   KahanSum ks;
@@ -1074,13 +1100,17 @@ __global__ void __launch_bounds__(kSampleThreads)
   double all = 0.0;
   const double before = s_base + block_excl_scan_f64(mine, s_redd, &all);
   if (mine > 0.0 && before <= target && target < before + mine) {
-    double cum = before;
+    // the crossing inside this thread's tokens, in fp32 and in the unnormalised units of
+    // ev: the threshold's offset into the segment times Z (32 fp32 terms round to ~2e-6 of
+    // the segment's own small mass)
+    const float need = static_cast<float>((target - before) * Z);
+    float cum = 0.f;
     int y = -1, last = -1;
 #pragma unroll
     for (int e = 0; e < kSeg; ++e) {
       if (ev[e] > 0.f) last = e;
-      cum += static_cast<double>(ev[e]) * invZ;
-      if (y < 0 && cum > target) y = e;
+      cum += ev[e];
+      if (y < 0 && cum > need) y = e;
     }
     s_y = static_cast<int>(t0) + (y >= 0 ? y : last);
   }
