@@ -118,6 +118,23 @@ def test_vocab_shapes_mixed_decisions(jf, V, dtype):
     check(jf, logits, dtype, draft, parent, T, seed=V)
 
 
+@pytest.mark.parametrize("dtype,V", [("f32", 1001), ("bf16", 1000)])
+def test_largest_trees(jf, dtype, V):
+    """4096 nodes (the most a call takes): the walk's shared memory is at its largest."""
+    rng = np.random.default_rng(V)
+    B, N, T = 2, 4096, 1.0
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - 6), i) for i in range(1, N)])
+                       for _ in range(B)]).astype(np.int32)
+    x = (rng.standard_normal((B, N, V)) * 2.0).astype(np.float32)
+    logits = wl.to_bf16_bits(x) if dtype == "bf16" else x
+    rows = osv._rows_f64(logits, dtype)
+    draft = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for c in range(1, N):
+            draft[b, c] = rng.choice(V, p=osv.target_probs(rows[b, parent[b, c]], T))
+    check(jf, logits, dtype, draft, parent, T, seed=V)
+
+
 @pytest.mark.parametrize("name", ["c1_tiny_random16", "c3_qwen3_8b_tree256"])
 def test_workloads_forced_drafts(jf, name):
     """Workload logits with half the children's tokens planted as their parent's maximum
