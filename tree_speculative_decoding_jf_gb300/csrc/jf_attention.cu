@@ -1878,11 +1878,11 @@ bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms
   if (sms <= 0) sms = 148;
   // Time model: waves * (tiles per split + prologue/epilogue) * max(tensor time of a key
   // tile, its share of HBM bandwidth), plus, for workspace splits, writing and re-reading
-  // the partials and one more launch.  Cluster splits (2..8 CTAs merging through DSMEM)
+  // the partials (at L2 speed while they fit in a third of it) and one more launch.  Cluster splits (2..8 CTAs merging through DSMEM)
   // pay no merge traffic but pack fewer CTAs per wave.
   const double hbm_per_tile = 2.0 * kKeyTile * D * 2;          // K + V bytes per key tile
   const double flops_per_tile = 4.0 * kRowTile * kKeyTile * D;  // QK^T + PV per row tile
-  const double per_sm_flops = 1.9e15 / sms, hbm = 6.5e12;
+  const double per_sm_flops = 1.9e15 / sms, hbm = 6.5e12, l2bw = 20e12;
   auto t_tile = [&](double active) {
     return std::max(pl->NT * flops_per_tile / per_sm_flops, hbm_per_tile * active / hbm);
   };
@@ -1896,8 +1896,9 @@ bool plan_attention(int B, int N, int Hq, int Hkv, int D, int max_pages, int sms
     const long long waves = (ctas + sms - 1) / sms;
     double est = waves * (chunk + 1.5) * t_tile(static_cast<double>(std::min<long long>(ctas, sms)));
     if (s > 1) {
+      // the partials are written and read back once; up to a third of L2 they stay there
       const double part = static_cast<double>(B) * Hq * N * s * (D + 1) * 4.0;
-      est += 1.5e-6 + 2.0 * part / hbm;
+      est += 1.5e-6 + 2.0 * part / (part <= 43e6 ? l2bw : hbm);
     }
     if (est < best * 0.98) { best = est; best_s = s; best_cluster = false; }
     // Clusters only when every cluster of the grid is resident at once: with several
