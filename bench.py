@@ -16,7 +16,7 @@ on.  ``value`` is the mean attention time over the K steps; the other calls go t
 ``breakdown_us``.  ``ms_per_step`` is the one-graph step, replayed K more times after an
 L2 eviction each (``step_three_graphs`` is the step as the sum of the three graphs with
 events between them).  The same run then
-times the attention call alone for at least half a second (so the clock sampler sees
+times the attention call alone for at least a second (so the clock sampler sees
 sustained load), the attention calls of the budget-16 and budget-256 Qwen3-8B workloads,
 the lossless (sampled) verification, the draft-tree build, the ragged attention call and
 the KV compaction.  ``e2e`` times the
@@ -50,7 +50,7 @@ METRIC = "tree-causal paged attention µs/call, HBM GB/s & TFLOP/s vs GB300 roof
 DEFAULT_CONFIG = "c5_qwen3_30b_b8_tree256_32k"
 # Other workloads whose attention call is timed in the same run (budgets 16 and 256).
 SIDE_CONFIGS = ("c2_qwen3_8b_chain16", "c3_qwen3_8b_tree256")
-SUSTAINED_S = 0.5                      # length of the attention-only loop
+SUSTAINED_S = 1.0                      # length of the attention-only loop
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one jf_tree_attention call
 # (attention kernel + combine) from ncu captures of the current kernels (None until a
