@@ -277,6 +277,18 @@ def test_attention_configs(jf, name, nrows):
     assert_attention_close(w, out, lse, rows)
 
 
+@pytest.mark.parametrize("name", ["c3_qwen3_8b_tree256", "c4_qwen3_8b_b32_tree64_paged",
+                                  "c5_qwen3_30b_b8_tree256_32k"])
+def test_attention_every_row_of_the_large_workloads(jf, name):
+    """Every output row of the budget-256 and 32-sequence workloads against the fp64 oracle
+    (workload 5: 65536 rows over 32768-token prefixes, about 1.1 TFLOP of fp64 on the host),
+    so no dispatch boundary, split range or stream-K piece escapes the check."""
+    w = cfg(name)
+    out, lse, err = gpu_attention(jf, w)
+    assert err == 0
+    assert_attention_close(w, out, lse, oracle.all_rows(w))
+
+
 def first_stream_k_cut_pair(w, sms):
     """(b, kv-head) of the first pair that a stream-K range boundary cuts inside, for the
     range partition the attention call uses on `sms` SMs: the key tiles of all pairs laid
