@@ -6,7 +6,12 @@ D and the prefix lengths; fixed test shapes reach each of them once.  These case
 shapes at random (fixed seeds) so that the dispatch boundaries, odd row counts, mixed
 prefix lengths (including empty ones) and deep or flat trees meet in combinations nobody
 picked by hand.  Every row is compared when there are few, else a sample that includes
-each sequence's root, last and deepest node."""
+each sequence's root, last and deepest node.
+
+JF_FUZZ_SCALE=k (default 1) runs k times as many cases of each kind: the first cases are
+the default ones, the rest new seeds."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -17,7 +22,8 @@ from test_gpu_parity import assert_attention_close, gpu_attention, jf, sample_ro
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 48
+SCALE = max(1, int(os.environ.get("JF_FUZZ_SCALE", "1")))
+N_CASES = 48 * SCALE
 
 
 def draw(case):
@@ -77,7 +83,7 @@ def test_fuzz_shapes_cover_the_dispatches():
 
 # ----------------------------------------------------------------------------- ragged
 
-N_RAGGED = 16
+N_RAGGED = 16 * SCALE
 
 
 @pytest.mark.parametrize("case", range(N_RAGGED))
@@ -101,7 +107,7 @@ def test_ragged_attention_random_shapes(jf, case):
 
 # ----------------------------------------------------------------------------- verify
 
-N_VERIFY = 24
+N_VERIFY = 24 * SCALE
 
 
 @pytest.mark.parametrize("case", range(N_VERIFY))
@@ -131,7 +137,7 @@ def test_verify_random_shapes(jf, case):
 
 # ----------------------------------------------------------------------------- draft tree
 
-N_DRAFT = 24
+N_DRAFT = 24 * SCALE
 
 
 @pytest.mark.parametrize("case", range(N_DRAFT))
