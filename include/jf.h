@@ -201,6 +201,68 @@ jf_status jf_tree_verify_static(const void* logits, int32_t dtype, const int32_t
                                 int32_t* bonus, int32_t* dev_err, jf_stream_t stream);
 
 /*
+ * Vocabulary-sharded greedy verification.  When the target model's output layer is split
+ * by vocabulary across GPUs (tensor parallelism), each GPU holds the logits of one token
+ * range [vocab_offset, vocab_offset + V_shard) for every node.  The verify rule of
+ * jf_tree_verify (one target pass scores every drafted node; explainer §4) needs only
+ * each node's argmax, and the argmax over the whole vocabulary is the best of the
+ * per-range argmaxes (greatest value, then lowest token id), so the ranges exchange one
+ * 8-byte key per node and range chunk and every GPU runs the same walk on them:
+ *
+ *   1. chunks = jf_tree_verify_shard_chunks(B, N, largest V_shard)  (same on every GPU)
+ *   2. jf_tree_verify_shard_keys(logits_shard, ..., keys_local)  keys_local [B*N][chunks]
+ *   3. the caller all-gathers keys_local into keys [S][B*N][chunks] (S ranges, any
+ *      order; e.g. torch.distributed.all_gather_into_tensor on uint64 / int64 storage)
+ *   4. jf_tree_verify_from_keys(keys, S, chunks, ...)  -> the outputs of jf_tree_verify
+ *
+ * A key is (order-preserving bits of the value) << 32 | (0xFFFFFFFF - global token id):
+ * the larger key (as an UNSIGNED integer) is the larger value, then the lower id; -0 and
+ * +0 compare equal.  Key 0 marks a chunk with no tokens.  A signed MAX all-reduce of the
+ * int64 storage would order positive values below negative ones: gather, do not reduce.
+ * The library runs no collective itself.
+ */
+
+/* Chunks per node of jf_tree_verify_shard_keys for this shard size; -1 for unsupported
+ * sizes.  Depends on the CURRENT device's SM count: use the same value on every GPU. */
+int32_t jf_tree_verify_shard_chunks(int32_t B, int32_t N, int32_t V_shard);
+
+/*
+ * jf_tree_verify_shard_keys -- per-chunk argmax keys of one vocabulary range.
+ *   logits_shard [B][N][V_shard], dtype JF_DTYPE_BF16 or JF_DTYPE_F32 (finite values).
+ *   vocab_offset global id of the range's first token (>= 0; vocab_offset + V_shard < 2^31).
+ *   chunks       >= 1, the same on every range: normally jf_tree_verify_shard_chunks(B, N,
+ *                largest V_shard).  The range is cut into chunks slices of equal length (a
+ *                multiple of 8 tokens); slices past its end get key 0.
+ *   keys         uint64 [B*N][chunks], device, 8-byte aligned; fully written.
+ * Launches one kernel and allocates nothing.
+ * Errors: JF_ERR_INVALID_ARGUMENT (null pointer, bad dtype, B, N, V_shard or chunks < 1,
+ * negative offset), JF_ERR_UNSUPPORTED (N > JF_MAX_NODES, ids past 2^31 - 1, grid too
+ * large), JF_ERR_MISALIGNED.
+ */
+jf_status jf_tree_verify_shard_keys(const void* logits_shard, int32_t dtype, int32_t B,
+                                    int32_t N, int32_t V_shard, int32_t vocab_offset,
+                                    int32_t chunks, uint64_t* keys, jf_stream_t stream);
+
+/*
+ * jf_tree_verify_from_keys -- the walk of jf_tree_verify on gathered keys.
+ *   keys       uint64 [S][B*N][chunks], device: every range's jf_tree_verify_shard_keys
+ *              output.  argmax[b][i] = the token id of the largest key of row b*N + i;
+ *              the ranges together must cover the vocabulary [0, V).
+ *   S, chunks  >= 1.
+ *   draft, parent, argmax, accept_len, path, bonus, dev_err: as in jf_tree_verify
+ *              (V bounds the draft tokens checked for JF_DEVERR_BAD_TOKEN).
+ *   workspace  at least 8 * B * N bytes, 8-byte aligned, no initialisation.
+ * Launches two kernels (the merge of the keys, then the walk) and allocates nothing.
+ * Errors: JF_ERR_INVALID_ARGUMENT, JF_ERR_UNSUPPORTED (N > JF_MAX_NODES),
+ * JF_ERR_WORKSPACE_TOO_SMALL, JF_ERR_MISALIGNED.
+ */
+jf_status jf_tree_verify_from_keys(const uint64_t* keys, int32_t S, int32_t chunks,
+                                   const int32_t* draft, const int32_t* parent, int32_t B,
+                                   int32_t N, int32_t V, int32_t* argmax, int32_t* accept_len,
+                                   int32_t* path, int32_t* bonus, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, jf_stream_t stream);
+
+/*
  * jf_debug_set_wait_limit_ns -- test hook for the bounded waits (no counterpart in the
  * paper).  Every wait of the tree-attention kernels on their own pipeline (a copy landing,
  * a tensor-core step finishing, a softmax pass) gives up after limit_ns nanoseconds,

@@ -102,3 +102,34 @@ def test_ragged_calls_validate_host_arguments_without_gpu(lib):
                                      fake, 1 << 20, None, None) == 1     # no tree_len
     assert lib.jf_tree_verify_ragged(fake, 7, fake, fake, fake, 1, 4, 10, None, fake, fake, fake,
                                      fake, 1 << 20, None, None) == 1     # bad dtype
+
+
+def test_shard_verify_calls_validate_host_arguments_without_gpu(lib):
+    """The vocabulary-sharded verify calls reject bad sizes, offsets and pointers before any
+    launch."""
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails early
+    lib.jf_tree_verify_shard_chunks.argtypes = [i32, i32, i32]
+    lib.jf_tree_verify_shard_chunks.restype = i32
+    assert lib.jf_tree_verify_shard_chunks(1, 0, 100) == -1
+    assert lib.jf_tree_verify_shard_chunks(1, 5000, 100) == -1
+    lib.jf_tree_verify_shard_keys.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P]
+    assert lib.jf_tree_verify_shard_keys(None, 0, 1, 4, 100, 0, 1, fake, None) == 1
+    assert lib.jf_tree_verify_shard_keys(fake, 7, 1, 4, 100, 0, 1, fake, None) == 1
+    assert lib.jf_tree_verify_shard_keys(fake, 0, 1, 4, 100, -1, 1, fake, None) == 1
+    assert lib.jf_tree_verify_shard_keys(fake, 0, 1, 4, 100, 0, 0, fake, None) == 1
+    assert lib.jf_tree_verify_shard_keys(fake, 0, 1, 5000, 100, 0, 1, fake, None) == 3
+    assert lib.jf_tree_verify_shard_keys(fake, 0, 1, 4, 100, 0x7FFFFFF0, 1, fake, None) == 3
+    assert lib.jf_tree_verify_shard_keys(fake, 0, 1, 4, 100, 0, 1,
+                                         ctypes.c_void_p(0x10004), None) == 7
+    lib.jf_tree_verify_from_keys.argtypes = [P, i32, i32, P, P, i32, i32, i32, P, P, P, P, P, sz,
+                                             P, P]
+    args = [fake, 2, 3, fake, fake, 2, 4, 100, None, fake, fake, fake, fake, 64, None, None]
+    no_ws = list(args); no_ws[12] = None
+    assert lib.jf_tree_verify_from_keys(*no_ws) == 1
+    no_s = list(args); no_s[1] = 0
+    assert lib.jf_tree_verify_from_keys(*no_s) == 1
+    small = list(args); small[13] = 63            # 8 * B * N = 64 bytes needed
+    assert lib.jf_tree_verify_from_keys(*small) == 4
+    mis = list(args); mis[12] = ctypes.c_void_p(0x10004)
+    assert lib.jf_tree_verify_from_keys(*mis) == 7

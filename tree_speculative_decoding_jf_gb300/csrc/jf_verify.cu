@@ -84,7 +84,7 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t k) {
 template <typename T>
 __global__ void __launch_bounds__(kArgmaxThreads)
     argmax_chunk_kernel(const T* __restrict__ logits, long long V, int chunks, int chunk_len,
-                        uint64_t* __restrict__ part) {
+                        uint64_t* __restrict__ part, int idx_off) {
   constexpr int kVec = 16 / sizeof(T);
   grid_dependency_wait();
   const long long row = blockIdx.x / chunks;
@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(kArgmaxThreads)
     if (first < 0) first = static_cast<int>(idx);
   }
   if (best.i < 0 && first >= 0) best.i = first;   // every value it saw was -inf
-  uint64_t key = best.i < 0 ? 0ull : pack_key(best.v, best.i);
+  // keys carry vocabulary indices: the row's own plus idx_off (a shard's first token)
+  uint64_t key = best.i < 0 ? 0ull : pack_key(best.v, best.i + idx_off);
 
   __shared__ uint64_t s_keys[kArgmaxThreads / 32];
   key = warp_max_u64(key);
@@ -556,10 +557,10 @@ jf_status tree_verify_call(const void* logits, int32_t dtype, const int32_t* dra
       dtype == JF_DTYPE_BF16
           ? jf::launch_pdl(jf::argmax_chunk_kernel<uint16_t>, dim3(static_cast<unsigned>(grid)),
                            dim3(jf::kArgmaxThreads), 0, s, static_cast<const uint16_t*>(logits),
-                           Vl, p.chunks, p.chunk_len, part)
+                           Vl, p.chunks, p.chunk_len, part, 0)
           : jf::launch_pdl(jf::argmax_chunk_kernel<float>, dim3(static_cast<unsigned>(grid)),
                            dim3(jf::kArgmaxThreads), 0, s, static_cast<const float*>(logits), Vl,
-                           p.chunks, p.chunk_len, part);
+                           p.chunks, p.chunk_len, part, 0);
   if (ea != cudaSuccess) return JF_ERR_CUDA;
   return jf::launch_walk(part, p.chunks, draft, parent, tree_len, B, N, V, argmax, accept_len, path,
                          bonus, dev_err, s);
@@ -643,12 +644,104 @@ extern "C" jf_status jf_tree_verify_static(const void* logits, int32_t dtype,
       dtype == JF_DTYPE_BF16
           ? jf::launch_pdl(jf::argmax_chunk_kernel<uint16_t>, dim3(grid), dim3(jf::kArgmaxThreads),
                            0, s, static_cast<const uint16_t*>(logits), Vl, p.chunks, p.chunk_len,
-                           part)
+                           part, 0)
           : jf::launch_pdl(jf::argmax_chunk_kernel<float>, dim3(grid), dim3(jf::kArgmaxThreads), 0,
-                           s, static_cast<const float*>(logits), Vl, p.chunks, p.chunk_len, part);
+                           s, static_cast<const float*>(logits), Vl, p.chunks, p.chunk_len, part, 0);
   if (ea != cudaSuccess) return JF_ERR_CUDA;
   return jf::launch_walk(part, p.chunks, draft, parent, nullptr, B, N, V, argmax, accept_len, path,
                          bonus, dev_err, s);
+}
+
+// ------------------------------------------------------------- vocabulary-sharded verify
+// A target model whose output layer is split by vocabulary gives each GPU the logits of
+// one vocabulary range.  The argmax keys (value, ~global index) of every range are
+// exchanged (an all-gather the caller runs) and the walk runs on their maximum: the keys
+// order by value and then by lower index, so the maximum over all ranges is the
+// unsharded argmax.
+
+namespace jf {
+namespace {
+
+// keys [S][rows][chunks] -> merged [rows]: one thread per row.
+__global__ void __launch_bounds__(256)
+    merge_shard_keys_kernel(const uint64_t* __restrict__ keys, int S, long long rows, int chunks,
+                            uint64_t* __restrict__ merged) {
+  grid_dependency_wait();
+  const long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r < rows) {
+    uint64_t k = 0ull;
+    for (int sh = 0; sh < S; ++sh)
+      for (int c = 0; c < chunks; ++c) {
+        const uint64_t v = keys[(static_cast<long long>(sh) * rows + r) * chunks + c];
+        k = v > k ? v : k;
+      }
+    merged[r] = k;
+  }
+  grid_dependents_launch();
+}
+
+}  // namespace
+}  // namespace jf
+
+extern "C" int32_t jf_tree_verify_shard_chunks(int32_t B, int32_t N, int32_t V_shard) {
+  jf::VerifyPlan p;
+  if (!jf::plan_verify(B, N, V_shard, &p)) return -1;
+  return p.chunks;
+}
+
+extern "C" jf_status jf_tree_verify_shard_keys(const void* logits_shard, int32_t dtype, int32_t B,
+                                               int32_t N, int32_t V_shard, int32_t vocab_offset,
+                                               int32_t chunks, uint64_t* keys,
+                                               jf_stream_t stream) {
+  if (logits_shard == nullptr || keys == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
+  if (B < 1 || N < 1 || V_shard < 1 || chunks < 1 || vocab_offset < 0) return JF_ERR_INVALID_ARGUMENT;
+  if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  if (static_cast<long long>(vocab_offset) + V_shard > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  if (!jf::aligned_to(keys, 8)) return JF_ERR_MISALIGNED;
+  if (!jf::aligned_to(logits_shard, dtype == JF_DTYPE_BF16 ? 2 : 4)) return JF_ERR_MISALIGNED;
+  // chunks of at least 8 logits; trailing chunks past the shard end write key 0
+  long long len = (static_cast<long long>(V_shard) + chunks - 1) / chunks;
+  len = (len + 7) / 8 * 8;
+  const long long grid = static_cast<long long>(B) * N * chunks;
+  if (grid > 0x7FFFFFFFll || len > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const long long Vl = V_shard;
+  const int cl = static_cast<int>(len);
+  const cudaError_t e =
+      dtype == JF_DTYPE_BF16
+          ? jf::launch_pdl(jf::argmax_chunk_kernel<uint16_t>, dim3(static_cast<unsigned>(grid)),
+                           dim3(jf::kArgmaxThreads), 0, s, static_cast<const uint16_t*>(logits_shard),
+                           Vl, chunks, cl, keys, vocab_offset)
+          : jf::launch_pdl(jf::argmax_chunk_kernel<float>, dim3(static_cast<unsigned>(grid)),
+                           dim3(jf::kArgmaxThreads), 0, s, static_cast<const float*>(logits_shard),
+                           Vl, chunks, cl, keys, vocab_offset);
+  return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+}
+
+extern "C" jf_status jf_tree_verify_from_keys(const uint64_t* keys, int32_t S, int32_t chunks,
+                                              const int32_t* draft, const int32_t* parent, int32_t B,
+                                              int32_t N, int32_t V, int32_t* argmax,
+                                              int32_t* accept_len, int32_t* path, int32_t* bonus,
+                                              void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_err, jf_stream_t stream) {
+  if (keys == nullptr || draft == nullptr || parent == nullptr || accept_len == nullptr ||
+      path == nullptr || bonus == nullptr || workspace == nullptr)
+    return JF_ERR_INVALID_ARGUMENT;
+  if (S < 1 || chunks < 1 || B < 1 || N < 1 || V < 1) return JF_ERR_INVALID_ARGUMENT;
+  if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(B) * N;
+  if (workspace_bytes < static_cast<size_t>(rows) * sizeof(uint64_t)) return JF_ERR_WORKSPACE_TOO_SMALL;
+  if (!jf::aligned_to(workspace, 8) || !jf::aligned_to(keys, 8)) return JF_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint64_t* merged = static_cast<uint64_t*>(workspace);
+  const long long blocks = (rows + 255) / 256;
+  if (blocks > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
+  if (jf::launch_pdl(jf::merge_shard_keys_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                     keys, static_cast<int>(S), rows, static_cast<int>(chunks), merged) != cudaSuccess)
+    return JF_ERR_CUDA;
+  return jf::launch_walk(merged, 1, draft, parent, nullptr, B, N, V, argmax, accept_len, path, bonus,
+                         dev_err, s);
 }
 
 // ------------------------------------------------------------------------ stochastic verify

@@ -75,6 +75,13 @@ def _load():
                                            P, P]
     lib.jf_tree_verify_sampled.restype = ctypes.c_int
     lib.jf_debug_set_wait_limit_ns.restype = ctypes.c_int
+    lib.jf_tree_verify_shard_chunks.argtypes = [i32, i32, i32]
+    lib.jf_tree_verify_shard_chunks.restype = ctypes.c_int32
+    lib.jf_tree_verify_shard_keys.argtypes = [P, i32, i32, i32, i32, i32, i32, P, P]
+    lib.jf_tree_verify_shard_keys.restype = ctypes.c_int
+    lib.jf_tree_verify_from_keys.argtypes = [P, i32, i32, P, P, i32, i32, i32, P, P, P, P, P, sz,
+                                             P, P]
+    lib.jf_tree_verify_from_keys.restype = ctypes.c_int
     return lib
 
 
@@ -327,6 +334,54 @@ def jf_tree_verify_static(logits, draft, parent, accept_len, path, bonus, argmax
         _ptr(path), _ptr(bonus), _ptr(dev_err), _stream(stream)))
 
 
+def jf_tree_verify_shard_chunks(B, N, V_shard) -> int:
+    n = _lib.jf_tree_verify_shard_chunks(B, N, V_shard)
+    if n < 0:
+        raise JFError("jf_tree_verify_shard_chunks", 3)
+    return int(n)
+
+
+def jf_tree_verify_shard_keys(logits_shard, vocab_offset, keys, stream=None) -> None:
+    """Argmax keys of one vocabulary range: logits_shard [B][N][V_shard] (bf16 or f32) holds
+    the tokens vocab_offset .. vocab_offset + V_shard - 1; keys is int64 [B][N][chunks]
+    (the uint64 keys' bits).  See include/jf.h."""
+    B, N, Vs = logits_shard.shape
+    if logits_shard.dtype == torch.bfloat16:
+        dt = JF_DTYPE_BF16
+    elif logits_shard.dtype == torch.float32:
+        dt = JF_DTYPE_F32
+    else:
+        raise TypeError("logits_shard must be bfloat16 or float32")
+    _need(logits_shard, "logits_shard", logits_shard.dtype)
+    _need(keys, "keys", torch.int64)
+    if keys.dim() != 3 or tuple(keys.shape[:2]) != (B, N):
+        raise ValueError(f"keys has shape {tuple(keys.shape)}, expected ({B}, {N}, chunks)")
+    _check("jf_tree_verify_shard_keys", _lib.jf_tree_verify_shard_keys(
+        _ptr(logits_shard), dt, B, N, Vs, int(vocab_offset), keys.shape[2], _ptr(keys),
+        _stream(stream)))
+
+
+def jf_tree_verify_from_keys(keys, V, draft, parent, accept_len, path, bonus, workspace,
+                             argmax=None, dev_err=None, stream=None) -> None:
+    """The greedy walk on every range's keys, int64 [S][B][N][chunks] (an all-gather of
+    jf_tree_verify_shard_keys' outputs); workspace uint8 of at least 8*B*N bytes."""
+    S, B, N, chunks = keys.shape
+    _need(keys, "keys", torch.int64)
+    for name, t, shape in (("draft", draft, (B, N)), ("parent", parent, (B, N)),
+                           ("accept_len", accept_len, (B,)), ("path", path, (B, N)),
+                           ("bonus", bonus, (B,))):
+        _need(t, name, torch.int32, shape)
+    _need(workspace, "workspace", torch.uint8)
+    if argmax is not None:
+        _need(argmax, "argmax", torch.int32, (B, N))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_tree_verify_from_keys", _lib.jf_tree_verify_from_keys(
+        _ptr(keys), S, chunks, _ptr(draft), _ptr(parent), B, N, int(V), _ptr(argmax),
+        _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(workspace), workspace.numel(),
+        _ptr(dev_err), _stream(stream)))
+
+
 def jf_compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,
                            new_prefix_len, dev_err=None, stream=None) -> None:
     """Moves the accepted path's K/V next to the prefix, in place (see include/jf.h)."""
@@ -440,6 +495,33 @@ def tree_verify_sampled(logits, draft, parent, uniform, bonus_uniform, temperatu
     jf_tree_verify_sampled(logits, draft, parent, uniform, bonus_uniform, temperature, accept_len,
                            path, bonus, ws, dev_err, stream)
     return accept_len, path, bonus
+
+
+def tree_verify_shard_keys(logits_shard, vocab_offset, chunks=None, stream=None):
+    """Allocating wrapper of jf_tree_verify_shard_keys: int64 keys [B][N][chunks].  Every
+    range must use the same chunks (by default the planned count for this range's size:
+    pass the largest range's count when the ranges differ in size)."""
+    B, N, Vs = logits_shard.shape
+    if chunks is None:
+        chunks = jf_tree_verify_shard_chunks(B, N, Vs)
+    keys = torch.empty((B, N, chunks), dtype=torch.int64, device=logits_shard.device)
+    jf_tree_verify_shard_keys(logits_shard, vocab_offset, keys, stream)
+    return keys
+
+
+def tree_verify_from_keys(keys, V, draft, parent, dev_err=None, stream=None):
+    """Allocating wrapper of jf_tree_verify_from_keys on gathered keys [S][B][N][chunks]:
+    (argmax, accept_len, path, bonus) as tree_verify returns them."""
+    S, B, N, _ = keys.shape
+    dev = keys.device
+    argmax = torch.empty((B, N), dtype=torch.int32, device=dev)
+    accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    bonus = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = torch.empty((8 * B * N,), dtype=torch.uint8, device=dev)
+    jf_tree_verify_from_keys(keys, V, draft, parent, accept_len, path, bonus, ws, argmax,
+                             dev_err, stream)
+    return argmax, accept_len, path, bonus
 
 
 def compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,
