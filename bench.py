@@ -417,6 +417,36 @@ def run_gpu(args, w, rank, world, peaks):
         timed(g_samp, k)
     samp_ms = ms([timed(g_samp, k) for k in range(args.steps)])
 
+    # ---- vocabulary-sharded verification as one of 8 GPUs would run it (the target's
+    # output layer split into 8 token ranges): this GPU's range keys, then the merge and
+    # walk on all 8 ranges' keys.  The other ranges' keys are made once beforehand; the
+    # all-gather between the two calls is not timed.  Not part of the step.
+    S_v = 8
+    cuts_v = [V * s // S_v for s in range(S_v + 1)]
+    ch_v = max(jf.jf_tree_verify_shard_chunks(B, N, cuts_v[s + 1] - cuts_v[s]) for s in range(S_v))
+    range0 = t["logits"][:, :, cuts_v[0]:cuts_v[1]].contiguous()
+    keys_v = torch.stack([jf.tree_verify_shard_keys(
+        t["logits"][:, :, cuts_v[s]:cuts_v[s + 1]].contiguous(), cuts_v[s], ch_v)
+        for s in range(S_v)])
+    v_am = torch.empty_like(argmax)
+    v_acc, v_path, v_bonus = torch.empty_like(acc), torch.empty_like(path), torch.empty_like(bonus)
+    ws_k = torch.empty((8 * B * N,), dtype=torch.uint8, device=dev)
+
+    def call_sharded():
+        jf.jf_tree_verify_shard_keys(range0, 0, keys_v[0])
+        jf.jf_tree_verify_from_keys(keys_v, V, t["draft"], t["parent"], v_acc, v_path, v_bonus,
+                                    ws_k, v_am, err)
+
+    call_sharded()
+    g_shard = capture(call_sharded)
+    for k in range(args.warmup):
+        timed(g_shard, k)
+    shard_ms = ms([timed(g_shard, k) for k in range(args.steps)])
+    torch.cuda.synchronize(dev)
+    shard_same = bool((v_am == argmax).all() and (v_acc == acc).all() and (v_path == path).all()
+                      and (v_bonus == bonus).all())
+    del range0, keys_v
+
     # ---- before verification: best-first draft-tree construction from per-depth draft
     # logits (16 depths, 8 candidates per depth, the workload's budget); not part of the step.
     dl = wl.draft_logits(B, 16, V, seed=w.seed)
@@ -456,6 +486,34 @@ def run_gpu(args, w, rank, world, peaks):
     for k in range(args.warmup):
         timed(g_rag, k)
     rag_ms = ms([timed(g_rag, k) for k in range(args.steps)])
+
+    # ---- the same ragged trees in the packed (cu_seqlens) layout: q, out and the mask
+    # hold only real nodes; the call must match the ragged one row for row.
+    cu_np = np.concatenate([[0], np.cumsum(rag_len)]).astype(np.int32)
+    T_p = int(cu_np[-1])
+    t_cu = torch.from_numpy(cu_np).to(dev)
+    q_p = torch.cat([t["q"][b, :int(n)] for b, n in enumerate(rag_len)]).contiguous()
+    par_p = torch.cat([t["parent"][b, :int(n)] for b, n in enumerate(rag_len)]).contiguous()
+    mask_p = torch.empty((T_p, mask.shape[-1]), dtype=torch.int64, device=dev)
+    jf.jf_build_tree_mask_packed(par_p, t["prefix_len"], t_cu, N, mask_p, None, None, err)
+    out_p = torch.empty((T_p, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse_p = torch.empty((Hq, T_p), dtype=torch.float32, device=dev)
+
+    def call_attn_packed():
+        jf.jf_tree_attention_packed(q_p, t["k_cache"], t["v_cache"], t["block_table"],
+                                    t["prefix_len"], t_cu, N, mask_p, w.scale, out_p, lse_p,
+                                    ws_a, err)
+
+    call_attn_packed()
+    g_pk = capture(call_attn_packed)
+    for k in range(args.warmup):
+        timed(g_pk, k)
+    pk_ms = ms([timed(g_pk, k) for k in range(args.steps)])
+    torch.cuda.synchronize(dev)
+    pk_same = all(torch.equal(out_p[int(cu_np[b]):int(cu_np[b + 1])].view(torch.int16),
+                              out[b, :int(n)].view(torch.int16))
+                  for b, n in enumerate(rag_len))
+    del q_p, out_p, lse_p, mask_p
     torch.cuda.synchronize(dev)
 
     # ---- after verification: accepted-path KV compaction (not part of the step).  It
@@ -476,8 +534,9 @@ def run_gpu(args, w, rank, world, peaks):
     return dict(step_ms=step_ms, step_ev_ms=step_ev_ms, mask_ms=mask_ms, attn_ms=attn_ms, ver_ms=ver_ms, sus_ms=sus_ms,
                 clocks=clk, e2e=e2e, launches=2 * launches_per_step * args.steps, ws=ws_a_bytes,
                 compact_ms=compact_ms, accepted=acc.cpu().tolist(), tree_ms=tree_ms, samp_ms=samp_ms,
-                samp_accepted=s_acc.cpu().tolist(),
-                tree_bytes=tree_bytes, rag_ms=rag_ms, rag_len=rag_len.tolist(), side=side_lines)
+                samp_accepted=s_acc.cpu().tolist(), shard_ms=shard_ms, shard_same=shard_same,
+                tree_bytes=tree_bytes, rag_ms=rag_ms, rag_len=rag_len.tolist(), side=side_lines,
+                pk_ms=pk_ms, pk_same=pk_same)
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -598,6 +657,8 @@ def main():
                          "verify_sampled_hbm_gbs": verify_algorithmic_bytes(w) /
                          (statistics.mean(r["samp_ms"]) * 1e-3) / 1e9,
                          "verify_sampled_accepted_nodes": r["samp_accepted"],
+                         "verify_vocab_shard8": statistics.mean(r["shard_ms"]) * 1e3,
+                         "verify_vocab_shard8_equals_verify": r["shard_same"],
                          "other_workloads_attention": r["side"],
                          "draft_tree_build": statistics.mean(r["tree_ms"]) * 1e3,
                          "draft_tree_logits_hbm_gbs": r["tree_bytes"] /
@@ -606,6 +667,8 @@ def main():
                          "kv_compaction_accepted_nodes": r["accepted"],
                          "attention_ragged": statistics.mean(r["rag_ms"]) * 1e3,
                          "attention_ragged_tree_len": r["rag_len"],
+                         "attention_packed": statistics.mean(r["pk_ms"]) * 1e3,
+                         "attention_packed_equals_ragged": r["pk_same"],
                          "attention_ragged_hbm_gbs": attention_algorithmic_bytes(w, r["rag_len"]) /
                          (statistics.mean(r["rag_ms"]) * 1e-3) / 1e9,
                          "attention_ragged_tflops": attention_algorithmic_flops(w, r["rag_len"]) /

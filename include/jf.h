@@ -60,7 +60,7 @@ typedef enum { JF_DTYPE_BF16 = 0, JF_DTYPE_F32 = 1 } jf_dtype;
 #define JF_DEVERR_BAD_TOKEN 0x8  /* draft token (non-root node) outside [0, V)          */
 #define JF_DEVERR_TIMEOUT 0x10   /* an in-kernel wait gave up after its time limit      */
 #define JF_DEVERR_BAD_PATH 0x20  /* accepted path / length malformed (KV compaction)     */
-#define JF_DEVERR_BAD_TREE_LEN 0x40 /* tree_len[b] outside [1, N] (ragged calls)         */
+#define JF_DEVERR_BAD_TREE_LEN 0x40 /* tree_len[b] outside [1, N], or a bad packed span   */
 
 /* Largest tree (nodes per sequence) any call accepts. */
 #define JF_MAX_NODES 4096
@@ -356,6 +356,47 @@ jf_status jf_tree_verify_ragged(const void* logits, int32_t dtype, const int32_t
                                 int32_t N, int32_t V, int32_t* argmax, int32_t* accept_len,
                                 int32_t* path, int32_t* bonus, void* workspace,
                                 size_t workspace_bytes, int32_t* dev_err, jf_stream_t stream);
+
+/*
+ * Packed (cu_seqlens) layout of ragged trees: the per-node arrays hold only real nodes,
+ * sequence after sequence.  cu_seqlens int32 [B + 1] (device) with cu_seqlens[0] = 0 and
+ * cu_seqlens[B] = T: sequence b's n_b = cu_seqlens[b + 1] - cu_seqlens[b] nodes
+ * (1 <= n_b <= N_max) sit at rows cu_seqlens[b] .. cu_seqlens[b + 1] - 1, and parent and
+ * path entries are node ids within the sequence (0 .. n_b - 1).  Each call computes, for
+ * every sequence, what its _ragged counterpart computes with N = N_max and
+ * tree_len[b] = n_b (same kernels, same plan: outputs equal bit for bit), with packed
+ * arrays in place of padded ones:
+ *   parent, draft, depth, pos, argmax   int32 [T]
+ *   mask                                uint64 [T][W], W = ceil(N_max / 64)
+ *   q, out                              bf16 [T][Hq][D]
+ *   lse                                 fp32 [Hq][T]
+ *   logits                              [T][V]
+ *   accept_len, bonus [B] and path [B][N_max] keep their shapes.
+ * A span that is empty, longer than N_max, decreasing or outside [0, T) sets
+ * JF_DEVERR_BAD_TREE_LEN; nothing of that sequence is then read or written except its
+ * accept_len (0), path (0, then -1) and bonus (-1) in verify.  T is a host argument
+ * (the caller knows the batch it packed).  Workspaces: jf_tree_attention_workspace_size
+ * with N = N_max; jf_tree_verify_packed_workspace_size(T, V) for verify.
+ * Limits: as the padded calls, plus 1 <= T and T + N_max < 2^31.
+ */
+jf_status jf_build_tree_mask_packed(const int32_t* parent, const int32_t* prefix_len,
+                                    const int32_t* cu_seqlens, int32_t B, int32_t N_max,
+                                    int32_t T, uint64_t* mask, int32_t* depth, int32_t* pos,
+                                    int32_t* dev_err, jf_stream_t stream);
+jf_status jf_tree_attention_packed(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, const int32_t* prefix_len,
+                                   const int32_t* cu_seqlens, const uint64_t* mask, int32_t B,
+                                   int32_t N_max, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                                   int32_t page_size, int32_t max_pages, int32_t num_pages,
+                                   float scale, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, jf_stream_t stream);
+size_t jf_tree_verify_packed_workspace_size(int32_t T, int32_t V);
+jf_status jf_tree_verify_packed(const void* logits, int32_t dtype, const int32_t* draft,
+                                const int32_t* parent, const int32_t* cu_seqlens, int32_t B,
+                                int32_t N_max, int32_t T, int32_t V, int32_t* argmax,
+                                int32_t* accept_len, int32_t* path, int32_t* bonus,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                jf_stream_t stream);
 
 /* ---------------------------------------------------------------- before verification
  * jf_build_draft_tree -- builds the draft tree from per-depth draft logits.  JetFlow

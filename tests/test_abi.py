@@ -133,3 +133,35 @@ def test_shard_verify_calls_validate_host_arguments_without_gpu(lib):
     assert lib.jf_tree_verify_from_keys(*small) == 4
     mis = list(args); mis[12] = ctypes.c_void_p(0x10004)
     assert lib.jf_tree_verify_from_keys(*mis) == 7
+
+
+def test_packed_calls_validate_host_arguments_without_gpu(lib):
+    """The packed (cu_seqlens) entry points need cu_seqlens and a positive T."""
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails early
+    lib.jf_build_tree_mask_packed.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P]
+    assert lib.jf_build_tree_mask_packed(fake, fake, None, 2, 16, 20, fake, None, None, None,
+                                         None) == 1
+    assert lib.jf_build_tree_mask_packed(fake, fake, fake, 2, 16, 0, fake, None, None, None,
+                                         None) == 1
+    assert lib.jf_build_tree_mask_packed(fake, fake, fake, 2, 5000, 20, fake, None, None, None,
+                                         None) == 3
+    lib.jf_tree_attention_packed.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                             i32, i32, i32, ctypes.c_float, P, P, P, sz, P, P]
+    args = [fake] * 7 + [2, 16, 20, 32, 8, 128, 16, 10, 10, 0.088, fake, None, None, 0, None,
+                         None]
+    no_cu = list(args); no_cu[5] = None
+    assert lib.jf_tree_attention_packed(*no_cu) == 1
+    no_t = list(args); no_t[9] = 0
+    assert lib.jf_tree_attention_packed(*no_t) == 1
+    huge_t = list(args); huge_t[9] = 0x7FFFFFF8
+    assert lib.jf_tree_attention_packed(*huge_t) == 3
+    lib.jf_tree_verify_packed_workspace_size.argtypes = [i32, i32]
+    lib.jf_tree_verify_packed_workspace_size.restype = sz
+    assert lib.jf_tree_verify_packed_workspace_size(0, 100) == ctypes.c_size_t(-1).value
+    lib.jf_tree_verify_packed.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz,
+                                          P, P]
+    assert lib.jf_tree_verify_packed(fake, 0, fake, fake, None, 2, 16, 20, 100, None, fake, fake,
+                                     fake, fake, 1 << 20, None, None) == 1     # no cu_seqlens
+    assert lib.jf_tree_verify_packed(fake, 0, fake, fake, fake, 2, 16, 0, 100, None, fake, fake,
+                                     fake, fake, 1 << 20, None, None) == 1     # T = 0

@@ -119,7 +119,21 @@ struct AttnParams {
   int cluster_merge;    // 1: the splits of a unit form one cluster and merge through DSMEM
   float scale_log2;     // softmax scale * log2(e)
   const int32_t* tree_len;  // ragged calls: nodes per sequence (else null: N everywhere)
+  const int32_t* cu;        // packed calls: cumulative node counts [B + 1] (else null)
+  long long T;              // packed calls: total nodes (rows of q, out, mask)
 };
+
+// Packed calls (cu != null) keep q, out and mask as [T][...] rows, sequence b's nodes at
+// rows cu[b] .. cu[b + 1] - 1, and lse as [Hq][T]; the others [B][N][...] and [B][Hq][N].
+// row0 is the sequence's first row (b * N when not packed).
+__device__ __forceinline__ size_t out_row(long long row0, int i, int Hq, int h) {
+  return static_cast<size_t>((row0 + i) * Hq + h);
+}
+__device__ __forceinline__ size_t lse_index(bool packed, long long row0, long long T, int b,
+                                            int h, int i, int Hq, int N) {
+  return packed ? static_cast<size_t>(h * T + row0 + i)
+                : static_cast<size_t>((static_cast<long long>(b) * Hq + h) * N + i);
+}
 
 // Time limit of the kernels' bounded waits on their own pipeline (the waits that drain
 // copies and MMAs before a CTA exits always allow kWaitLimitNs).  Lowered only through
@@ -366,6 +380,9 @@ struct MergeArgs {
   uint16_t* out;
   float* lse;
   int N, Hq, G, M, splits;
+  long long row0, T;   // the sequence's first row; total rows (packed calls)
+  int rows;            // rows the sequence owns: N, or its node count when packed
+  bool packed;
 };
 
 template <int NT, int D>
@@ -402,9 +419,9 @@ __device__ __noinline__ void merge_cluster(uint8_t* sm, const MergeArgs p, int b
     for (int s2 = 0; s2 < S; ++s2) w[s2] *= inv;
     const int rr = r_lo + e;
     const int rg = (mp * NT + rr / kRowTile) * kRowTile + rr % kRowTile;
-    if (p.lse != nullptr && rg < p.M) {
+    if (p.lse != nullptr && rg < p.M && rg / p.G < p.rows) {
       const int i = rg / p.G, h = g * p.G + (rg % p.G);
-      p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.N + i] =
+      p.lse[lse_index(p.packed, p.row0, p.T, b, h, i, p.Hq, p.N)] =
           (sum > 0.f ? mx + __log2f(sum) : -INFINITY) * 0.69314718055994531f;
     }
   }
@@ -415,7 +432,7 @@ __device__ __noinline__ void merge_cluster(uint8_t* sm, const MergeArgs p, int b
     const int rr = r_lo + el;
     const int t = rr / kRowTile, row = rr % kRowTile;
     const int rg = (mp * NT + t) * kRowTile + row;
-    if (rg >= p.M) continue;
+    if (rg >= p.M || rg / p.G >= p.rows) continue;
     const float* w = s_w + el * kMaxSplits;
     const uint8_t* src = reinterpret_cast<const uint8_t*>(part_row<NT, D>(sm, t, row)) +
                          ((static_cast<uint32_t>(k) ^ static_cast<uint32_t>(row & 7)) << 4);
@@ -431,7 +448,7 @@ __device__ __noinline__ void merge_cluster(uint8_t* sm, const MergeArgs p, int b
         acc.z += w[s2] * v[s2].z; acc.w += w[s2] * v[s2].w;
       }
     const int i = rg / p.G, h = g * p.G + (rg % p.G);
-    uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * D + k * 4;
+    uint16_t* dst = p.out + out_row(p.row0, i, p.Hq, h) * D + k * 4;
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
   }
   cluster_sync();                                        // nobody leaves while others read it
@@ -533,14 +550,21 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   int b = slot;
   if constexpr (LPT) b = lpt_sequence(p.prefix_len, p.B, p.max_pages * kPage - p.N, slot);
 
-  // Q does not depend on the sequence length: its load starts before anything is read.
+  // Q does not depend on the sequence length: its load starts before anything is read
+  // (packed calls read the sequence's first row first; rows of the next sequence or past
+  // the end that a tile reaches are padding rows, their results never stored).
   if (threadIdx.x == 0) {
+    int qrow0 = 0, qb = b;
+    if (p.cu != nullptr) {
+      qrow0 = static_cast<int>(seq_span(p.cu, nullptr, b, p.N, p.T).row0);
+      qb = 0;
+    }
     mbar_arrive_expect_tx(&q_full, NT * C::kTileBytes);
     for (int t = 0; t < NT; ++t) {
       const int node0 = ((mp * NT + t) * kRowTile) / p.G;
       for (int hh = 0; hh < C::kHalves; ++hh)
         tma_load_4d(q_s + t * C::kTileBytes + hh * C::kHalfBytes, &qmap, &q_full, hh * 64,
-                    g * p.G, node0, b);
+                    g * p.G, qrow0 + node0, qb);
     }
   }
   // The first key tiles' page ids are read together with the prefix length (one round
@@ -561,9 +585,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   }
 
   const int cap = p.max_pages * kPage;
-  const int nt = tree_nodes(p.tree_len, b, p.N);
-  if (p.tree_len != nullptr && nt != p.tree_len[b] && threadIdx.x == 0)
-    report(p.dev_err, JF_DEVERR_BAD_TREE_LEN);
+  const SeqSpan sp = seq_span(p.cu, p.tree_len, b, p.N, p.T);
+  const int nt = sp.n;
+  if (!sp.ok && threadIdx.x == 0) report(p.dev_err, JF_DEVERR_BAD_TREE_LEN);
   int P = p.prefix_len[b];
   if (P < 0 || P > cap - nt) {
     if (threadIdx.x == 0) report(p.dev_err, JF_DEVERR_BAD_PREFIX);
@@ -575,10 +599,11 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
   const int k1 = min(ntiles, k0 + p.chunk_tiles);
   const int T = max(0, k1 - k0);
 
-  // Ragged calls: a row-tile group whose rows all belong to padding nodes (node >= n_b)
-  // has nothing to compute (those rows carry no meaning).  The splits of a unit share the
-  // group, so the CTAs of a merging cluster leave together.  The Q load is drained first.
-  if (p.tree_len != nullptr && (mp * NT * kRowTile) / p.G >= nt) {
+  // Ragged and packed calls: a row-tile group whose rows all belong to padding nodes
+  // (node >= n_b) has nothing to compute (those rows carry no meaning; a packed sequence
+  // with a bad span has n_b = 0).  The splits of a unit share the group, so the CTAs of a
+  // merging cluster leave together.  The Q load is drained first.
+  if ((p.tree_len != nullptr || p.cu != nullptr) && (mp * NT * kRowTile) / p.G >= nt) {
     if (threadIdx.x == 0) {
       int zero = 0;
       mbar_wait(&q_full, 0, &zero);
@@ -596,7 +621,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       __syncthreads();
       for (int t = 0; t < NT; ++t)
         for (int e = threadIdx.x; e < kRowTile; e += blockDim.x) part_lse<NT, D>(sm, t)[e] = -INFINITY;
-      merge_cluster<NT, D>(sm, MergeArgs{p.out, p.lse, p.N, p.Hq, p.G, p.M, p.splits}, b, g, mp, split);
+      merge_cluster<NT, D>(sm, MergeArgs{p.out, p.lse, p.N, p.Hq, p.G, p.M, p.splits, sp.row0, p.T, sp.rows, p.cu != nullptr}, b, g, mp, split);
       return;
     }
     if (warp >= 4) {                  // split past the sequence: an empty partial (weight 0)
@@ -870,14 +895,14 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     const int wq = warp & 3;
     const int rl = wq * 32 + lane;                       // row within the tile = TMEM lane
     const int r = (mp * NT + t) * kRowTile + rl;
-    const bool valid = r < p.M;
+    const bool valid = r < p.M && r / p.G < sp.rows;    // the row exists in memory
     const int node_base = ((mp * NT + t) * kRowTile) / p.G;
     const int i = r / p.G;
     const int h = g * p.G + (r % p.G);
     const int W = p.W;
     // The node's ancestor-mask words a tile needs (at most three 64-bit words for 128
     // keys) are loaded into registers before the tile's S is waited for.
-    const uint64_t* mrow = p.mask + (static_cast<size_t>(b) * p.N + (valid ? i : 0)) * W;
+    const uint64_t* mrow = p.mask + (sp.row0 + (valid ? i : 0)) * W;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + C::kTmemS + t * 128 + lane_off;
     const uint32_t tO = tmem + C::kTmemO + t * 128 + lane_off;
@@ -940,7 +965,29 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       // chunk k ^ (r % 8)), then one thread stores the tile with TMA.
       const int tile_row0 = (mp * NT + t) * kRowTile;
       const uint32_t sw = static_cast<uint32_t>(rl & 7);
-      if (p.splits == 1) {
+      // A packed call's tile that reaches past the sequence's last node is stored row by
+      // row (a TMA box would overwrite the next sequence's rows).
+      const bool row_store = p.cu != nullptr && node_base + kRowTile / p.G > nt;
+      if (p.splits == 1 && row_store) {
+        uint16_t* orow = p.out + out_row(sp.row0, valid ? i : 0, p.Hq, h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);                 // every lane: the load is warp-wide
+          tmem_ld_wait(o);
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + c * 32 + v * 8) = w;
+            }
+          }
+        }
+      } else if (p.splits == 1) {
         uint8_t* stg = sm + C::kKOff + t * C::kTileBytes;          // [half][128 rows][128 B]
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -963,7 +1010,9 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
         named_bar(1 + t, 128);
         if (rl == 0) {
           for (int hh = 0; hh < C::kHalves; ++hh)
-            tma_store_4d(&omap, stg + hh * C::kHalfBytes, hh * 64, g * p.G, node_base, b);
+            tma_store_4d(&omap, stg + hh * C::kHalfBytes, hh * 64, g * p.G,
+                         p.cu != nullptr ? static_cast<int>(sp.row0) + node_base : node_base,
+                         p.cu != nullptr ? 0 : b);
           bulk_commit();
           bulk_wait_read_all();
         }
@@ -994,7 +1043,8 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
       if (valid) {
         if (p.splits == 1) {
           if (p.lse != nullptr)
-            p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.N + i] = lse2 * 0.69314718055994531f;
+            p.lse[lse_index(p.cu != nullptr, sp.row0, p.T, b, h, i, p.Hq, p.N)] =
+                lse2 * 0.69314718055994531f;
         } else {
           p.ws_lse[((static_cast<size_t>(b) * p.Hkv + g) * p.splits + split) * p.M + r] = lse2;
         }
@@ -1004,7 +1054,7 @@ __global__ void __launch_bounds__(Cfg<NT, D>::kThreads, 1)
     }
   }
 
-  if (p.cluster_merge) merge_cluster<NT, D>(sm, MergeArgs{p.out, p.lse, p.N, p.Hq, p.G, p.M, p.splits}, b, g, mp, split);
+  if (p.cluster_merge) merge_cluster<NT, D>(sm, MergeArgs{p.out, p.lse, p.N, p.Hq, p.G, p.M, p.splits, sp.row0, p.T, sp.rows, p.cu != nullptr}, b, g, mp, split);
 
   tc_fence_before();
   __syncthreads();
@@ -1667,7 +1717,8 @@ __global__ void __launch_bounds__(256)
     tree_attention_combine_kernel(const float* __restrict__ ws_o,
                                   const float* __restrict__ ws_lse, int splits, int N, int Hq,
                                   int Hkv, long long rows, uint16_t* __restrict__ out,
-                                  float* __restrict__ lse) {
+                                  float* __restrict__ lse, const int32_t* __restrict__ cu,
+                                  long long T) {
   constexpr int E = D / 32;
   static_assert(kBatch >= 1 && kBatch <= 16 && (kBatch & (kBatch - 1)) == 0, "batch of splits");
   using VecE = typename std::conditional<E == 4, float4, float2>::type;
@@ -1685,6 +1736,13 @@ __global__ void __launch_bounds__(256)
   const long long M = static_cast<long long>(N) * G;
   const long long r = static_cast<long long>(i) * G + (h % G);
   const long long base = (b * Hkv + g) * splits;       // partial row of split s: (base + s) * M + r
+  // Packed calls: rows of nodes past the sequence's last one do not exist in out and lse.
+  long long row0 = b * N;
+  if (cu != nullptr) {
+    const SeqSpan sp = seq_span(cu, nullptr, static_cast<int>(b), N, T);
+    if (i >= sp.rows) return;
+    row0 = sp.row0;
+  }
   // With more than one batch the running maximum must be known first.
   float mx = -INFINITY;
   if (splits > kBatch) {
@@ -1722,7 +1780,7 @@ __global__ void __launch_bounds__(256)
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint16_t* dst = out + rr * D + lane * E;
+  uint16_t* dst = out + out_row(row0, i, Hq, h) * D + lane * E;
   uint32_t packed[E / 2];
 #pragma unroll
   for (int e = 0; e < E; e += 2) packed[e / 2] = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
@@ -1732,7 +1790,8 @@ __global__ void __launch_bounds__(256)
     *reinterpret_cast<uint32_t*>(dst) = packed[0];
   }
   if (lse != nullptr && lane == 0)
-    lse[(b * Hq + h) * N + i] = (wsum > 0.f ? mx + __log2f(wsum) : -INFINITY) * 0.69314718055994531f;
+    lse[lse_index(cu != nullptr, row0, T, static_cast<int>(b), h, i, Hq, N)] =
+        (wsum > 0.f ? mx + __log2f(wsum) : -INFINITY) * 0.69314718055994531f;
 }
 
 // ------------------------------------------------------------------------ host side
@@ -2008,13 +2067,16 @@ extern "C" size_t jf_tree_attention_workspace_size(int32_t B, int32_t N, int32_t
 
 namespace {
 
+// Packed calls pass cu (cumulative node counts, [B + 1]) and T = total nodes; N is then
+// the largest tree the call may hold.  The others pass nullptr and 0.
 jf_status tree_attention_call(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* block_table, const int32_t* prefix_len,
                               const int32_t* tree_len, const uint64_t* mask, int32_t B,
                               int32_t N, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
                               int32_t max_pages, int32_t num_pages, float scale, void* out,
                               float* lse, void* workspace, size_t workspace_bytes,
-                              int32_t* dev_err, jf_stream_t stream) {
+                              int32_t* dev_err, jf_stream_t stream, const int32_t* cu = nullptr,
+                              int32_t T = 0) {
   using namespace jf;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       prefix_len == nullptr || mask == nullptr || out == nullptr)
@@ -2024,13 +2086,15 @@ jf_status tree_attention_call(const void* q, const void* k_cache, const void* v_
     return JF_ERR_INVALID_ARGUMENT;
   if (!shape_supported(B, N, Hq, Hkv, D, max_pages, page_size)) return JF_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_pages) * kPage >= (1ll << 31)) return JF_ERR_UNSUPPORTED;
+  if (cu != nullptr && T < 1) return JF_ERR_INVALID_ARGUMENT;
+  if (cu != nullptr && static_cast<long long>(T) + N >= (1ll << 31)) return JF_ERR_UNSUPPORTED;
   if (!aligned_to(q, 16) || !aligned_to(k_cache, 16) || !aligned_to(v_cache, 16) ||
       !aligned_to(out, 16) || !aligned_to(mask, 8))
     return JF_ERR_MISALIGNED;
   const int sms = current_sm_count();
   if (sms <= 0) return JF_ERR_CUDA;
   AttnPlan pl;
-  plan_attention(B, N, Hq, Hkv, D, max_pages, sms, &pl, tree_len == nullptr);
+  plan_attention(B, N, Hq, Hkv, D, max_pages, sms, &pl, tree_len == nullptr && cu == nullptr);
   if (pl.ws_bytes > 0) {
     if (workspace == nullptr || workspace_bytes < pl.ws_bytes) return JF_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned_to(workspace, 16)) return JF_ERR_MISALIGNED;
@@ -2040,12 +2104,14 @@ jf_status tree_attention_call(const void* q, const void* k_cache, const void* v_
   std::memset(&om, 0, sizeof(om));
   std::memset(&wm, 0, sizeof(wm));
   {
-    // q and out share one layout: [B][N][Hq][D], 128-row tiles of (node, head-in-group).
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
-                                static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+    // q and out share one layout: [B][N][Hq][D] ([1][T][Hq][D] packed), 128-row tiles of
+    // (node, head-in-group).
+    const cuuint64_t rows_n = cu != nullptr ? static_cast<cuuint64_t>(T) : static_cast<cuuint64_t>(N);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), rows_n,
+                                cu != nullptr ? 1u : static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(Hq) * D * 2,
-                                   static_cast<cuuint64_t>(N) * Hq * D * 2};
+                                   rows_n * Hq * D * 2};
     const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kRowTile / G), 1};
     if (!encode(&qm, q, 4, dims, strides, box)) return JF_ERR_CUDA;
     if (pl.splits == 1 && !encode(&om, out, 4, dims, strides, box)) return JF_ERR_CUDA;
@@ -2077,6 +2143,8 @@ jf_status tree_attention_call(const void* q, const void* k_cache, const void* v_
   prm.block_table = block_table;
   prm.prefix_len = prefix_len;
   prm.tree_len = tree_len;
+  prm.cu = cu;
+  prm.T = cu != nullptr ? T : 0;
   prm.mask = mask;
   prm.out = static_cast<uint16_t*>(out);
   prm.lse = lse;
@@ -2136,9 +2204,10 @@ jf_status tree_attention_call(const void* q, const void* k_cache, const void* v_
     const long long nrows = static_cast<long long>(rows);
     uint16_t* o16 = static_cast<uint16_t*>(out);
     auto pick = [&](auto kern4, auto kern8, auto kern16) {
-      return nsp <= 4   ? cudaLaunchKernelEx(&lc, kern4, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse)
-             : nsp <= 8 ? cudaLaunchKernelEx(&lc, kern8, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse)
-                        : cudaLaunchKernelEx(&lc, kern16, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse);
+      const long long Tl = prm.T;
+      return nsp <= 4   ? cudaLaunchKernelEx(&lc, kern4, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse, cu, Tl)
+             : nsp <= 8 ? cudaLaunchKernelEx(&lc, kern8, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse, cu, Tl)
+                        : cudaLaunchKernelEx(&lc, kern16, wso, wsl, nsp, N, Hq, Hkv, nrows, o16, lse, cu, Tl);
     };
     const cudaError_t e =
         D == 128 ? pick(tree_attention_combine_kernel<128, 4>, tree_attention_combine_kernel<128, 8>,
@@ -2178,6 +2247,21 @@ extern "C" jf_status jf_tree_attention_ragged(const void* q, const void* k_cache
   return tree_attention_call(q, k_cache, v_cache, block_table, prefix_len, tree_len, mask, B, N,
                              Hq, Hkv, D, page_size, max_pages, num_pages, scale, out, lse,
                              workspace, workspace_bytes, dev_err, stream);
+}
+
+extern "C" jf_status jf_tree_attention_packed(const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_table,
+                                              const int32_t* prefix_len, const int32_t* cu_seqlens,
+                                              const uint64_t* mask, int32_t B, int32_t N_max,
+                                              int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                                              int32_t page_size, int32_t max_pages,
+                                              int32_t num_pages, float scale, void* out,
+                                              float* lse, void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_err, jf_stream_t stream) {
+  if (cu_seqlens == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return tree_attention_call(q, k_cache, v_cache, block_table, prefix_len, nullptr, mask, B, N_max,
+                             Hq, Hkv, D, page_size, max_pages, num_pages, scale, out, lse,
+                             workspace, workspace_bytes, dev_err, stream, cu_seqlens, T);
 }
 
 extern "C" jf_status jf_debug_set_wait_limit_ns(uint64_t limit_ns, int32_t withhold_arrivals) {

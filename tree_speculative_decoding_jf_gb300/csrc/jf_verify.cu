@@ -156,8 +156,8 @@ inline int walk_threads(int N) { return std::min(kWalkThreads, std::max(128, (N 
 __global__ void __launch_bounds__(kWalkThreads)
     tree_walk_kernel(const uint64_t* __restrict__ part, int chunks,
                      const int32_t* __restrict__ draft, const int32_t* __restrict__ parent,
-                     const int32_t* __restrict__ tree_len, int N, int V,
-                     int32_t* __restrict__ argmax_out,
+                     const int32_t* __restrict__ tree_len, const int32_t* __restrict__ cu,
+                     long long T, int N, int V, int32_t* __restrict__ argmax_out,
                      int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                      int32_t* __restrict__ bonus, int32_t* dev_err) {
   extern __shared__ uint64_t sm64[];
@@ -175,14 +175,13 @@ __global__ void __launch_bounds__(kWalkThreads)
 
   grid_dependency_wait();
   const int b = blockIdx.x;
-  const size_t rb = static_cast<size_t>(b) * N;
-  // Ragged calls: nodes >= nt are padding, never read and never accepted.
-  int nt = N;
-  if (tree_len != nullptr) {
-    const int raw = tree_len[b];
-    nt = max(1, min(raw, N));
-    if (raw != nt && threadIdx.x == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
-  }
+  // Ragged calls: nodes >= nt are padding, never read and never accepted.  Packed calls:
+  // the sequence's rows start at cu[b] and it owns no padding rows.
+  const SeqSpan sp = seq_span(cu, tree_len, b, N, T);
+  if (!sp.ok && threadIdx.x == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
+  const size_t rb = static_cast<size_t>(sp.row0);
+  const int nt = sp.n;
+  const int rows = sp.rows;
   // The block is sized to the tree (threadIdx.x + k * blockDim.x covers every node for
   // k < kPer).  Parents and drafts are requested first and stay in flight while the
   // chunk keys are merged, so both arrive in one memory round trip.
@@ -204,7 +203,7 @@ __global__ void __launch_bounds__(kWalkThreads)
     // Keys are fetched kKeyBatch per thread before any is merged, so a block of 128
     // threads has 1024 of them in flight per round trip.
     constexpr int kKeyBatch = 8;
-    const int total = N * chunks;
+    const int total = rows * chunks;
     const uint64_t* pk = part + rb * chunks;
     for (int e0 = threadIdx.x; e0 < total; e0 += blockDim.x * kKeyBatch) {
       uint64_t kv[kKeyBatch];
@@ -242,7 +241,7 @@ __global__ void __launch_bounds__(kWalkThreads)
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     const int am = static_cast<int>(~static_cast<uint32_t>(s_best[i] & 0xFFFFFFFFull));
     s_am[i] = am;
-    if (argmax_out != nullptr) argmax_out[rb + i] = am;
+    if (argmax_out != nullptr && i < rows) argmax_out[rb + i] = am;
   }
   bad_parent = __syncthreads_or(bad_parent);
   bad_token = __syncthreads_or(bad_token);
@@ -310,7 +309,8 @@ __global__ void __launch_bounds__(kWalkThreads)
   }
   __syncthreads();
   const int n = s_len;
-  for (int k = threadIdx.x; k < N; k += blockDim.x) path[rb + k] = k <= n ? s_path[k] : -1;
+  for (int k = threadIdx.x; k < N; k += blockDim.x)
+    path[static_cast<size_t>(b) * N + k] = k <= n ? s_path[k] : -1;
   grid_dependents_launch();
 }
 
@@ -332,7 +332,8 @@ inline bool small_walk_fits(int N, int chunks) {
 __global__ void __launch_bounds__(32)
     tree_walk_small_kernel(const uint64_t* __restrict__ part, int chunks,
                            const int32_t* __restrict__ draft, const int32_t* __restrict__ parent,
-                           const int32_t* __restrict__ tree_len, int N, int V,
+                           const int32_t* __restrict__ tree_len, const int32_t* __restrict__ cu,
+                           long long T, int N, int V,
                            int32_t* __restrict__ argmax_out, int32_t* __restrict__ accept_len,
                            int32_t* __restrict__ path, int32_t* __restrict__ bonus,
                            int32_t* dev_err) {
@@ -342,13 +343,11 @@ __global__ void __launch_bounds__(32)
   __shared__ uint32_t s_key[kSmallWalkNodes];
   grid_dependency_wait();
   const int b = blockIdx.x, lane = threadIdx.x;
-  const size_t rb = static_cast<size_t>(b) * N;
-  int nt = N;
-  if (tree_len != nullptr) {
-    const int raw = tree_len[b];
-    nt = max(1, min(raw, N));
-    if (raw != nt && lane == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
-  }
+  const SeqSpan sp = seq_span(cu, tree_len, b, N, T);
+  if (!sp.ok && lane == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
+  const size_t rb = static_cast<size_t>(sp.row0);
+  const int nt = sp.n;
+  const int rows = sp.rows;
   const bool two = N > 32;                          // two rows per lane
   int r_par[2] = {-1, -1}, r_draft[2] = {-1, -1};
 #pragma unroll
@@ -365,7 +364,7 @@ __global__ void __launch_bounds__(32)
   for (int u = 0; u < kSmallWalkKeys; ++u) {
     const int i = two ? lane + 32 * (u / H) : lane;
     const int c = two ? u % H : u;
-    kv[u] = (i < N && c < chunks) ? part[(rb + i) * chunks + c] : 0ull;
+    kv[u] = (i < rows && c < chunks) ? part[(rb + i) * chunks + c] : 0ull;
   }
   uint64_t best[2] = {0ull, 0ull};
 #pragma unroll
@@ -380,7 +379,7 @@ __global__ void __launch_bounds__(32)
     if (i < N) {
       const int am = static_cast<int>(~static_cast<uint32_t>(best[k] & 0xFFFFFFFFull));
       s_am[i] = am;
-      if (argmax_out != nullptr) argmax_out[rb + i] = am;
+      if (argmax_out != nullptr && i < rows) argmax_out[rb + i] = am;
       int p = i < nt ? r_par[k] : -1;
       const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
       if (!ok && i < nt) bad_parent = 1;
@@ -464,7 +463,7 @@ __global__ void __launch_bounds__(32)
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int i = lane + 32 * k;
-    if (i < N) path[rb + i] = i <= n ? s_path[i] : -1;
+    if (i < N) path[static_cast<size_t>(b) * N + i] = i <= n ? s_path[i] : -1;
   }
   grid_dependents_launch();
 }
@@ -474,10 +473,10 @@ struct VerifyPlan {
   int chunk_len;
 };
 
-bool plan_verify(int B, int N, int V, VerifyPlan* p) {
-  if (B < 1 || N < 1 || N > JF_MAX_NODES || V < 1) return false;
+// Chunks per logit row for `rows` rows of V logits.
+bool plan_verify_rows(long long rows, int V, VerifyPlan* p) {
+  if (rows < 1 || V < 1) return false;
   const int sms = current_sm_count() > 0 ? current_sm_count() : 148;
-  const long long rows = static_cast<long long>(B) * N;
   const long long target = static_cast<long long>(sms) * 4;   // CTAs to keep HBM busy
   long long c = (target + rows - 1) / rows;
   const long long cmax = std::max<long long>(1, (V + kMinChunkElems - 1) / kMinChunkElems);
@@ -490,16 +489,23 @@ bool plan_verify(int B, int N, int V, VerifyPlan* p) {
   return true;
 }
 
+bool plan_verify(int B, int N, int V, VerifyPlan* p) {
+  if (B < 1 || N < 1 || N > JF_MAX_NODES || V < 1) return false;
+  return plan_verify_rows(static_cast<long long>(B) * N, V, p);
+}
+
 // Launches the walk over the argmax keys in `part`: one warp per sequence for small trees,
 // else the block-wide walk.  Both are programmatic dependents of the argmax grid.
+// Packed calls pass cu (cumulative node counts) and T = cu[B]; others nullptr and 0.
 jf_status launch_walk(const uint64_t* part, int chunks, const int32_t* draft,
                       const int32_t* parent, const int32_t* tree_len, int B, int N, int V,
                       int32_t* argmax, int32_t* accept_len, int32_t* path, int32_t* bonus,
-                      int32_t* dev_err, cudaStream_t s) {
+                      int32_t* dev_err, cudaStream_t s, const int32_t* cu = nullptr,
+                      long long T = 0) {
   cudaError_t e;
   if (small_walk_fits(N, chunks)) {
     e = launch_pdl(tree_walk_small_kernel, dim3(B), dim3(32), 0, s, part, chunks, draft, parent,
-                   tree_len, N, V, argmax, accept_len, path, bonus, dev_err);
+                   tree_len, cu, T, N, V, argmax, accept_len, path, bonus, dev_err);
   } else {
     const size_t smem = static_cast<size_t>(N) * (7 * sizeof(int32_t) + sizeof(uint64_t));
     if (smem > 48 * 1024 &&
@@ -507,7 +513,7 @@ jf_status launch_walk(const uint64_t* part, int chunks, const int32_t* draft,
                              static_cast<int>(smem)) != cudaSuccess)
       return JF_ERR_CUDA;
     e = launch_pdl(tree_walk_kernel, dim3(B), dim3(walk_threads(N)), smem, s, part, chunks, draft,
-                   parent, tree_len, N, V, argmax, accept_len, path, bonus, dev_err);
+                   parent, tree_len, cu, T, N, V, argmax, accept_len, path, bonus, dev_err);
   }
   return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
 }
@@ -531,26 +537,29 @@ extern "C" size_t jf_tree_verify_workspace_size(int32_t B, int32_t N, int32_t V)
 
 namespace {
 
+// Packed calls (cu != nullptr) hold T = cu[B] logit rows; the others B * N.
 jf_status tree_verify_call(const void* logits, int32_t dtype, const int32_t* draft,
-                           const int32_t* parent, const int32_t* tree_len, int32_t B, int32_t N,
-                           int32_t V, int32_t* argmax, int32_t* accept_len, int32_t* path,
-                           int32_t* bonus, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_err, jf_stream_t stream) {
+                           const int32_t* parent, const int32_t* tree_len, const int32_t* cu,
+                           int32_t T, int32_t B, int32_t N, int32_t V, int32_t* argmax,
+                           int32_t* accept_len, int32_t* path, int32_t* bonus, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_err, jf_stream_t stream) {
   if (logits == nullptr || draft == nullptr || parent == nullptr || accept_len == nullptr ||
       path == nullptr || bonus == nullptr || workspace == nullptr)
     return JF_ERR_INVALID_ARGUMENT;
   if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
   if (B < 1 || N < 1 || V < 1) return JF_ERR_INVALID_ARGUMENT;
+  if (cu != nullptr && T < 1) return JF_ERR_INVALID_ARGUMENT;
   if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  const long long rows = cu != nullptr ? static_cast<long long>(T) : static_cast<long long>(B) * N;
   jf::VerifyPlan p;
-  if (!jf::plan_verify(B, N, V, &p)) return JF_ERR_UNSUPPORTED;
-  const size_t need = static_cast<size_t>(B) * N * p.chunks * sizeof(uint64_t);
+  if (!jf::plan_verify_rows(rows, V, &p)) return JF_ERR_UNSUPPORTED;
+  const size_t need = static_cast<size_t>(rows) * p.chunks * sizeof(uint64_t);
   if (workspace_bytes < need) return JF_ERR_WORKSPACE_TOO_SMALL;
   if (!jf::aligned_to(workspace, 8)) return JF_ERR_MISALIGNED;
   if (!jf::aligned_to(logits, dtype == JF_DTYPE_BF16 ? 2 : 4)) return JF_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint64_t* part = static_cast<uint64_t*>(workspace);
-  const long long grid = static_cast<long long>(B) * N * p.chunks;
+  const long long grid = rows * p.chunks;
   if (grid > 0x7FFFFFFFll) return JF_ERR_UNSUPPORTED;
   const long long Vl = V;
   const cudaError_t ea =
@@ -563,7 +572,7 @@ jf_status tree_verify_call(const void* logits, int32_t dtype, const int32_t* dra
                            p.chunks, p.chunk_len, part, 0);
   if (ea != cudaSuccess) return JF_ERR_CUDA;
   return jf::launch_walk(part, p.chunks, draft, parent, tree_len, B, N, V, argmax, accept_len, path,
-                         bonus, dev_err, s);
+                         bonus, dev_err, s, cu, T);
 }
 
 }  // namespace
@@ -573,8 +582,8 @@ extern "C" jf_status jf_tree_verify(const void* logits, int32_t dtype, const int
                                     int32_t* argmax, int32_t* accept_len, int32_t* path,
                                     int32_t* bonus, void* workspace, size_t workspace_bytes,
                                     int32_t* dev_err, jf_stream_t stream) {
-  return tree_verify_call(logits, dtype, draft, parent, nullptr, B, N, V, argmax, accept_len, path,
-                          bonus, workspace, workspace_bytes, dev_err, stream);
+  return tree_verify_call(logits, dtype, draft, parent, nullptr, nullptr, 0, B, N, V, argmax,
+                          accept_len, path, bonus, workspace, workspace_bytes, dev_err, stream);
 }
 
 extern "C" jf_status jf_tree_verify_ragged(const void* logits, int32_t dtype, const int32_t* draft,
@@ -584,8 +593,27 @@ extern "C" jf_status jf_tree_verify_ragged(const void* logits, int32_t dtype, co
                                            void* workspace, size_t workspace_bytes,
                                            int32_t* dev_err, jf_stream_t stream) {
   if (tree_len == nullptr) return JF_ERR_INVALID_ARGUMENT;
-  return tree_verify_call(logits, dtype, draft, parent, tree_len, B, N, V, argmax, accept_len,
-                          path, bonus, workspace, workspace_bytes, dev_err, stream);
+  return tree_verify_call(logits, dtype, draft, parent, tree_len, nullptr, 0, B, N, V, argmax,
+                          accept_len, path, bonus, workspace, workspace_bytes, dev_err, stream);
+}
+
+extern "C" size_t jf_tree_verify_packed_workspace_size(int32_t T, int32_t V) {
+  jf::VerifyPlan p;
+  if (T < 1 || !jf::plan_verify_rows(T, V, &p)) return static_cast<size_t>(-1);
+  return static_cast<size_t>(T) * p.chunks * sizeof(uint64_t);
+}
+
+extern "C" jf_status jf_tree_verify_packed(const void* logits, int32_t dtype, const int32_t* draft,
+                                           const int32_t* parent, const int32_t* cu_seqlens,
+                                           int32_t B, int32_t N_max, int32_t T, int32_t V,
+                                           int32_t* argmax, int32_t* accept_len, int32_t* path,
+                                           int32_t* bonus, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_err,
+                                           jf_stream_t stream) {
+  if (cu_seqlens == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return tree_verify_call(logits, dtype, draft, parent, nullptr, cu_seqlens, T, B, N_max, V,
+                          argmax, accept_len, path, bonus, workspace, workspace_bytes, dev_err,
+                          stream);
 }
 
 // ------------------------------------------------------------------------ allocation-free

@@ -82,6 +82,16 @@ def _load():
     lib.jf_tree_verify_from_keys.argtypes = [P, i32, i32, P, P, i32, i32, i32, P, P, P, P, P, sz,
                                              P, P]
     lib.jf_tree_verify_from_keys.restype = ctypes.c_int
+    lib.jf_build_tree_mask_packed.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P]
+    lib.jf_build_tree_mask_packed.restype = ctypes.c_int
+    lib.jf_tree_attention_packed.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                             i32, i32, i32, f32, P, P, P, sz, P, P]
+    lib.jf_tree_attention_packed.restype = ctypes.c_int
+    lib.jf_tree_verify_packed_workspace_size.argtypes = [i32, i32]
+    lib.jf_tree_verify_packed_workspace_size.restype = sz
+    lib.jf_tree_verify_packed.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz,
+                                          P, P]
+    lib.jf_tree_verify_packed.restype = ctypes.c_int
     return lib
 
 
@@ -379,6 +389,98 @@ def jf_tree_verify_from_keys(keys, V, draft, parent, accept_len, path, bonus, wo
     _check("jf_tree_verify_from_keys", _lib.jf_tree_verify_from_keys(
         _ptr(keys), S, chunks, _ptr(draft), _ptr(parent), B, N, int(V), _ptr(argmax),
         _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(workspace), workspace.numel(),
+        _ptr(dev_err), _stream(stream)))
+
+
+def jf_build_tree_mask_packed(parent, prefix_len, cu_seqlens, N_max, mask, depth=None, pos=None,
+                              dev_err=None, stream=None) -> None:
+    """Packed trees: parent int32 [T] (ids within each sequence), cu_seqlens int32 [B + 1],
+    mask int64 [T][ceil(N_max / 64)] (see include/jf.h)."""
+    (T,) = parent.shape
+    B = cu_seqlens.shape[0] - 1
+    W = (N_max + 63) // 64
+    _need(parent, "parent", torch.int32)
+    _need(prefix_len, "prefix_len", torch.int32, (B,))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (B + 1,))
+    _need(mask, "mask", torch.int64, (T, W))
+    for name, t in (("depth", depth), ("pos", pos)):
+        if t is not None:
+            _need(t, name, torch.int32, (T,))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_build_tree_mask_packed", _lib.jf_build_tree_mask_packed(
+        _ptr(parent), _ptr(prefix_len), _ptr(cu_seqlens), B, N_max, T, _ptr(mask), _ptr(depth),
+        _ptr(pos), _ptr(dev_err), _stream(stream)))
+
+
+def jf_tree_attention_packed(q, k_cache, v_cache, block_table, prefix_len, cu_seqlens, N_max,
+                             mask, scale, out, lse=None, workspace=None, dev_err=None,
+                             stream=None) -> None:
+    """Packed trees: q and out bf16 [T][Hq][D], mask int64 [T][W], lse float32 [Hq][T];
+    the workspace is sized by jf_tree_attention_workspace_size with N = N_max."""
+    T, Hq, D = q.shape
+    num_pages, page, Hkv, D2 = k_cache.shape
+    B = cu_seqlens.shape[0] - 1
+    max_pages = block_table.shape[1]
+    W = (N_max + 63) // 64
+    _need(q, "q", torch.bfloat16)
+    _need(k_cache, "k_cache", torch.bfloat16)
+    _need(v_cache, "v_cache", torch.bfloat16, k_cache.shape)
+    _need(block_table, "block_table", torch.int32, (B, max_pages))
+    _need(prefix_len, "prefix_len", torch.int32, (B,))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (B + 1,))
+    _need(mask, "mask", torch.int64, (T, W))
+    _need(out, "out", torch.bfloat16, (T, Hq, D))
+    if D2 != D:
+        raise ValueError("q and k_cache head dims differ")
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (Hq, T))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    ws_bytes = 0
+    if workspace is not None:
+        if workspace.device.type != "cuda" or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check("jf_tree_attention_packed", _lib.jf_tree_attention_packed(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(prefix_len),
+        _ptr(cu_seqlens), _ptr(mask), B, N_max, T, Hq, Hkv, D, page, max_pages, num_pages,
+        float(scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(dev_err),
+        _stream(stream)))
+
+
+def jf_tree_verify_packed_workspace_size(T, V) -> int:
+    n = _lib.jf_tree_verify_packed_workspace_size(T, V)
+    if n == SIZE_MAX:
+        raise JFError("jf_tree_verify_packed_workspace_size", 3)
+    return int(n)
+
+
+def jf_tree_verify_packed(logits, draft, parent, cu_seqlens, N_max, accept_len, path, bonus,
+                          argmax=None, workspace=None, dev_err=None, stream=None) -> None:
+    """Packed trees: logits [T][V] (bf16 or f32), draft/parent/argmax int32 [T], path int32
+    [B][N_max]; the workspace is sized by jf_tree_verify_packed_workspace_size(T, V)."""
+    T, V = logits.shape
+    B = cu_seqlens.shape[0] - 1
+    if logits.dtype == torch.bfloat16:
+        dt = JF_DTYPE_BF16
+    elif logits.dtype == torch.float32:
+        dt = JF_DTYPE_F32
+    else:
+        raise TypeError("logits must be bfloat16 or float32")
+    _need(logits, "logits", logits.dtype)
+    for name, t, shape in (("draft", draft, (T,)), ("parent", parent, (T,)),
+                           ("cu_seqlens", cu_seqlens, (B + 1,)), ("accept_len", accept_len, (B,)),
+                           ("path", path, (B, N_max)), ("bonus", bonus, (B,))):
+        _need(t, name, torch.int32, shape)
+    if argmax is not None:
+        _need(argmax, "argmax", torch.int32, (T,))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("jf_tree_verify_packed", _lib.jf_tree_verify_packed(
+        _ptr(logits), dt, _ptr(draft), _ptr(parent), _ptr(cu_seqlens), B, N_max, T, V,
+        _ptr(argmax), _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(workspace), ws_bytes,
         _ptr(dev_err), _stream(stream)))
 
 
