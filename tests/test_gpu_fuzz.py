@@ -162,3 +162,64 @@ def test_draft_tree_random_shapes(jf, case):
     sigma = float(rng.choice([0.5, 3.0, 8.0]))
     x = wl.draft_logits(B, Dmax, V, sigma=sigma, dtype=dtype, seed=600 + case)
     check(jf, x, dtype, K, N)
+
+
+# ----------------------------------------------------------------------------- packed
+
+N_PACKED = 12 * SCALE
+
+
+@pytest.mark.parametrize("case", range(N_PACKED))
+def test_packed_attention_random_shapes(jf, case):
+    """Random shapes and tree sizes in the packed (cu_seqlens) layout: masks, outputs and
+    LSEs equal the ragged call's bit for bit, rows against the oracle's slices."""
+    from test_gpu_packed import ragged_vs_packed_attention
+    from test_gpu_ragged import check_rows, poison_padding
+    w = draw(200 + case)
+    rng = np.random.default_rng(7500 + case)
+    tree_len = [int(x) for x in rng.integers(1, w.N + 1, w.B)]
+    w = poison_padding(w, tree_len)
+    out, lse = ragged_vs_packed_attention(jf, w, tree_len)
+    check_rows(w, tree_len, out, lse, rows_per_seq=24 if w.B > 8 else 64, seed=case)
+
+
+# ----------------------------------------------------------------------------- vocabulary shards
+
+N_SHARD = 12 * SCALE
+
+
+@pytest.mark.parametrize("case", range(N_SHARD))
+def test_sharded_verify_random_shapes(jf, case):
+    """Greedy verification with the vocabulary cut into 2-8 random ranges (keys per range,
+    merged walk): argmax, accepted length, path and bonus bit-exact against the oracle."""
+    from test_gpu_shard_verify import cuts, sharded
+    rng = np.random.default_rng(6000 + case)
+    V = int(rng.choice([9, 33, 1000, 4097, 32001, 151936]))
+    N = int(rng.choice([1, 2, 16, 64, 100, 256]))
+    B = int(rng.choice([1, 2, 5, 16]))
+    while B * N * V > 40_000_000:
+        if B > 1:
+            B //= 2
+        else:
+            N = max(1, N // 2)
+    S = int(min(rng.integers(2, 9), V))
+    width = int(rng.integers(1, 10))
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - width), i) for i in range(1, N)],
+                                np.int32) for _ in range(B)])
+    dtype = str(rng.choice(["bf16", "f32"]))
+    w = wl.make_workload(f"sfuzz{case}", B, N, 1, 1, 64, V, 8, tree="chain", parent=parent,
+                         logits_dtype=dtype, forcing="half", seed=600 + case)
+    lg = (torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16) if dtype == "bf16"
+          else torch.from_numpy(w.logits)).cuda()
+    ranges = cuts(V, S, rng, ragged=bool(rng.random() < 0.7))
+    keys, _ = sharded(jf, lg, ranges, rng.permutation(len(ranges)).tolist())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    am, acc, path, bonus = jf.tree_verify_from_keys(keys, V, torch.from_numpy(w.draft).cuda(),
+                                                    torch.from_numpy(w.parent).cuda(), dev_err=err)
+    ram = oracle.argmax(w.logits, dtype)
+    racc, rpath, rbonus = oracle.tree_walk(ram, w.draft, w.parent)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert (am.cpu().numpy() == ram).all()
+    assert (acc.cpu().numpy() == racc).all() and (path.cpu().numpy() == rpath).all()
+    assert (bonus.cpu().numpy() == rbonus).all()
