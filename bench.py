@@ -57,10 +57,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture of the current kernel exists for that workload); the capture commands are in
 # the profile summaries.
 NCU_TRAFFIC_BYTES = {
-    "c5_qwen3_30b_b8_tree256_32k": 569516032 + 29585664 + 38086400 + 2560,
-    "c3_qwen3_8b_tree256": 20030464 + 0 + 16926464 + 0,
-    "c4_qwen3_8b_b32_tree64_paged": 569020672 + 10700032,
-    "c2_qwen3_8b_chain16": 8671488 + 2403840,
+    "c5_qwen3_30b_b8_tree256_32k": 569551872 + 29477376 + 38097920 + 0,
+    "c3_qwen3_8b_tree256": 20050944 + 0 + 16927488 + 0,
+    "c4_qwen3_8b_b32_tree64_paged": 569012992 + 6938880,
+    "c2_qwen3_8b_chain16": 8674304 + 0 + 2405120 + 0,
 }
 
 
