@@ -398,6 +398,32 @@ jf_status jf_tree_verify_packed(const void* logits, int32_t dtype, const int32_t
                                 void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                 jf_stream_t stream);
 
+/*
+ * Lossless verification of ragged trees: jf_tree_verify_sampled with per-sequence tree
+ * sizes, padded (tree_len [B], as the _ragged calls) or packed (cu_seqlens [B + 1], as the
+ * _packed calls; uniform then float32 [T], one draw per packed node).  Padding nodes are
+ * never read and never accepted; every sequence's accept_len, path and bonus are what
+ * jf_tree_verify_sampled gives on the sequence's first n_b nodes alone, with the same
+ * random numbers.  Workspace: jf_tree_verify_workspace_size(B, N, V) for the ragged call,
+ * jf_tree_verify_packed_workspace_size(T, V) for the packed one.  A tree_len entry outside
+ * [1, N] is reported and clamped; a bad packed span is reported and its sequence gets
+ * accept_len 0, path (0, then -1) and bonus -1 without any of its rows being read.
+ */
+jf_status jf_tree_verify_sampled_ragged(const void* logits, int32_t dtype, const int32_t* draft,
+                                        const int32_t* parent, const int32_t* tree_len,
+                                        const float* uniform, const float* bonus_uniform,
+                                        float temperature, int32_t B, int32_t N, int32_t V,
+                                        int32_t* accept_len, int32_t* path, int32_t* bonus,
+                                        void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_err, jf_stream_t stream);
+jf_status jf_tree_verify_sampled_packed(const void* logits, int32_t dtype, const int32_t* draft,
+                                        const int32_t* parent, const int32_t* cu_seqlens,
+                                        const float* uniform, const float* bonus_uniform,
+                                        float temperature, int32_t B, int32_t N_max, int32_t T,
+                                        int32_t V, int32_t* accept_len, int32_t* path,
+                                        int32_t* bonus, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_err, jf_stream_t stream);
+
 /* ---------------------------------------------------------------- before verification
  * jf_build_draft_tree -- builds the draft tree from per-depth draft logits.  JetFlow
  * explainer ("JetFlow: Breaking the Scaling Ceiling of Speculative Decoding with Parallel

@@ -165,3 +165,20 @@ def test_packed_calls_validate_host_arguments_without_gpu(lib):
                                      fake, fake, 1 << 20, None, None) == 1     # no cu_seqlens
     assert lib.jf_tree_verify_packed(fake, 0, fake, fake, fake, 2, 16, 0, 100, None, fake, fake,
                                      fake, fake, 1 << 20, None, None) == 1     # T = 0
+
+
+def test_sampled_ragged_and_packed_calls_validate_host_arguments_without_gpu(lib):
+    P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: every call below fails early
+    lib.jf_tree_verify_sampled_ragged.argtypes = [P, i32, P, P, P, P, P, f32, i32, i32, i32, P, P,
+                                                  P, P, sz, P, P]
+    assert lib.jf_tree_verify_sampled_ragged(fake, 0, fake, fake, None, fake, fake, 1.0, 2, 8, 100,
+                                             fake, fake, fake, fake, 1 << 20, None, None) == 1
+    lib.jf_tree_verify_sampled_packed.argtypes = [P, i32, P, P, P, P, P, f32, i32, i32, i32, i32,
+                                                  P, P, P, P, sz, P, P]
+    assert lib.jf_tree_verify_sampled_packed(fake, 0, fake, fake, None, fake, fake, 1.0, 2, 8, 10,
+                                             100, fake, fake, fake, fake, 1 << 20, None, None) == 1
+    assert lib.jf_tree_verify_sampled_packed(fake, 0, fake, fake, fake, fake, fake, 1.0, 2, 8, 0,
+                                             100, fake, fake, fake, fake, 1 << 20, None, None) == 1
+    assert lib.jf_tree_verify_sampled_packed(fake, 0, fake, fake, fake, fake, fake, 0.0, 2, 8, 10,
+                                             100, fake, fake, fake, fake, 1 << 20, None, None) == 1

@@ -187,3 +187,82 @@ def test_reports_bad_tokens(jf):
                            u, torch.full((1,), 0.5, device="cuda"), 1.0, dev_err=err)
     torch.cuda.synchronize()
     assert err.item() == jf.DEVERR_BAD_TOKEN
+
+
+# ----------------------------------------------------------------------------- ragged / packed
+
+@pytest.mark.parametrize("V,dtype,T", [(1000, "f32", 1.0), (151936, "bf16", 0.7), (4097, "bf16", 1.3)])
+def test_ragged_and_packed_equal_the_per_sequence_calls(jf, V, dtype, T):
+    """Per-sequence tree sizes: the ragged call (padded arrays, hostile padding) and the
+    packed call (cu_seqlens) give every sequence exactly what jf_tree_verify_sampled gives
+    on that sequence's first n_b nodes with the same random numbers (same arithmetic per
+    row, so bit for bit); the fixed-size call is itself checked against the oracle above."""
+    B, N = 5, 40
+    w = wl.make_workload(f"sr{V}", B, N, 1, 1, 64, V, 8, tree="random_depth_limited",
+                         logits_dtype=dtype, forcing="half", seed=V % 97)
+    tree_len = [1, 2, 17, 39, 40]
+    u, bu = wl.sampling_uniforms(B, N, 5)
+    draft, parent = w.draft.copy(), w.parent.copy()
+    uni = u.copy()
+    for b, n in enumerate(tree_len):             # padding: out of range, never read
+        draft[b, n:] = -3
+        parent[b, n:] = 10 ** 6
+        uni[b, n:] = np.nan
+    lg = logits_tensor(w.logits, dtype)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    path = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    bonus = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(jf.jf_tree_verify_workspace_size(B, N, V), dtype=torch.uint8, device="cuda")
+    jf.jf_tree_verify_sampled_ragged(lg, dev(draft), dev(parent), dev(np.array(tree_len, np.int32)),
+                                     dev(uni), dev(bu), T, acc, path, bonus, ws, err)
+    # packed
+    cu = np.concatenate([[0], np.cumsum(tree_len)]).astype(np.int32)
+    Tn = int(cu[-1])
+    pk = lambda a: np.ascontiguousarray(np.concatenate([a[b, :n] for b, n in enumerate(tree_len)]))  # noqa: E731
+    acc_p = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    path_p = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
+    bonus_p = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    ws_p = torch.empty(jf.jf_tree_verify_packed_workspace_size(Tn, V), dtype=torch.uint8,
+                       device="cuda")
+    jf.jf_tree_verify_sampled_packed(logits_tensor(pk(w.logits), dtype), dev(pk(draft)),
+                                     dev(pk(parent)), dev(cu), N, dev(pk(uni)), dev(bu), T, acc_p,
+                                     path_p, bonus_p, ws_p, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(acc, acc_p) and torch.equal(path, path_p) and torch.equal(bonus, bonus_p)
+    acc, path, bonus = acc.cpu().numpy(), path.cpu().numpy(), bonus.cpu().numpy()
+    for b, n in enumerate(tree_len):
+        r_acc, r_path, r_bonus = jf.tree_verify_sampled(
+            logits_tensor(w.logits[b:b + 1, :n], dtype), dev(draft[b:b + 1, :n]),
+            dev(parent[b:b + 1, :n]), dev(u[b:b + 1, :n]), dev(bu[b:b + 1]), T)
+        assert acc[b] == r_acc.item() and bonus[b] == r_bonus.item(), b
+        assert (path[b, :n] == r_path.cpu().numpy()[0]).all() and (path[b, n:] == -1).all()
+    assert acc.max() >= 1
+
+
+def test_packed_bad_span_is_reported_and_not_read(jf):
+    B, N, V = 2, 8, 300
+    w = wl.make_workload("sbad", B, N, 1, 1, 64, V, 8, tree="random_depth_limited",
+                         logits_dtype="f32", forcing="half", seed=3)
+    cu = torch.tensor([0, 9, 11], dtype=torch.int32, device="cuda")     # 9 > N_max: bad
+    Tn = 11
+    lg = torch.from_numpy(np.ascontiguousarray(w.logits.reshape(B * N, V)[:Tn])).cuda()
+    u, bu = wl.sampling_uniforms(B, N, 1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    path = torch.full((B, N), -7, dtype=torch.int32, device="cuda")
+    bonus = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    par = np.concatenate([w.parent[0], [0], w.parent[1, :2]]).astype(np.int32)
+    dr = np.concatenate([w.draft[0], [0], w.draft[1, :2]]).astype(np.int32)
+    ws = torch.empty(jf.jf_tree_verify_packed_workspace_size(Tn, V), dtype=torch.uint8,
+                     device="cuda")
+    jf.jf_tree_verify_sampled_packed(lg, torch.from_numpy(dr).cuda(), torch.from_numpy(par).cuda(),
+                                     cu, N, torch.from_numpy(u.reshape(-1)[:Tn].copy()).cuda(),
+                                     torch.from_numpy(bu).cuda(), 1.0, acc, path, bonus, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() & jf.DEVERR_BAD_TREE_LEN
+    assert acc[0].item() == 0 and bonus[0].item() == -1
+    assert path[0, 0].item() == 0 and (path[0, 1:] == -1).all()
+    assert 0 <= bonus[1].item() < V and path[1, 0].item() == 0

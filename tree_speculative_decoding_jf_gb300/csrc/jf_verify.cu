@@ -600,7 +600,8 @@ extern "C" jf_status jf_tree_verify_ragged(const void* logits, int32_t dtype, co
 extern "C" size_t jf_tree_verify_packed_workspace_size(int32_t T, int32_t V) {
   jf::VerifyPlan p;
   if (T < 1 || !jf::plan_verify_rows(T, V, &p)) return static_cast<size_t>(-1);
-  return static_cast<size_t>(T) * p.chunks * sizeof(uint64_t);
+  return std::max(static_cast<size_t>(T) * p.chunks * sizeof(uint64_t),              // argmax keys
+                  static_cast<size_t>(T) * jf::sampled_chunks(V) * sizeof(float2));  // sampling stats
 }
 
 extern "C" jf_status jf_tree_verify_packed(const void* logits, int32_t dtype, const int32_t* draft,
@@ -982,7 +983,9 @@ __global__ void __launch_bounds__(kSampleThreads, 1)
                         const int32_t* __restrict__ parent, const float* __restrict__ uniform,
                         const float* __restrict__ bonus_uniform, float temperature, int N,
                         long long V, int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
-                        int32_t* __restrict__ bonus, int32_t* dev_err) {
+                        int32_t* __restrict__ bonus, int32_t* dev_err,
+                        const int32_t* __restrict__ tree_len, const int32_t* __restrict__ cu,
+                        long long total_rows) {
   extern __shared__ __align__(16) int32_t smw[];
   T* s_cv = reinterpret_cast<T*>(smw);  // [kSampleChunk] the bonus chunk's logits
   int32_t* s_par = smw + kSampleChunk * sizeof(T) / sizeof(int32_t);   // [N] parent (malformed -> -1)
@@ -1006,11 +1009,31 @@ __global__ void __launch_bounds__(kSampleThreads, 1)
   grid_dependency_wait();
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t rb = static_cast<size_t>(b) * N;
+  // Ragged calls: nodes >= nt are padding (never read, never anyone's child).  Packed
+  // calls: the sequence's rows start at cu[b]; a bad span is reported and not read.
+  const SeqSpan sp = seq_span(cu, tree_len, b, N, total_rows);
+  if (!sp.ok && threadIdx.x == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
+  if (sp.n == 0) {
+    if (threadIdx.x == 0) {
+      accept_len[b] = 0;
+      bonus[b] = -1;
+    }
+    for (int k = threadIdx.x; k < N; k += blockDim.x)
+      path[static_cast<size_t>(b) * N + k] = k == 0 ? 0 : -1;
+    grid_dependents_launch();
+    return;
+  }
+  const size_t rb = static_cast<size_t>(sp.row0);
+  const int nt = sp.n;
   const double Td = temperature;
   const float inv_t = 1.f / temperature;
   int bad_parent = 0, bad_token = 0;
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    if (i >= nt) {
+      s_par[i] = -1;
+      s_draft[i] = -1;
+      continue;
+    }
     int p = parent[rb + i];
     const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
     if (!ok) { bad_parent = 1; p = -1; }
@@ -1063,7 +1086,7 @@ __global__ void __launch_bounds__(kSampleThreads, 1)
   // no memory; larger ones find row u's when the walk reaches it.
   const bool all_stats = N <= kPreStats;
   if (all_stats)
-    for (int k = warp; k < N; k += static_cast<int>(blockDim.x >> 5)) row_stats(k, &s_aM[k], &s_aZ[k]);
+    for (int k = warp; k < nt; k += static_cast<int>(blockDim.x >> 5)) row_stats(k, &s_aM[k], &s_aZ[k]);
   __syncthreads();
   for (;;) {
     if (all_stats) {
@@ -1257,20 +1280,24 @@ __global__ void __launch_bounds__(kSampleThreads, 1)
     accept_len[b] = n;
     bonus[b] = s_y;
   }
-  for (int k = threadIdx.x; k < N; k += blockDim.x) path[rb + k] = k <= n ? s_path[k] : -1;
+  for (int k = threadIdx.x; k < N; k += blockDim.x)
+    path[static_cast<size_t>(b) * N + k] = k <= n ? s_path[k] : -1;
   grid_dependents_launch();
 }
 
 }  // namespace
 }  // namespace jf
 
-extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, const int32_t* draft,
-                                            const int32_t* parent, const float* uniform,
-                                            const float* bonus_uniform, float temperature,
-                                            int32_t B, int32_t N, int32_t V, int32_t* accept_len,
-                                            int32_t* path, int32_t* bonus, void* workspace,
-                                            size_t workspace_bytes, int32_t* dev_err,
-                                            jf_stream_t stream) {
+namespace {
+
+// Packed calls (cu != nullptr) hold T = cu[B] logit rows; the others B * N.
+jf_status tree_verify_sampled_call(const void* logits, int32_t dtype, const int32_t* draft,
+                                   const int32_t* parent, const float* uniform,
+                                   const float* bonus_uniform, float temperature, int32_t B,
+                                   int32_t N, int32_t V, int32_t* accept_len, int32_t* path,
+                                   int32_t* bonus, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_err, jf_stream_t stream, const int32_t* tree_len,
+                                   const int32_t* cu, int32_t T) {
   if (logits == nullptr || draft == nullptr || parent == nullptr || uniform == nullptr ||
       bonus_uniform == nullptr || accept_len == nullptr || path == nullptr || bonus == nullptr ||
       workspace == nullptr)
@@ -1278,17 +1305,19 @@ extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, c
   if (dtype != JF_DTYPE_BF16 && dtype != JF_DTYPE_F32) return JF_ERR_INVALID_ARGUMENT;
   if (B < 1 || N < 1 || V < 1 || !(temperature > 0.f) || !std::isfinite(temperature))
     return JF_ERR_INVALID_ARGUMENT;
+  if (cu != nullptr && T < 1) return JF_ERR_INVALID_ARGUMENT;
   if (N > JF_MAX_NODES) return JF_ERR_UNSUPPORTED;
+  const long long rows = cu != nullptr ? static_cast<long long>(T) : static_cast<long long>(B) * N;
   jf::VerifyPlan p;
   p.chunk_len = jf::kSampleChunk;
   p.chunks = jf::sampled_chunks(V);
-  const size_t need = static_cast<size_t>(B) * N * p.chunks * sizeof(float2);
+  const size_t need = static_cast<size_t>(rows) * p.chunks * sizeof(float2);
   if (workspace_bytes < need) return JF_ERR_WORKSPACE_TOO_SMALL;
   if (!jf::aligned_to(workspace, 8)) return JF_ERR_MISALIGNED;
   if (!jf::aligned_to(logits, dtype == JF_DTYPE_BF16 ? 2 : 4)) return JF_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float2* stats = static_cast<float2*>(workspace);
-  const long long total = static_cast<long long>(B) * N * p.chunks;     // one warp each
+  const long long total = rows * p.chunks;                              // one warp each
   const int sms = jf::current_sm_count() > 0 ? jf::current_sm_count() : 148;
   int warps = jf::kSampleThreads / 32;
   while (warps > 1 && total < static_cast<long long>(warps) * 4 * sms) warps >>= 1;
@@ -1315,11 +1344,49 @@ extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, c
       return cudaErrorInvalidValue;
     return jf::launch_pdl(kern, dim3(B), dim3(jf::kSampleThreads), smem, s, lg,
                           static_cast<const float2*>(stats), p.chunks, p.chunk_len, draft, parent,
-                          uniform, bonus_uniform, temperature, N, Vl, accept_len, path, bonus, dev_err);
+                          uniform, bonus_uniform, temperature, N, Vl, accept_len, path, bonus, dev_err,
+                          tree_len, cu, static_cast<long long>(cu != nullptr ? T : 0));
   };
   const cudaError_t ew =
       dtype == JF_DTYPE_BF16
           ? walk(jf::sampled_walk_kernel<uint16_t>, static_cast<const uint16_t*>(logits))
           : walk(jf::sampled_walk_kernel<float>, static_cast<const float*>(logits));
   return ew == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" jf_status jf_tree_verify_sampled(const void* logits, int32_t dtype, const int32_t* draft,
+                                            const int32_t* parent, const float* uniform,
+                                            const float* bonus_uniform, float temperature,
+                                            int32_t B, int32_t N, int32_t V, int32_t* accept_len,
+                                            int32_t* path, int32_t* bonus, void* workspace,
+                                            size_t workspace_bytes, int32_t* dev_err,
+                                            jf_stream_t stream) {
+  return tree_verify_sampled_call(logits, dtype, draft, parent, uniform, bonus_uniform,
+                                  temperature, B, N, V, accept_len, path, bonus, workspace,
+                                  workspace_bytes, dev_err, stream, nullptr, nullptr, 0);
+}
+
+extern "C" jf_status jf_tree_verify_sampled_ragged(
+    const void* logits, int32_t dtype, const int32_t* draft, const int32_t* parent,
+    const int32_t* tree_len, const float* uniform, const float* bonus_uniform, float temperature,
+    int32_t B, int32_t N, int32_t V, int32_t* accept_len, int32_t* path, int32_t* bonus,
+    void* workspace, size_t workspace_bytes, int32_t* dev_err, jf_stream_t stream) {
+  if (tree_len == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return tree_verify_sampled_call(logits, dtype, draft, parent, uniform, bonus_uniform,
+                                  temperature, B, N, V, accept_len, path, bonus, workspace,
+                                  workspace_bytes, dev_err, stream, tree_len, nullptr, 0);
+}
+
+extern "C" jf_status jf_tree_verify_sampled_packed(
+    const void* logits, int32_t dtype, const int32_t* draft, const int32_t* parent,
+    const int32_t* cu_seqlens, const float* uniform, const float* bonus_uniform,
+    float temperature, int32_t B, int32_t N_max, int32_t T, int32_t V, int32_t* accept_len,
+    int32_t* path, int32_t* bonus, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+    jf_stream_t stream) {
+  if (cu_seqlens == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return tree_verify_sampled_call(logits, dtype, draft, parent, uniform, bonus_uniform,
+                                  temperature, B, N_max, V, accept_len, path, bonus, workspace,
+                                  workspace_bytes, dev_err, stream, nullptr, cu_seqlens, T);
 }

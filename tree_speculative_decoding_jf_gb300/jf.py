@@ -92,6 +92,12 @@ def _load():
     lib.jf_tree_verify_packed.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz,
                                           P, P]
     lib.jf_tree_verify_packed.restype = ctypes.c_int
+    lib.jf_tree_verify_sampled_ragged.argtypes = [P, i32, P, P, P, P, P, f32, i32, i32, i32, P, P,
+                                                  P, P, sz, P, P]
+    lib.jf_tree_verify_sampled_ragged.restype = ctypes.c_int
+    lib.jf_tree_verify_sampled_packed.argtypes = [P, i32, P, P, P, P, P, f32, i32, i32, i32, i32,
+                                                  P, P, P, P, sz, P, P]
+    lib.jf_tree_verify_sampled_packed.restype = ctypes.c_int
     return lib
 
 
@@ -482,6 +488,62 @@ def jf_tree_verify_packed(logits, draft, parent, cu_seqlens, N_max, accept_len, 
         _ptr(logits), dt, _ptr(draft), _ptr(parent), _ptr(cu_seqlens), B, N_max, T, V,
         _ptr(argmax), _ptr(accept_len), _ptr(path), _ptr(bonus), _ptr(workspace), ws_bytes,
         _ptr(dev_err), _stream(stream)))
+
+
+def jf_tree_verify_sampled_ragged(logits, draft, parent, tree_len, uniform, bonus_uniform,
+                                  temperature, accept_len, path, bonus, workspace, dev_err=None,
+                                  stream=None) -> None:
+    """Lossless verification with per-sequence tree sizes (padded [B][N] arrays, tree_len
+    int32 [B]); the workspace is sized by jf_tree_verify_workspace_size."""
+    B, N, V = logits.shape
+    dt = _logit_dtype(logits)
+    _need(logits, "logits", logits.dtype)
+    for name, t, shape in (("draft", draft, (B, N)), ("parent", parent, (B, N)),
+                           ("tree_len", tree_len, (B,)), ("accept_len", accept_len, (B,)),
+                           ("path", path, (B, N)), ("bonus", bonus, (B,))):
+        _need(t, name, torch.int32, shape)
+    _need(uniform, "uniform", torch.float32, (B, N))
+    _need(bonus_uniform, "bonus_uniform", torch.float32, (B,))
+    _need(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_tree_verify_sampled_ragged", _lib.jf_tree_verify_sampled_ragged(
+        _ptr(logits), dt, _ptr(draft), _ptr(parent), _ptr(tree_len), _ptr(uniform),
+        _ptr(bonus_uniform), float(temperature), B, N, V, _ptr(accept_len), _ptr(path),
+        _ptr(bonus), _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream(stream)))
+
+
+def jf_tree_verify_sampled_packed(logits, draft, parent, cu_seqlens, N_max, uniform,
+                                  bonus_uniform, temperature, accept_len, path, bonus, workspace,
+                                  dev_err=None, stream=None) -> None:
+    """Lossless verification of packed trees: logits [T][V], draft/parent int32 [T], uniform
+    float32 [T], path int32 [B][N_max]; the workspace is sized by
+    jf_tree_verify_packed_workspace_size(T, V)."""
+    T, V = logits.shape
+    B = cu_seqlens.shape[0] - 1
+    dt = _logit_dtype(logits)
+    _need(logits, "logits", logits.dtype)
+    for name, t, shape in (("draft", draft, (T,)), ("parent", parent, (T,)),
+                           ("cu_seqlens", cu_seqlens, (B + 1,)), ("accept_len", accept_len, (B,)),
+                           ("path", path, (B, N_max)), ("bonus", bonus, (B,))):
+        _need(t, name, torch.int32, shape)
+    _need(uniform, "uniform", torch.float32, (T,))
+    _need(bonus_uniform, "bonus_uniform", torch.float32, (B,))
+    _need(workspace, "workspace", torch.uint8)
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_tree_verify_sampled_packed", _lib.jf_tree_verify_sampled_packed(
+        _ptr(logits), dt, _ptr(draft), _ptr(parent), _ptr(cu_seqlens), _ptr(uniform),
+        _ptr(bonus_uniform), float(temperature), B, N_max, T, V, _ptr(accept_len), _ptr(path),
+        _ptr(bonus), _ptr(workspace), workspace.numel(), _ptr(dev_err), _stream(stream)))
+
+
+def _logit_dtype(logits) -> int:
+    if logits.dtype == torch.bfloat16:
+        return JF_DTYPE_BF16
+    if logits.dtype == torch.float32:
+        return JF_DTYPE_F32
+    raise TypeError("logits must be bfloat16 or float32")
 
 
 def jf_compact_accepted_kv(k_cache, v_cache, block_table, prefix_len, path, accept_len,
