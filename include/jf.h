@@ -452,6 +452,22 @@ jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype, const int
                               int32_t* cand_token, float* cand_logp, int32_t* parent,
                               int32_t* draft, int32_t* depth, float* score, jf_stream_t stream);
 
+/*
+ * jf_build_draft_tree_ragged -- the same with a budget per sequence (the best budget depends
+ * on the load, explainer §4): budget int32 [B] (device), each clamped to [1, N]
+ * (JF_DEVERR_BAD_TREE_LEN in *dev_err, which may be NULL, when one is outside).  Sequence
+ * b's tree is the best-first tree of budget[b] nodes, nodes 0 .. budget[b] - 1 of the
+ * [B][N] outputs (equal to what jf_build_draft_tree gives with N = budget[b]); the
+ * remaining entries are padding (parent = draft = depth = -1, score = -inf), so budget
+ * serves as tree_len for the _ragged calls.  Limits as jf_build_draft_tree.
+ */
+jf_status jf_build_draft_tree_ragged(const void* draft_logits, int32_t dtype,
+                                     const int32_t* root_token, const int32_t* budget, int32_t B,
+                                     int32_t Dmax, int32_t V, int32_t K, int32_t N,
+                                     int32_t* cand_token, float* cand_logp, int32_t* parent,
+                                     int32_t* draft, int32_t* depth, float* score,
+                                     int32_t* dev_err, jf_stream_t stream);
+
 /* ---------------------------------------------------------------- after verification
  * jf_compact_accepted_kv -- moves the K/V of the accepted draft path next to the prefix,
  * so the next decoding step continues from one contiguous context.  JetFlow explainer

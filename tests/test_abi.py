@@ -182,3 +182,14 @@ def test_sampled_ragged_and_packed_calls_validate_host_arguments_without_gpu(lib
                                              100, fake, fake, fake, fake, 1 << 20, None, None) == 1
     assert lib.jf_tree_verify_sampled_packed(fake, 0, fake, fake, fake, fake, fake, 0.0, 2, 8, 10,
                                              100, fake, fake, fake, fake, 1 << 20, None, None) == 1
+
+
+def test_ragged_draft_tree_needs_budgets(lib):
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    fake = ctypes.c_void_p(0x10000)      # never dereferenced: the call fails early
+    lib.jf_build_draft_tree_ragged.argtypes = [P, i32, P, P, i32, i32, i32, i32, i32, P, P, P, P,
+                                               P, P, P, P]
+    assert lib.jf_build_draft_tree_ragged(fake, 0, None, None, 2, 4, 100, 4, 16, fake, fake, fake,
+                                          fake, fake, None, None, None) == 1
+    assert lib.jf_build_draft_tree_ragged(fake, 0, None, fake, 2, 2, 100, 2, 16, fake, fake, fake,
+                                          fake, fake, None, None, None) == 3   # lattice 7 < 16

@@ -199,3 +199,44 @@ def test_lattice_smaller_than_budget_is_rejected(jf):
     x = torch.zeros((1, 2, 10), dtype=torch.float32, device="cuda")
     with pytest.raises(RuntimeError):
         jf.build_draft_tree(x, 2, 8)                 # 1 + 2 + 4 = 7 < 8 nodes
+
+
+@pytest.mark.parametrize("B,Dmax,V,K,N,dtype", [(4, 16, 32000, 8, 64, "bf16"),
+                                                 (6, 12, 151936, 8, 256, "bf16"),
+                                                 (3, 5, 1000, 4, 40, "f32")])
+def test_ragged_budgets_are_prefixes_of_the_full_tree(jf, B, Dmax, V, K, N, dtype):
+    """Best-first expansion pops nodes in an order that does not depend on the budget, so
+    the tree of budget n is the first n nodes of the tree of budget N: with per-sequence
+    budgets, sequence b's nodes 0 .. n_b - 1 must equal the fixed-size call's bit for bit
+    (same candidates: same call shape) and the rest be padding.  Budgets outside [1, N]
+    are reported and clamped."""
+    rng = np.random.default_rng(B * 100 + N)
+    logits = wl.draft_logits(B, Dmax, V, seed=N + V % 13, dtype=dtype)
+    t = (torch.from_numpy(np.ascontiguousarray(logits).view(np.int16)).view(torch.bfloat16)
+         if dtype == "bf16" else torch.from_numpy(np.ascontiguousarray(logits, np.float32))).cuda()
+    rt = torch.from_numpy(rng.integers(0, V, B).astype(np.int32)).cuda()
+    full = jf.build_draft_tree(t, K, N, root_token=rt)
+    budgets = rng.integers(1, N + 1, B).astype(np.int32)
+    budgets[0], budgets[-1] = 0, N + 5                   # out of range: clamped to 1 and N
+    want = np.clip(budgets, 1, N)
+    out = dict(cand_token=torch.empty((B, Dmax, K), dtype=torch.int32, device="cuda"),
+               cand_logp=torch.empty((B, Dmax, K), dtype=torch.float32, device="cuda"),
+               parent=torch.full((B, N), 7, dtype=torch.int32, device="cuda"),
+               draft=torch.full((B, N), 7, dtype=torch.int32, device="cuda"),
+               depth=torch.full((B, N), 7, dtype=torch.int32, device="cuda"),
+               score=torch.zeros((B, N), dtype=torch.float32, device="cuda"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    jf.jf_build_draft_tree_ragged(t, K, N, torch.from_numpy(budgets).cuda(), out["cand_token"],
+                                  out["cand_logp"], out["parent"], out["draft"], out["depth"],
+                                  root_token=rt, score=out["score"], dev_err=err)
+    torch.cuda.synchronize()
+    assert err.item() == jf.DEVERR_BAD_TREE_LEN
+    f_par, f_dr, f_dep, f_sc, f_tok, f_lp = [x.cpu().numpy() for x in full]
+    g = {k: v.cpu().numpy() for k, v in out.items()}
+    assert (g["cand_token"] == f_tok).all() and (g["cand_logp"] == f_lp).all()
+    for b, n in enumerate(want):
+        assert (g["parent"][b, :n] == f_par[b, :n]).all(), b
+        assert (g["draft"][b, :n] == f_dr[b, :n]).all() and (g["depth"][b, :n] == f_dep[b, :n]).all()
+        assert (g["score"][b, :n] == f_sc[b, :n]).all()
+        assert (g["parent"][b, n:] == -1).all() and (g["draft"][b, n:] == -1).all()
+        assert (g["depth"][b, n:] == -1).all() and np.isneginf(g["score"][b, n:]).all()

@@ -461,7 +461,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     best_first_tree_kernel(const int32_t* __restrict__ cand_token, const float* __restrict__ cand_logp,
                            const int32_t* __restrict__ root_token, int Dmax, int K, int N,
                            int32_t* __restrict__ parent, int32_t* __restrict__ draft,
-                           int32_t* __restrict__ depth_out, float* __restrict__ score_out) {
+                           int32_t* __restrict__ depth_out, float* __restrict__ score_out,
+                           const int32_t* __restrict__ budget, int32_t* dev_err) {
   // The chosen set G (at most N keys, in key order) and its successor, double-buffered;
   // this level's candidates C (at most N * kMaxK slots) and the merge's scratch.
   extern __shared__ uint64_t s_keys[];
@@ -479,6 +480,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   grid_dependency_wait();
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // This sequence's budget: N, or budget[b] clamped to [1, N] (per-sequence budgets).
+  int Nb = N;
+  if (budget != nullptr) {
+    const int raw = budget[b];
+    Nb = max(1, min(raw, N));
+    if (raw != Nb && threadIdx.x == 0) report(dev_err, JF_DEVERR_BAD_TREE_LEN);
+  }
   for (int e = threadIdx.x; e < Dmax * K; e += blockDim.x) {
     s_lp[e] = cand_logp[static_cast<size_t>(b) * Dmax * K + e];
     s_tok[e] = cand_token[static_cast<size_t>(b) * Dmax * K + e];
@@ -495,8 +503,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     // a child only matters if it beats G's last; a parent's children fall in score with
     // their rank, so those form a prefix of its K children.  Slot f's count is found by
     // thread f and scanned per warp and across the (at most 8) warps.
-    const bool full = nG == N;
-    const uint64_t thr_hi = full ? g_hi[N - 1] : ~0ull, thr_lo = full ? g_lo[N - 1] : ~0ull;
+    const bool full = nG == Nb;
+    const uint64_t thr_hi = full ? g_hi[Nb - 1] : ~0ull, thr_lo = full ? g_lo[Nb - 1] : ~0ull;
     const int f = threadIdx.x;
     int cnt = 0;
     float ps = 0.f;
@@ -581,7 +589,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
     // The next G is the first N keys of G + C: a key's place is the number of keys below
     // it, its index in its own sorted set plus the other set's keys below it (counted
     // one by one when C is small and unsorted).
-    const int total = nG + nC, keep = min(N, total);
+    const int total = nG + nC, keep = min(Nb, total);
     int kept_d = 0;
     for (int e = threadIdx.x; e < total; e += blockDim.x) {
       const bool in_g = e < nG;
@@ -610,7 +618,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
   // G in key order is the tree in pop order: node id = slot
   for (int i = threadIdx.x; i < N; i += blockDim.x) {
     const size_t o = static_cast<size_t>(b) * N + i;
-    if (i >= nG) {                          // lattice smaller than N (rejected on the host)
+    if (i >= nG) {                          // past the sequence's budget: padding
       parent[o] = -1; draft[o] = -1; depth_out[o] = -1;
       if (score_out != nullptr) score_out[o] = -INFINITY;
       continue;
@@ -637,11 +645,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1)
 }  // namespace
 }  // namespace jf
 
-extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype,
-                                         const int32_t* root_token, int32_t B, int32_t Dmax,
-                                         int32_t V, int32_t K, int32_t N, int32_t* cand_token,
-                                         float* cand_logp, int32_t* parent, int32_t* draft,
-                                         int32_t* depth, float* score, jf_stream_t stream) {
+namespace {
+
+jf_status build_draft_tree_call(const void* draft_logits, int32_t dtype, const int32_t* root_token,
+                                int32_t B, int32_t Dmax, int32_t V, int32_t K, int32_t N,
+                                int32_t* cand_token, float* cand_logp, int32_t* parent,
+                                int32_t* draft, int32_t* depth, float* score,
+                                const int32_t* budget, int32_t* dev_err, jf_stream_t stream) {
   if (draft_logits == nullptr || cand_token == nullptr || cand_logp == nullptr || parent == nullptr ||
       draft == nullptr || depth == nullptr)
     return JF_ERR_INVALID_ARGUMENT;
@@ -708,6 +718,29 @@ extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype
   }
   e = jf::launch_pdl(jf::best_first_tree_kernel, dim3(static_cast<unsigned>(B)), dim3(jf::kTreeThreads), kTreeSmem, s,
                      static_cast<const int32_t*>(cand_token), static_cast<const float*>(cand_logp),
-                     root_token, Dmax, K, N, parent, draft, depth, score);
+                     root_token, Dmax, K, N, parent, draft, depth, score, budget, dev_err);
   return e == cudaSuccess ? JF_OK : JF_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" jf_status jf_build_draft_tree(const void* draft_logits, int32_t dtype,
+                                         const int32_t* root_token, int32_t B, int32_t Dmax,
+                                         int32_t V, int32_t K, int32_t N, int32_t* cand_token,
+                                         float* cand_logp, int32_t* parent, int32_t* draft,
+                                         int32_t* depth, float* score, jf_stream_t stream) {
+  return build_draft_tree_call(draft_logits, dtype, root_token, B, Dmax, V, K, N, cand_token,
+                               cand_logp, parent, draft, depth, score, nullptr, nullptr, stream);
+}
+
+extern "C" jf_status jf_build_draft_tree_ragged(const void* draft_logits, int32_t dtype,
+                                                const int32_t* root_token, const int32_t* budget,
+                                                int32_t B, int32_t Dmax, int32_t V, int32_t K,
+                                                int32_t N, int32_t* cand_token, float* cand_logp,
+                                                int32_t* parent, int32_t* draft, int32_t* depth,
+                                                float* score, int32_t* dev_err,
+                                                jf_stream_t stream) {
+  if (budget == nullptr) return JF_ERR_INVALID_ARGUMENT;
+  return build_draft_tree_call(draft_logits, dtype, root_token, B, Dmax, V, K, N, cand_token,
+                               cand_logp, parent, draft, depth, score, budget, dev_err, stream);
 }

@@ -62,6 +62,9 @@ def _load():
                                            P, P, P]
     lib.jf_compact_accepted_kv.restype = ctypes.c_int
     lib.jf_build_draft_tree.argtypes = [P, i32, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+    lib.jf_build_draft_tree_ragged.argtypes = [P, i32, P, P, i32, i32, i32, i32, i32, P, P, P, P,
+                                               P, P, P, P]
+    lib.jf_build_draft_tree_ragged.restype = ctypes.c_int
     lib.jf_build_draft_tree.restype = ctypes.c_int
     lib.jf_build_tree_mask_ragged.argtypes = [P, P, P, i32, i32, P, P, P, P, P]
     lib.jf_build_tree_mask_ragged.restype = ctypes.c_int
@@ -588,6 +591,31 @@ def jf_build_draft_tree(draft_logits, K, N, cand_token, cand_logp, parent, draft
     _check("jf_build_draft_tree", _lib.jf_build_draft_tree(
         _ptr(draft_logits), dt, _ptr(root_token), B, Dmax, V, K, N, _ptr(cand_token),
         _ptr(cand_logp), _ptr(parent), _ptr(draft), _ptr(depth), _ptr(score), _stream(stream)))
+
+
+def jf_build_draft_tree_ragged(draft_logits, K, N, budget, cand_token, cand_logp, parent, draft,
+                               depth, root_token=None, score=None, dev_err=None,
+                               stream=None) -> None:
+    """Best-first draft trees with a budget per sequence (budget int32 [B], clamped to
+    [1, N]); entries past a sequence's budget are padding (see include/jf.h)."""
+    B, Dmax, V = draft_logits.shape
+    dt = _logit_dtype(draft_logits)
+    _need(draft_logits, "draft_logits", draft_logits.dtype)
+    _need(budget, "budget", torch.int32, (B,))
+    _need(cand_token, "cand_token", torch.int32, (B, Dmax, K))
+    _need(cand_logp, "cand_logp", torch.float32, (B, Dmax, K))
+    for name, t in (("parent", parent), ("draft", draft), ("depth", depth)):
+        _need(t, name, torch.int32, (B, N))
+    if score is not None:
+        _need(score, "score", torch.float32, (B, N))
+    if root_token is not None:
+        _need(root_token, "root_token", torch.int32, (B,))
+    if dev_err is not None:
+        _need(dev_err, "dev_err", torch.int32, (1,))
+    _check("jf_build_draft_tree_ragged", _lib.jf_build_draft_tree_ragged(
+        _ptr(draft_logits), dt, _ptr(root_token), _ptr(budget), B, Dmax, V, K, N,
+        _ptr(cand_token), _ptr(cand_logp), _ptr(parent), _ptr(draft), _ptr(depth), _ptr(score),
+        _ptr(dev_err), _stream(stream)))
 
 
 # ----------------------------------------------------------------------------- conveniences
