@@ -244,7 +244,8 @@ jf_status jf_tree_verify_shard_keys(const void* logits_shard, int32_t dtype, int
                                     int32_t chunks, uint64_t* keys, jf_stream_t stream);
 
 /*
- * jf_tree_verify_from_keys -- the walk of jf_tree_verify on gathered keys.
+ * jf_tree_verify_from_keys -- the walk of jf_tree_verify on gathered keys (fixed-size
+ * trees: every sequence has N nodes).
  *   keys       uint64 [S][B*N][chunks], device: every range's jf_tree_verify_shard_keys
  *              output.  argmax[b][i] = the token id of the largest key of row b*N + i;
  *              the ranges together must cover the vocabulary [0, V).
