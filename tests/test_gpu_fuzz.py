@@ -223,3 +223,65 @@ def test_sharded_verify_random_shapes(jf, case):
     assert (am.cpu().numpy() == ram).all()
     assert (acc.cpu().numpy() == racc).all() and (path.cpu().numpy() == rpath).all()
     assert (bonus.cpu().numpy() == rbonus).all()
+
+
+# ----------------------------------------------------------------------------- ragged lossless verify
+
+N_SAMPLED_RAGGED = 8 * SCALE
+
+
+@pytest.mark.parametrize("case", range(N_SAMPLED_RAGGED))
+def test_sampled_ragged_and_packed_random_shapes(jf, case):
+    """Lossless verification with random tree sizes: the ragged and packed calls give each
+    sequence what the fixed-size call gives on its slice, bit for bit."""
+    rng = np.random.default_rng(8800 + case)
+    V = int(rng.choice([50, 1000, 8193, 32001, 151936]))
+    N = int(rng.choice([1, 5, 16, 40, 64, 100]))
+    B = int(rng.choice([1, 2, 3, 6]))
+    T = float(rng.choice([0.5, 1.0, 1.5]))
+    while B * N * V > 30_000_000:
+        if B > 1:
+            B //= 2
+        else:
+            N = max(1, N // 2)
+    dtype = str(rng.choice(["bf16", "f32"]))
+    width = int(rng.integers(1, 8))
+    parent = np.stack([np.array([-1] + [rng.integers(max(0, i - width), i) for i in range(1, N)],
+                                np.int32) for _ in range(B)])
+    w = wl.make_workload(f"srf{case}", B, N, 1, 1, 64, V, 8, tree="chain", parent=parent,
+                         logits_dtype=dtype, forcing="half", seed=880 + case)
+    tree_len = rng.integers(1, N + 1, B)
+    u, bu = wl.sampling_uniforms(B, N, case)
+    draft, par = w.draft.copy(), w.parent.copy()
+    for b, n in enumerate(tree_len):
+        draft[b, n:] = -1
+        par[b, n:] = -7
+    to_dev = (lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()) \
+        if dtype == "bf16" else (lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda())
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    path = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    bonus = torch.empty(B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(jf.jf_tree_verify_workspace_size(B, N, V), dtype=torch.uint8, device="cuda")
+    jf.jf_tree_verify_sampled_ragged(to_dev(w.logits), dev(draft), dev(par),
+                                     dev(tree_len.astype(np.int32)), dev(u), dev(bu), T, acc,
+                                     path, bonus, ws, err)
+    cu = np.concatenate([[0], np.cumsum(tree_len)]).astype(np.int32)
+    Tn = int(cu[-1])
+    pk = lambda a: np.ascontiguousarray(np.concatenate([a[b, :n] for b, n in enumerate(tree_len)]))  # noqa: E731
+    acc_p, path_p, bonus_p = torch.empty_like(acc), torch.empty_like(path), torch.empty_like(bonus)
+    ws_p = torch.empty(jf.jf_tree_verify_packed_workspace_size(Tn, V), dtype=torch.uint8,
+                       device="cuda")
+    jf.jf_tree_verify_sampled_packed(to_dev(pk(w.logits)), dev(pk(draft)), dev(pk(par)), dev(cu),
+                                     N, dev(pk(u)), dev(bu), T, acc_p, path_p, bonus_p, ws_p, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(acc, acc_p) and torch.equal(path, path_p) and torch.equal(bonus, bonus_p)
+    acc, path, bonus = acc.cpu().numpy(), path.cpu().numpy(), bonus.cpu().numpy()
+    for b, n in enumerate(tree_len):
+        r_acc, r_path, r_bonus = jf.tree_verify_sampled(
+            to_dev(w.logits[b:b + 1, :n]), dev(draft[b:b + 1, :n]), dev(par[b:b + 1, :n]),
+            dev(u[b:b + 1, :n]), dev(bu[b:b + 1]), T)
+        assert acc[b] == r_acc.item() and bonus[b] == r_bonus.item(), b
+        assert (path[b, :n] == r_path.cpu().numpy()[0]).all() and (path[b, n:] == -1).all()
