@@ -5,7 +5,9 @@ Each step: ragged draft trees (a seeded tree and budget per sequence), their que
 keys/values written at positions P_b .. P_b + N - 1 of the paged pool (the target
 forward pass's stand-in, the same values on both sides), then mask, attention and greedy
 verification on the GPU, and the accepted path's K/V compacted next to the prefix; the
-next step starts from the compacted pool and the new prefix lengths.  The oracle runs mask,
+next step starts from the compacted pool and the new prefix lengths, which on the GPU side
+stay on the device (the compaction's output is the next mask and attention calls' input,
+with no host round trip between the steps).  The oracle runs mask,
 attention rows, argmax, walk and compaction on its own copy of the state: masks, accepted
 lengths, paths, bonus tokens, new prefix lengths and the whole pool must agree bit for bit
 after every step, attention rows within 2e-3 + 1e-2 |ref|.  Nothing the GPU computes feeds
@@ -49,6 +51,7 @@ def test_decode_loop_matches_oracle(jf, G, D):
     v_gpu = torch.from_numpy(v_np.view(np.int16)).view(torch.bfloat16).cuda()
     bt_gpu = torch.from_numpy(bt).cuda()
     P = P0.copy()
+    P_dev = torch.from_numpy(P0).cuda()        # the GPU side keeps its prefix lengths on device
     total_accepted = 0
     for step in range(steps):
         tree_len = rng.integers(1, N + 1, B)
@@ -82,7 +85,7 @@ def test_decode_loop_matches_oracle(jf, G, D):
         # ---- GPU
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         tl = torch.from_numpy(tree_len.astype(np.int32)).cuda()
-        t_par, t_P = torch.from_numpy(parent).cuda(), torch.from_numpy(P).cuda()
+        t_par, t_P = torch.from_numpy(parent).cuda(), P_dev
         mask, depth, pos = jf.build_tree_mask(t_par, t_P, dev_err=err, tree_len=tl)
         out, lse = jf.tree_attention(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda(),
                                      k_gpu, v_gpu, bt_gpu, t_P, mask, scale=w.scale, with_lse=True,
@@ -116,6 +119,7 @@ def test_decode_loop_matches_oracle(jf, G, D):
         assert (k_gpu.view(torch.int16).cpu().numpy().view(np.uint16) == rk).all(), step
         assert (v_gpu.view(torch.int16).cpu().numpy().view(np.uint16) == rv).all(), step
         k_np, v_np, P = rk, rv, rnewp.astype(np.int32)
+        P_dev = newp                            # compaction -> next step, no host round trip
         total_accepted += int(r_acc.sum())
     assert total_accepted >= steps * B          # the loop really moved the prefixes
     assert (P > P0).all()
