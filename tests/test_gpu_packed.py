@@ -111,10 +111,11 @@ def test_packed_tiles_cross_sequence_boundaries(jf):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_packed_verify_equals_ragged_and_oracle(jf, dtype):
-    B, N, V = 6, 40, 3001
+@pytest.mark.parametrize("V", [3001, 151936])      # one chunk per row, or several
+def test_packed_verify_equals_ragged_and_oracle(jf, dtype, V):
+    B, N = 6, 40
     w = wl.make_workload("pv", B, N, 4, 1, 64, V, 128, tree="random_depth_limited",
-                         logits_dtype=dtype, forcing="half", seed=31)
+                         logits_dtype=dtype, forcing="half", seed=31 + V % 7)
     tree_len = [1, 2, 17, 39, 40, 23]
     lg = w.logits.reshape(B, N, V)
     am = oracle.argmax(lg, dtype).reshape(B, N)
